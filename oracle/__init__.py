@@ -1,0 +1,246 @@
+"""CPU oracle for MXFP8 quantization and the block-scaled grouped GEMM.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py``.  The
+product package never imports it and shares no code with it.
+
+The arithmetic lives in ``mxfp8_oracle.c`` (plain C, fp64); this module builds
+it with gcc, loads it with ctypes and wraps it for numpy arrays.  bf16 tensors
+are passed as their uint16 bit patterns.  See the C file's header for the
+sources and for which functions are pinned by which tests.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mxfp8_oracle.c")
+_LIB = os.path.join(_HERE, "libmxfp8_oracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP when available, never fast-math)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", _LIB, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_f64.restype = ctypes.c_double
+        L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_f64.restype = ctypes.c_double
+        L.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_e8m0_to_f64.restype = ctypes.c_double
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e8m0_from_amax.argtypes = [ctypes.c_double]
+        L.oracle_e8m0_from_amax.restype = ctypes.c_uint8
+        L.oracle_quantize_vec.argtypes = [P, I64, I64, P, P]
+        L.oracle_quantize_rows.argtypes = [P, I64, I64, P, P]
+        L.oracle_quantize_cols.argtypes = [P, I64, I64, P, P]
+        L.oracle_quantize_32x32.argtypes = [P, I64, I64, P, P]
+        L.oracle_blocked_offset.argtypes = [I64, I64, I64]
+        L.oracle_blocked_offset.restype = I64
+        L.oracle_blocked_rowgroups.argtypes = [P, I64, I64, P, I64, P]
+        L.oracle_blocked_rowgroups.restype = I64
+        L.oracle_blocked_colgroups.argtypes = [P, I64, I64, P, I64, P]
+        L.oracle_blocked_colgroups.restype = I64
+        L.oracle_dot.argtypes = [P, P, P, P, I64]
+        L.oracle_dot.restype = ctypes.c_double
+        L.oracle_grouped_mm_rows.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P]
+        L.oracle_grouped_mm_wgrad.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P]
+        L.oracle_num_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    assert x.dtype == np.uint16, "bf16 inputs are passed as uint16 bit patterns"
+    return x
+
+
+def num_threads() -> int:
+    return lib().oracle_num_threads()
+
+
+# ---------------------------------------------------------------- scalars
+def bf16_to_f64(b: int) -> float:
+    return lib().oracle_bf16_to_f64(int(b))
+
+
+def e4m3_to_f64(q: int) -> float:
+    return lib().oracle_e4m3_to_f64(int(q))
+
+
+def e8m0_to_f64(s: int) -> float:
+    return lib().oracle_e8m0_to_f64(int(s))
+
+
+def e4m3_encode(y: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(y)))
+
+
+def e8m0_from_amax(amax: float) -> int:
+    return int(lib().oracle_e8m0_from_amax(float(amax)))
+
+
+def e4m3_table() -> np.ndarray:
+    """fp64 value of every E4M3 code 0..255 (NaN for the two NaN codes)."""
+    return np.array([e4m3_to_f64(c) for c in range(256)], dtype=np.float64)
+
+
+def dequant(q: np.ndarray, s_expanded: np.ndarray) -> np.ndarray:
+    """deq(q, s) = E4M3(q) * 2^(s-127), elementwise (s already broadcast to q's shape)."""
+    tab = e4m3_table()
+    sv = np.ldexp(1.0, s_expanded.astype(np.int64) - 127)
+    return tab[q] * sv
+
+
+# ---------------------------------------------------------------- quantize
+def quantize_vec(x_u16: np.ndarray):
+    x = _u16(x_u16).reshape(-1)
+    n = x.size
+    assert n % 32 == 0
+    q = np.empty(n, np.uint8)
+    s = np.empty(n // 32, np.uint8)
+    lib().oracle_quantize_vec(_p(x), n, 1, _p(q), _p(s))
+    return q, s
+
+
+def quantize_rows(x_u16: np.ndarray):
+    """Blocks of 32 along the last dim of x[R, C] -> q[R, C], compact s[R, C/32]."""
+    x = _u16(x_u16)
+    R, C = x.shape
+    assert C % 32 == 0
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R, C // 32), np.uint8)
+    lib().oracle_quantize_rows(_p(x), R, C, _p(q), _p(s))
+    return q, s
+
+
+def quantize_cols(x_u16: np.ndarray):
+    """Blocks of 32 along the first dim of x[R, C] -> qT[C, R], compact sT[C, R/32]."""
+    x = _u16(x_u16)
+    R, C = x.shape
+    assert R % 32 == 0
+    qT = np.empty((C, R), np.uint8)
+    sT = np.empty((C, R // 32), np.uint8)
+    lib().oracle_quantize_cols(_p(x), R, C, _p(qT), _p(sT))
+    return qT, sT
+
+
+def quantize_32x32(x_u16: np.ndarray):
+    x = _u16(x_u16)
+    R, C = x.shape
+    assert R % 32 == 0 and C % 32 == 0
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R // 32, C // 32), np.uint8)
+    lib().oracle_quantize_32x32(_p(x), R, C, _p(q), _p(s))
+    return q, s
+
+
+# ---------------------------------------------------------------- layouts
+def blocked_offset(r: int, kb: int, kb_tiles: int) -> int:
+    return int(lib().oracle_blocked_offset(r, kb, kb_tiles))
+
+
+def _ends(ends) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(ends, dtype=np.int64))
+
+
+def blocked_rowgroups_bytes(ends, Kb: int) -> int:
+    e = _ends(ends)
+    sizes = np.diff(np.concatenate([[0], e]))
+    return int(sum(-(-int(m) // 128) * 128 for m in sizes) * (-(-Kb // 4)) * 4)
+
+
+def blocked_rowgroups(s: np.ndarray, ends) -> np.ndarray:
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    R, Kb = s.shape
+    e = _ends(ends)
+    out = np.empty(blocked_rowgroups_bytes(e, Kb), np.uint8)
+    n = lib().oracle_blocked_rowgroups(_p(s), R, Kb, _p(e), e.size, _p(out))
+    assert n == out.size
+    return out
+
+
+def blocked_colgroups_bytes(R: int, ends) -> int:
+    e = _ends(ends)
+    sizes = np.diff(np.concatenate([[0], e]))
+    return int(-(-R // 128) * 128 * sum(-(-int(m) // 128) * 4 for m in sizes))
+
+
+def blocked_colgroups(s: np.ndarray, ends) -> np.ndarray:
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    R, Mb = s.shape
+    e = _ends(ends)
+    out = np.empty(blocked_colgroups_bytes(R, e), np.uint8)
+    n = lib().oracle_blocked_colgroups(_p(s), R, Mb, _p(e), e.size, _p(out))
+    assert n == out.size
+    return out
+
+
+# ---------------------------------------------------------------- GEMMs
+def dot(a, sa, b, sb) -> float:
+    a = np.ascontiguousarray(a, np.uint8)
+    b = np.ascontiguousarray(b, np.uint8)
+    sa = np.ascontiguousarray(sa, np.uint8)
+    sb = np.ascontiguousarray(sb, np.uint8)
+    assert a.size == b.size and a.size % 32 == 0
+    return float(lib().oracle_dot(_p(a), _p(sa), _p(b), _p(sb), a.size))
+
+
+def grouped_mm_rows(aq, as_, bq, bs, ends) -> np.ndarray:
+    """fwd / dgrad: out[m, n] = sum_k A[m,k] B_g[n,k] for m in group g (fp64 [M, Nb])."""
+    aq = np.ascontiguousarray(aq, np.uint8)
+    as_ = np.ascontiguousarray(as_, np.uint8)
+    bq = np.ascontiguousarray(bq, np.uint8)
+    bs = np.ascontiguousarray(bs, np.uint8)
+    M, K = aq.shape
+    G, Nb, K2 = bq.shape
+    assert K == K2
+    e = _ends(ends)
+    assert e.size == G and e[-1] == M
+    out = np.zeros((M, Nb), np.float64)
+    lib().oracle_grouped_mm_rows(_p(aq), _p(as_), _p(bq), _p(bs), _p(e), G, M, Nb, K, _p(out))
+    return out
+
+
+def grouped_mm_wgrad(dq, ds, aq, as_, ends) -> np.ndarray:
+    """wgrad: out[g][n, k] = sum_{m in g} dOut[m,n] A[m,k] (fp64 [G, N, K])."""
+    dq = np.ascontiguousarray(dq, np.uint8)
+    ds = np.ascontiguousarray(ds, np.uint8)
+    aq = np.ascontiguousarray(aq, np.uint8)
+    as_ = np.ascontiguousarray(as_, np.uint8)
+    N, M = dq.shape
+    K, M2 = aq.shape
+    assert M == M2
+    e = _ends(ends)
+    G = e.size
+    out = np.zeros((G, N, K), np.float64)
+    lib().oracle_grouped_mm_wgrad(_p(dq), _p(ds), _p(aq), _p(as_), _p(e), G, M, N, K, _p(out))
+    return out
