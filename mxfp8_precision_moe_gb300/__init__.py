@@ -1,0 +1,229 @@
+"""GB300 (sm_103a) MXFP8 routed-expert hot path: dynamic MXFP8 quantization and
+block-scaled grouped GEMMs, the computation behind
+``_to_mxfp8_then_scaled_grouped_mm`` ("MXFP8 training for MoEs", the engine
+paragraph: quantize activations and weights dynamically, run a scaled grouped
+GEMM, return the original precision, differentiable).
+
+This module is a thin binding over the C ABI in ``include/mxfp8moe.h``
+(``libmxfp8moe.so``): it allocates outputs with torch, passes raw device
+pointers and the current CUDA stream, and raises on any status other than
+MXFP8_OK.  Every step of the computation runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback.
+
+Tensors: bf16 inputs; e4m3 codes are returned as ``torch.uint8`` (view them as
+``torch.float8_e4m3fn`` if needed); E8M0 scales are ``torch.uint8``; group
+offsets are int32 cumulative end rows on the device.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import (BLOCK32X32, COL, MAX_GROUPS, ROW, SCALES_BLOCKED, SCALES_COMPACT, Mxfp8Error, check, load)
+
+__all__ = [
+    "ROW", "COL", "BLOCK32X32", "SCALES_COMPACT", "SCALES_BLOCKED", "MAX_GROUPS", "Mxfp8Error",
+    "mxfp8_quantize_2d", "mxfp8_quantize_3d_experts", "mxfp8_grouped_mm_fwd", "mxfp8_grouped_mm_dgrad",
+    "mxfp8_grouped_mm_wgrad", "mxfp8_scale_bytes", "mxfp8_scale_bytes_colgroups", "mxfp8_check_offsets",
+    "mxfp8_debug_wait_timeout", "new_status", "read_status", "to_mxfp8_then_scaled_grouped_mm", "load",
+]
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("mxfp8: every tensor must live on a CUDA device")
+            if not t.is_contiguous():
+                raise ValueError("mxfp8: tensors must be contiguous")
+
+
+def _u8(shape, device):
+    return torch.empty(shape, dtype=torch.uint8, device=device)
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed int32 device word for device-detected errors."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_status(status: torch.Tensor, where: str = "device") -> None:
+    """Synchronize on the status word and raise if a kernel reported an error."""
+    check(int(status.item()), where)
+
+
+# ---------------------------------------------------------------- sizes
+def mxfp8_scale_bytes(rows: int, K: int, G: int, scale_layout: int) -> int:
+    return int(load().mxfp8_scale_bytes(rows, K, G, scale_layout))
+
+
+def mxfp8_scale_bytes_colgroups(R: int, M: int, G: int) -> int:
+    return int(load().mxfp8_scale_bytes_colgroups(R, M, G))
+
+
+# ---------------------------------------------------------------- quantization
+def mxfp8_quantize_2d(x: torch.Tensor, dirs: int = ROW, scale_layout: int = SCALES_BLOCKED,
+                      offs: torch.Tensor | None = None, dev_status: torch.Tensor | None = None):
+    """Quantize x[M, K] (bf16).  Returns (q_row, s_row, q_col, s_col), None for
+    directions not requested.  q_row [M, K]; q_col [K, M].  Compact scales are
+    2D ([M, K/32], [K, M/32], or [M/32, K/32] for 32x32 blocks); blocked scales
+    are flat byte buffers (upper-bound size, zero padded)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("mxfp8_quantize_2d: x must be a 2D bf16 tensor")
+    _cuda(x, offs, dev_status)
+    M, K = x.shape
+    G = int(offs.numel()) if offs is not None else 1
+    dev = x.device
+    q_row = s_row = q_col = s_col = None
+    if dirs & (ROW | BLOCK32X32):
+        q_row = _u8((M, K), dev)
+        if dirs & BLOCK32X32:
+            s_row = _u8((M // 32, K // 32), dev)
+        elif scale_layout == SCALES_COMPACT:
+            s_row = _u8((M, K // 32), dev)
+        else:
+            s_row = _u8((mxfp8_scale_bytes(M, K, G, SCALES_BLOCKED),), dev)
+    if dirs & COL:
+        q_col = _u8((K, M), dev)
+        if scale_layout == SCALES_COMPACT:
+            s_col = _u8((K, M // 32), dev)
+        else:
+            s_col = _u8((mxfp8_scale_bytes_colgroups(K, M, G),), dev)
+    if offs is not None and offs.dtype != torch.int32:
+        raise ValueError("offs must be int32")
+    st = load().mxfp8_quantize_2d(_p(x), M, K, dirs, scale_layout, _p(offs), G if offs is not None else 0,
+                                  _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(dev_status), _stream(dev))
+    check(st, "mxfp8_quantize_2d")
+    return q_row, s_row, q_col, s_col
+
+
+def mxfp8_quantize_3d_experts(w: torch.Tensor, dirs: int = ROW | COL, scale_layout: int = SCALES_BLOCKED,
+                              dev_status: torch.Tensor | None = None):
+    """Quantize expert weights w[G, N, K] (bf16).  Returns (q, s, qT, sT):
+    q [G, N, K] along K ("plain"), qT [G, K, N] along N ("transposed");
+    scales [G, ...] per expert (compact 3D, or blocked flat per expert)."""
+    if w.dtype != torch.bfloat16 or w.dim() != 3:
+        raise ValueError("mxfp8_quantize_3d_experts: w must be a 3D bf16 tensor")
+    _cuda(w, dev_status)
+    G, N, K = w.shape
+    dev = w.device
+    q = s = qT = sT = None
+    if dirs & ROW:
+        q = _u8((G, N, K), dev)
+        s = _u8((G, N, K // 32), dev) if scale_layout == SCALES_COMPACT else \
+            _u8((G, ((N + 127) // 128) * 128 * ((K + 127) // 128) * 4), dev)
+    if dirs & COL:
+        qT = _u8((G, K, N), dev)
+        sT = _u8((G, K, N // 32), dev) if scale_layout == SCALES_COMPACT else \
+            _u8((G, ((K + 127) // 128) * 128 * ((N + 127) // 128) * 4), dev)
+    st = load().mxfp8_quantize_3d_experts(_p(w), G, N, K, dirs, scale_layout, _p(q), _p(s), _p(qT), _p(sT),
+                                          _p(dev_status), _stream(dev))
+    check(st, "mxfp8_quantize_3d_experts")
+    return q, s, qT, sT
+
+
+# ---------------------------------------------------------------- grouped GEMMs
+def mxfp8_grouped_mm_fwd(a_q, a_s, w_q, w_s, offs, out=None, dev_status=None):
+    """out[m, n] = sum_k A[m,k] W[g][n,k] for rows m of group g; bf16 [M, N]."""
+    _cuda(a_q, a_s, w_q, w_s, offs, out, dev_status)
+    M, K = a_q.shape
+    G, N, _ = w_q.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
+    st = load().mxfp8_grouped_mm_fwd(_p(a_q), _p(a_s), _p(w_q), _p(w_s), _p(offs), G, M, N, K, _p(out),
+                                     _p(dev_status), _stream(a_q.device))
+    check(st, "mxfp8_grouped_mm_fwd")
+    return out
+
+
+def mxfp8_grouped_mm_dgrad(dout_q, dout_s, wt_q, wt_s, offs, out=None, dev_status=None):
+    """dA[m, k] = sum_n dOut[m,n] W[g][n,k]; dout_q [M, N], wt_q [G, K, N]; bf16 [M, K]."""
+    _cuda(dout_q, dout_s, wt_q, wt_s, offs, out, dev_status)
+    M, N = dout_q.shape
+    G, K, _ = wt_q.shape
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=dout_q.device)
+    st = load().mxfp8_grouped_mm_dgrad(_p(dout_q), _p(dout_s), _p(wt_q), _p(wt_s), _p(offs), G, M, N, K, _p(out),
+                                       _p(dev_status), _stream(dout_q.device))
+    check(st, "mxfp8_grouped_mm_dgrad")
+    return out
+
+
+def mxfp8_grouped_mm_wgrad(doutT_q, doutT_s, aT_q, aT_s, offs, out=None, dev_status=None):
+    """dW[g][n, k] = sum_{m in g} dOut[m,n] A[m,k]; doutT_q [N, M], aT_q [K, M]; bf16 [G, N, K]."""
+    _cuda(doutT_q, doutT_s, aT_q, aT_s, offs, out, dev_status)
+    N, M = doutT_q.shape
+    K, _ = aT_q.shape
+    G = int(offs.numel())
+    if out is None:
+        out = torch.empty((G, N, K), dtype=torch.bfloat16, device=doutT_q.device)
+    st = load().mxfp8_grouped_mm_wgrad(_p(doutT_q), _p(doutT_s), _p(aT_q), _p(aT_s), _p(offs), G, M, N, K,
+                                       _p(out), _p(dev_status), _stream(doutT_q.device))
+    check(st, "mxfp8_grouped_mm_wgrad")
+    return out
+
+
+def mxfp8_check_offsets(offs: torch.Tensor, M: int, align: int, dev_status: torch.Tensor) -> None:
+    _cuda(offs, dev_status)
+    st = load().mxfp8_check_offsets(_p(offs), int(offs.numel()), M, align, _p(dev_status), _stream(offs.device))
+    check(st, "mxfp8_check_offsets")
+
+
+def mxfp8_debug_wait_timeout(dev_status: torch.Tensor, limit_ns: int) -> None:
+    _cuda(dev_status)
+    st = load().mxfp8_debug_wait_timeout(_p(dev_status), int(limit_ns), _stream(dev_status.device))
+    check(st, "mxfp8_debug_wait_timeout")
+
+
+# ---------------------------------------------------------------- composite differentiable op
+class _ToMxfp8ThenScaledGroupedMM(torch.autograd.Function):
+    """Forward: quantize A along K (and along the tokens for the wgrad), quantize
+    W plain (forward) and transposed (dgrad), one grouped GEMM.  Backward:
+    quantize dOut along N (dgrad) and along the tokens (wgrad), two grouped
+    GEMMs.  Quantization is treated as the identity for gradients."""
+
+    @staticmethod
+    def forward(ctx, A, W, offs):
+        need_dA = ctx.needs_input_grad[0]
+        need_dW = ctx.needs_input_grad[1]
+        a_dirs = ROW | (COL if need_dW else 0)
+        aq, as_, aTq, aTs = mxfp8_quantize_2d(A.contiguous(), a_dirs, SCALES_BLOCKED, offs)
+        w_dirs = ROW | (COL if need_dA else 0)
+        wq, ws, wTq, wTs = mxfp8_quantize_3d_experts(W.contiguous(), w_dirs, SCALES_BLOCKED)
+        out = mxfp8_grouped_mm_fwd(aq, as_, wq, ws, offs)
+        ctx.save_for_backward(aTq, aTs, wTq, wTs, offs)
+        ctx.shape = (A.shape[0], W.shape[0], W.shape[1], W.shape[2])
+        return out
+
+    @staticmethod
+    def backward(ctx, dOut):
+        aTq, aTs, wTq, wTs, offs = ctx.saved_tensors
+        need_dA, need_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        dirs = (ROW if need_dA else 0) | (COL if need_dW else 0)
+        if dirs == 0:
+            return None, None, None
+        dq, ds, dTq, dTs = mxfp8_quantize_2d(dOut.contiguous().to(torch.bfloat16), dirs, SCALES_BLOCKED, offs)
+        dA = mxfp8_grouped_mm_dgrad(dq, ds, wTq, wTs, offs) if need_dA else None
+        dW = mxfp8_grouped_mm_wgrad(dTq, dTs, aTq, aTs, offs) if need_dW else None
+        return dA, dW, None
+
+
+def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torch.Tensor) -> torch.Tensor:
+    """Differentiable MXFP8 grouped GEMM: out[m] = A[m] @ W[g]^T for rows m of
+    group g (offs = int32 cumulative end rows).  A [M, K] bf16, W [G, N, K] bf16,
+    out [M, N] bf16.  Group sizes must be multiples of 32 when gradients of W
+    are needed (token-wise quantization for the wgrad)."""
+    if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise ValueError("to_mxfp8_then_scaled_grouped_mm expects bf16 A and W")
+    if offs.dtype != torch.int32:
+        raise ValueError("offs must be int32")
+    return _ToMxfp8ThenScaledGroupedMM.apply(A, W, offs)

@@ -1,0 +1,544 @@
+// grouped_mm.cu -- block-scaled MXFP8 grouped GEMMs (forward, dgrad, wgrad)
+// for sm_103a on the 5th-generation tensor cores.
+//
+// What is computed ("MXFP8 training for MoEs", engine paragraph and "Why Does
+// MXFP8 Speed Up MoE Training": routed experts run as grouped GEMMs over
+// tokens sorted by expert, forward and a mirrored backward; "MXFP8
+// (Micro-scaling FP8)", "Low-precision Flash Attention": scales run along each
+// GEMM's K):
+//   fwd    out[m, n]   = sum_k  A[m,k]    W[g][n,k]      (rows of group g)
+//   dgrad  dA[m, k]    = sum_n  dOut[m,n] W[g][n,k]      (W quantized along N)
+//   wgrad  dW[g][n, k] = sum_{m in g} dOut[m,n] A[m,k]    (both quantized along tokens)
+// All three are one "TN" contraction of two K-major e4m3 operands with E8M0
+// scales per 32 K-elements in the blocked tensor-core layout; they differ only
+// in how tiles map to groups:
+//   ROWGROUPED (fwd, dgrad): the token operand's rows are split by group; each
+//     group's rows are tiled by 128 and contracted with that expert's matrix.
+//   KGROUPED (wgrad): every group owns a full output matrix; its contraction
+//     runs over the group's own tokens only (empty group -> zeros).
+//
+// Kernel structure (one CTA per SM, persistent over a static tile order):
+//   warp 0      TMA producer: 128B-swizzled A/B tiles (128 x 128 B and BN x 128 B)
+//               and the matching 512-byte scale tiles into a ring of SMEM stages.
+//   warp 1      MMA issuer: tcgen05.cp copies the scale tiles into tensor memory,
+//               then four tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each,
+//               scale byte k of the 32-bit TMEM scale word) per stage into an fp32
+//               accumulator in tensor memory; tcgen05.commit frees stages.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (each warp its 32-lane
+//               quarter), fp32 -> bf16 round-to-nearest-even, masked 16-byte
+//               stores of the rows and columns that belong to the tile's group.
+// Every mbarrier wait is bounded (MXFP8_ERR_TIMEOUT + orderly exit).
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace mx {
+
+constexpr int BM = 128;  // tile rows = tensor-memory lanes
+constexpr int BK = 128;  // contraction bytes (= e4m3 elements) per stage: one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr int kBand = 16;  // m-tiles per raster band (tiles of a band share B tiles in L2)
+
+enum GemmMode : int { ROWGROUPED = 0, KGROUPED = 1 };
+
+template <int BN>
+struct Cfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kAcc = BN == 256 ? 1 : 2;
+    static constexpr int kABytes = BM * BK;
+    static constexpr int kBBytes = BN * BK;
+    static constexpr int kSfaBytes = 512;
+    static constexpr int kSfbBytes = (BN / 128) * 512;
+    static constexpr int kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    static constexpr int kSfCols = 4 + BN / 32;           // tensor-memory columns of one stage's scales
+    static constexpr int kSfCol0 = BN * kAcc;             // first scale column
+    static constexpr int kTmemCols = 512;
+    static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "tensor memory overflow");
+    static constexpr int kOffB = kStages * kABytes;
+    static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+    static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
+    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+    static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
+    static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
+};
+
+struct GemmParams {
+    const uint8_t* sfa;       // blocked scales of the A operand
+    const uint8_t* sfb;       // blocked scales of the B operand
+    int64_t sfa_ct;           // ROWGROUPED: column tiles per 128-row band of A scales
+    int64_t sfb_ct;           // ROWGROUPED: same for B scales
+    int64_t sfb_estride;      // ROWGROUPED: bytes of B scales per expert
+    int64_t na;               // KGROUPED: rows of A (= N); ROWGROUPED: unused
+    int64_t nb;               // rows of B per expert (ROWGROUPED) or in total (KGROUPED)
+    int64_t kc;               // ROWGROUPED: contraction length
+    const int32_t* offs;
+    int32_t G;
+    int64_t M;                // tokens
+    __nv_bfloat16* out;
+    int64_t ldo;              // ROWGROUPED: output row pitch (elements)
+    int mode;
+    int32_t* dev_status;
+    uint64_t timeout_ns;
+};
+
+struct TileInfo {
+    int g;
+    int64_t a_row, b_row;     // TMA row coordinates
+    int64_t a_x0;             // TMA contraction coordinate of k-tile 0
+    int k_tiles;
+    int64_t sfa_base;         // byte offset of k-tile 0's A scale tile
+    int64_t sfb_base[2];      // byte offsets of k-tile 0's B scale tiles
+    int64_t sf_kstep;         // bytes between consecutive k-tiles' scale tiles (always 512)
+    __nv_bfloat16* out;       // first element of the tile
+    int64_t ldo;
+    int valid_rows, valid_cols;
+};
+
+__device__ __forceinline__ int band_split(int64_t l, int64_t mt, int64_t nt, int64_t& m, int64_t& n) {
+    const int64_t band = l / (kBand * nt);
+    const int64_t bm = min64(kBand, mt - band * kBand);
+    const int64_t idx = l - band * kBand * nt;
+    n = idx / bm;
+    m = band * kBand + (idx - n * bm);
+    return 0;
+}
+
+template <int BN>
+__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, const int32_t* ends_s,
+                                              const int32_t* pstart_s, int64_t ptotal) {
+    TileInfo ti;
+    const int64_t ntb = (p.nb + BN - 1) / BN;  // tiles along B rows
+    if (p.mode == ROWGROUPED) {
+        // group of tile t: last g whose tile range starts at or before t
+        int lo = 0, hi = p.G;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((int64_t)(pstart_s[mid] / BM) * ntb <= t) lo = mid + 1;
+            else hi = mid;
+        }
+        const int g = lo - 1;
+        const int64_t start = g ? ends_s[g - 1] : 0, size = ends_s[g] - start;
+        const int64_t mt = (size + BM - 1) / BM;
+        int64_t m, n;
+        band_split(t - (int64_t)(pstart_s[g] / BM) * ntb, mt, ntb, m, n);
+        ti.g = g;
+        ti.a_row = start + m * BM;
+        ti.b_row = (int64_t)g * p.nb + n * BN;
+        ti.a_x0 = 0;
+        ti.k_tiles = (int)((p.kc + BK - 1) / BK);
+        ti.sfa_base = ((int64_t)(pstart_s[g] / BM + m) * p.sfa_ct) * 512;
+        const int64_t last_chunk = (p.nb + 127) / 128 - 1;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t ch = min64(n * (BN / 128) + j, last_chunk);
+            ti.sfb_base[j] = (int64_t)g * p.sfb_estride + ch * p.sfb_ct * 512;
+        }
+        ti.out = p.out + ti.a_row * p.ldo + n * BN;
+        ti.ldo = p.ldo;
+        ti.valid_rows = (int)min64(BM, size - m * BM);
+        ti.valid_cols = (int)min64(BN, p.nb - n * BN);
+    } else {
+        const int64_t nta = (p.na + BM - 1) / BM;
+        const int64_t per_g = nta * ntb;
+        const int g = (int)(t / per_g);
+        int64_t m, n;
+        band_split(t - g * per_g, nta, ntb, m, n);
+        const int64_t start = g ? ends_s[g - 1] : 0, size = ends_s[g] - start;
+        const int64_t ct = ptotal / 128;           // column tiles of the token-grouped scale layout
+        const int64_t kt0 = pstart_s[g] / 128;     // this group's first column tile
+        ti.g = g;
+        ti.a_row = m * BM;
+        ti.b_row = n * BN;
+        ti.a_x0 = start;
+        ti.k_tiles = (int)((size + BK - 1) / BK);
+        ti.sfa_base = (m * ct + kt0) * 512;
+        const int64_t last_chunk = (p.nb + 127) / 128 - 1;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t ch = min64(n * (BN / 128) + j, last_chunk);
+            ti.sfb_base[j] = (ch * ct + kt0) * 512;
+        }
+        ti.out = p.out + ((int64_t)g * p.na + m * BM) * p.nb + n * BN;
+        ti.ldo = p.nb;
+        ti.valid_rows = (int)min64(BM, p.na - m * BM);
+        ti.valid_cols = (int)min64(BN, p.nb - n * BN);
+    }
+    ti.sf_kstep = 512;
+    return ti;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_mm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                      const GemmParams p) {
+    using C = Cfg<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ int32_t ends_s[kMaxGroups];
+    __shared__ int32_t pstart_s[kMaxGroups];
+    __shared__ int32_t ptotal_s;
+    __shared__ int32_t bad_s;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* tfull = empty + C::kStages;
+    uint64_t* tempty = tfull + C::kAcc;
+    uint64_t* drain = tempty + C::kAcc;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- group table (warp 0), barriers (warp 1 lane 0), tensor memory (warp 1)
+    if (warp == 0) {
+        // clamped monotone ends and padded starts (multiples of 128 rows / tokens)
+        const int G = p.G;
+        const int per = (G + 31) / 32;
+        const int g0 = lane * per, g1 = min(G, g0 + per);
+        const int32_t Mc = (int32_t)p.M;
+        int32_t mx = 0;
+        for (int g = g0; g < g1; ++g) mx = max(mx, min(max(p.offs[g], 0), Mc));
+        int32_t incl = mx;
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl = max(incl, o);
+        }
+        int32_t run = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) run = 0;
+        int32_t prev = run, psum = 0, bad = 0;
+        for (int g = g0; g < g1; ++g) {
+            const int32_t e = max(prev, min(max(p.offs[g], 0), Mc));
+            ends_s[g] = e;
+            if (p.mode == KGROUPED && (e - prev) % 32 != 0) bad = 1;  // TMA token coordinates must stay 16B aligned
+            psum += ((e - prev + 127) / 128) * 128;
+            prev = e;
+        }
+        int32_t sincl = psum;
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, sincl, d);
+            if (lane >= d) sincl += o;
+        }
+        int32_t sexcl = sincl - psum;
+        prev = run;
+        for (int g = g0; g < g1; ++g) {
+            pstart_s[g] = sexcl;
+            const int32_t e = ends_s[g];
+            sexcl += ((e - prev + 127) / 128) * 128;
+            prev = e;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 31) ptotal_s = sincl;
+        if (lane == 0) {
+            bad_s = bad;
+            abort_s = 0;
+            prefetch_tmap(&tmap_a);
+            prefetch_tmap(&tmap_b);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int s = 0; s < C::kStages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 1);
+            }
+            for (int a = 0; a < C::kAcc; ++a) {
+                mbar_init(&tfull[a], 1);
+                mbar_init(&tempty[a], 4);
+            }
+            mbar_init(drain, 1);
+            fence_barrier_init();
+        }
+        __syncwarp();
+        tmem_alloc(&tmem_base_s, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem = tmem_base_s;
+    volatile int* abort_flag = &abort_s;
+    const int64_t ptotal = ptotal_s;
+    if (bad_s) {
+        if (threadIdx.x == 0) report(p.dev_status, MXFP8_ERR_OFFSETS);
+    } else {
+        const int64_t ntb = (p.nb + BN - 1) / BN;
+        const int64_t ntiles = p.mode == ROWGROUPED ? (ptotal / BM) * ntb
+                                                    : (int64_t)p.G * ((p.na + BM - 1) / BM) * ntb;
+
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, last_phase = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileInfo ti = tile_info<BN>(p, t, ends_s, pstart_s, ptotal);
+                for (int kt = 0; kt < ti.k_tiles; ++kt) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * C::kABytes;
+                    uint8_t* sb = smem + C::kOffB + stage * C::kBBytes;
+                    uint8_t* ssa = smem + C::kOffSfa + stage * C::kSfaBytes;
+                    uint8_t* ssb = smem + C::kOffSfb + stage * C::kSfbBytes;
+                    mbar_arrive_expect_tx(&full[stage], C::kTx);
+                    const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kt * BK);
+                    tma_load_2d(sa, &tmap_a, kx, (int32_t)ti.a_row, &full[stage]);
+                    tma_load_2d(sb, &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
+                    bulk_load(ssa, p.sfa + ti.sfa_base + kt * ti.sf_kstep, 512, &full[stage]);
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        bulk_load(ssb + j * 512, p.sfb + ti.sfb_base[j] + kt * ti.sf_kstep, 512, &full[stage]);
+                    issued_mask |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let copies already in flight land before the CTA exits
+                for (int s = 0; s < C::kStages; ++s)
+                    if (issued_mask & (1u << s)) {
+                        volatile int no_abort = 0;
+                        mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, p.timeout_ns, &no_abort, nullptr);
+                    }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileInfo ti = tile_info<BN>(p, t, ends_s, pstart_s, ptotal);
+                if (ti.k_tiles == 0) continue;
+                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * BN;
+                for (int kt = 0; kt < ti.k_tiles; ++kt) {
+                    if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + C::kSfCol0 + stage * C::kSfCols;
+                    const uint32_t sfb_t = sfa_t + 4;
+                    const uint32_t a_s = smem_u32(smem + stage * C::kABytes);
+                    const uint32_t b_s = smem_u32(smem + C::kOffB + stage * C::kBBytes);
+                    const uint32_t sfa_s = smem_u32(smem + C::kOffSfa + stage * C::kSfaBytes);
+                    const uint32_t sfb_s = smem_u32(smem + C::kOffSfb + stage * C::kSfbBytes);
+                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sfa_s, 0, 128, 0));
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j) tc_cp_32x128b_warpx4(sfb_t + 4 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k) {
+                        const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
+                        const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
+                        tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, k, k), sfa_t, sfb_t, (kt | k) != 0);
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(&tfull[acc]);
+                if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
+            }
+            // all tensor-core work of this CTA must be done before the columns are freed
+            tc_commit(drain);
+            volatile int no_abort = 0;
+            mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
+        } else if (warp >= 2) {
+            // ------------------------------------------------ epilogue
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                const TileInfo ti = tile_info<BN>(p, t, ends_s, pstart_s, ptotal);
+                const bool row_ok = r < ti.valid_rows;
+                __nv_bfloat16* orow = ti.out + (int64_t)r * ti.ldo;
+                if (ti.k_tiles == 0) {
+                    if (row_ok)
+                        for (int c = 0; c < ti.valid_cols; c += 8)
+                            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+                    continue;
+                }
+                if (!mbar_wait_bounded(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN + c, v);
+                    tmem_ld_wait();
+                    if (row_ok && c < ti.valid_cols) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2D uint8 tensor [rows][cols] (row pitch = cols bytes), box = box_rows x 128 bytes, 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+static mxfp8_status_t launch_gemm(const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
+                                  int64_t b_cols, GemmParams& p, int64_t tiles_bound, cudaStream_t st) {
+    using C = Cfg<BN>;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, BN)) return MXFP8_ERR_DRIVER;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(grouped_mm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+            cudaSuccess)
+            return MXFP8_ERR_LAUNCH;
+        attr_set = true;
+    }
+    const int grid = (int)max64(1, min64(tiles_bound, host::num_sms()));
+    grouped_mm_kernel<BN><<<grid, kThreads, C::kSmem, st>>>(ma, mb, p);
+    return host::last_launch_status();
+}
+
+static uint64_t default_timeout_ns() { return 2000000000ull; }
+
+// fwd and dgrad: token operand tok_q [M, Kc], expert operand ex_q [G, Nb, Kc].
+static mxfp8_status_t rowgrouped(const void* tok_q, const void* tok_s, const void* ex_q, const void* ex_s,
+                                 const int32_t* offs, int32_t G, int64_t M, int64_t Nb, int64_t Kc, void* out,
+                                 int32_t* dev_status, cudaStream_t st) {
+    if (!tok_q || !tok_s || !ex_q || !ex_s || !offs || !out) return MXFP8_ERR_NULL;
+    if (G < 1 || G > MXFP8_MAX_GROUPS || M < 0 || Nb <= 0 || Kc <= 0 || M > INT32_MAX || (int64_t)G * Nb > INT32_MAX)
+        return MXFP8_ERR_SHAPE;
+    if (Kc % 32 || Nb % 32) return MXFP8_ERR_ALIGN;
+    if (!host::aligned16(tok_q) || !host::aligned16(tok_s) || !host::aligned16(ex_q) || !host::aligned16(ex_s) ||
+        !host::aligned16(out))
+        return MXFP8_ERR_ALIGN;
+    if (mxfp8_status_t a = host::check_arch(); a != MXFP8_OK) return a;
+    if (M == 0) return MXFP8_OK;
+    GemmParams p{};
+    p.sfa = static_cast<const uint8_t*>(tok_s);
+    p.sfb = static_cast<const uint8_t*>(ex_s);
+    p.sfa_ct = (Kc + 127) / 128;
+    p.sfb_ct = (Kc + 127) / 128;
+    p.sfb_estride = ((Nb + 127) / 128) * 128 * p.sfb_ct * 4;
+    p.nb = Nb;
+    p.kc = Kc;
+    p.offs = offs;
+    p.G = G;
+    p.M = M;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.ldo = Nb;
+    p.mode = ROWGROUPED;
+    p.dev_status = dev_status;
+    p.timeout_ns = default_timeout_ns();
+    if (Nb >= 256) {
+        const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 255) / 256);
+        return launch_gemm<256>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st);
+    }
+    const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 127) / 128);
+    return launch_gemm<128>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st);
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" mxfp8_status_t mxfp8_grouped_mm_fwd(const void* a_q, const void* a_s, const void* w_q, const void* w_s,
+                                               const int32_t* offs, int32_t G, int64_t M, int64_t N, int64_t K,
+                                               void* out_bf16, int32_t* dev_status, mxfp8_stream_t stream) {
+    return rowgrouped(a_q, a_s, w_q, w_s, offs, G, M, N, K, out_bf16, dev_status,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" mxfp8_status_t mxfp8_grouped_mm_dgrad(const void* dout_q, const void* dout_s, const void* wt_q,
+                                                 const void* wt_s, const int32_t* offs, int32_t G, int64_t M,
+                                                 int64_t N, int64_t K, void* da_bf16, int32_t* dev_status,
+                                                 mxfp8_stream_t stream) {
+    return rowgrouped(dout_q, dout_s, wt_q, wt_s, offs, G, M, K, N, da_bf16, dev_status,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" mxfp8_status_t mxfp8_grouped_mm_wgrad(const void* doutT_q, const void* doutT_s, const void* aT_q,
+                                                 const void* aT_s, const int32_t* offs, int32_t G, int64_t M,
+                                                 int64_t N, int64_t K, void* dw_bf16, int32_t* dev_status,
+                                                 mxfp8_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!doutT_q || !doutT_s || !aT_q || !aT_s || !offs || !dw_bf16) return MXFP8_ERR_NULL;
+    if (G < 1 || G > MXFP8_MAX_GROUPS || M < 0 || N <= 0 || K <= 0 || M > INT32_MAX || N > INT32_MAX ||
+        K > INT32_MAX)
+        return MXFP8_ERR_SHAPE;
+    if (N % 32 || K % 32 || M % 32) return MXFP8_ERR_ALIGN;
+    if (!host::aligned16(doutT_q) || !host::aligned16(doutT_s) || !host::aligned16(aT_q) || !host::aligned16(aT_s) ||
+        !host::aligned16(dw_bf16))
+        return MXFP8_ERR_ALIGN;
+    if (mxfp8_status_t a = host::check_arch(); a != MXFP8_OK) return a;
+    if (M == 0) {
+        return cudaMemsetAsync(dw_bf16, 0, (size_t)G * N * K * 2, st) == cudaSuccess ? MXFP8_OK : MXFP8_ERR_LAUNCH;
+    }
+    GemmParams p{};
+    p.sfa = static_cast<const uint8_t*>(doutT_s);
+    p.sfb = static_cast<const uint8_t*>(aT_s);
+    p.na = N;
+    p.nb = K;
+    p.offs = offs;
+    p.G = G;
+    p.M = M;
+    p.out = static_cast<__nv_bfloat16*>(dw_bf16);
+    p.mode = KGROUPED;
+    p.dev_status = dev_status;
+    p.timeout_ns = default_timeout_ns();
+    if (K >= 256) {
+        const int64_t bound = (int64_t)G * ((N + BM - 1) / BM) * ((K + 255) / 256);
+        return launch_gemm<256>(doutT_q, N, M, aT_q, K, M, p, bound, st);
+    }
+    const int64_t bound = (int64_t)G * ((N + BM - 1) / BM) * ((K + 127) / 128);
+    return launch_gemm<128>(doutT_q, N, M, aT_q, K, M, p, bound, st);
+}
