@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP8 routed-expert hot path on GB300.
+
+One step = one pass of the whole path over one batch of the Llama4-Scout-like
+routed-expert workload (G=8 experts, K=5120, N=8192, M=16384 tokens in
+Zipf(1.1) groups; synthetic bf16 data, random weights):
+    quantize A row+column  -> quantize W plain+transposed -> grouped GEMM fwd
+    quantize dOut row+column -> grouped GEMM dgrad -> grouped GEMM wgrad
+every call through the C ABI (libmxfp8moe.so).  `value` = algorithmic fwd+bwd
+GEMM FLOPs (3 x 2*M*N*K) / step time, with inputs resident in HBM; `e2e` = the
+same metric with the inputs copied from pinned host memory and the results
+copied back inside every step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Multi-GPU: independent replicas (the path has no exchange step), one process
+per GPU under torchrun; the max step time over ranks sets `value`.
+--impl reference times the CPU oracle (fp64, plain C) on a bounded sample of
+the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP8 grouped-GEMM fwd+bwd TFLOP/s & % MXFP8 peak; quantize GB/s vs HBM"
+WORKLOAD = ("Llama4-Scout-like routed experts fwd+bwd: G=8, K=5120, N=8192, M=16384 tokens, "
+            "Zipf(1.1) group sizes in 32-token chunks (seed 0)")
+FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
+L2_BYTES = 129 * 2 ** 20
+
+# DRAM traffic of one grouped-GEMM forward launch on this workload, from the
+# ncu capture summarised in profiles/grouped_mm_fwd_scout.md, valid only while
+# the kernel sources hash to the value recorded with it.
+FWD_TRAFFIC = {"bytes": 731750144, "src_sha": "df7a213bbccbc00d"}
+
+
+def kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("grouped_mm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "mxfp8_precision_moe_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    ap.add_argument("--no-baseline", action="store_true", help="skip the cuBLAS bf16 comparison leg")
+    return ap.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------- clocks during the timed region
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        ident = str(device_index)
+        try:
+            bus = getattr(torch.cuda.get_device_properties(device_index), "pci_bus_id", None)
+            if bus:
+                ident = bus
+        except Exception:
+            pass
+        cmd = ["nvidia-smi", "-i", ident, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for t, p in self.samples if t0 <= t <= t1] or [p for _, p in self.samples[-5:]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        mx = [num(p[1]) for p in win if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[3 + i].lower() == "active"})
+        pw = [num(p[2]) for p in win if num(p[2]) is not None]
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------- the step, through the C ABI
+class Step:
+    """Device buffers of one replica and the C-ABI calls of one pass of the path."""
+
+    def __init__(self, w: dict, device):
+        import mxfp8_precision_moe_gb300 as mx
+
+        L = mx.load()
+        self.mx, self.L = mx, L
+        G, M, N, K = w["G"], w["M"], w["N"], w["K"]
+        self.G, self.M, self.N, self.K = G, M, N, K
+        u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device=device)
+        bf = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=device)
+        self.A, self.W, self.D = w["A"].to(device), w["W"].to(device), w["dOut"].to(device)
+        self.offs = w["offs"].to(device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        sb = mx.mxfp8_scale_bytes
+        sc = mx.mxfp8_scale_bytes_colgroups
+        self.aq, self.as_ = u8(M, K), u8(sb(M, K, G, 1))
+        self.aTq, self.aTs = u8(K, M), u8(sc(K, M, G))
+        ce = lambda r, c: ((r + 127) // 128) * 128 * ((c + 127) // 128) * 4
+        self.wq, self.ws = u8(G, N, K), u8(G, ce(N, K))
+        self.wTq, self.wTs = u8(G, K, N), u8(G, ce(K, N))
+        self.dq, self.ds = u8(M, N), u8(sb(M, N, G, 1))
+        self.dTq, self.dTs = u8(N, M), u8(sc(N, M, G))
+        self.out, self.dA, self.dW = bf(M, N), bf(M, K), bf(G, N, K)
+        P = lambda t: ctypes.c_void_p(t.data_ptr())
+        st = P(self.status)
+        RC = 3  # MXFP8_ROW | MXFP8_COL
+        self.calls = [
+            ("quant_A", L.mxfp8_quantize_2d, (P(self.A), M, K, RC, 1, P(self.offs), G, P(self.aq), P(self.as_),
+                                              P(self.aTq), P(self.aTs), st)),
+            ("quant_W", L.mxfp8_quantize_3d_experts, (P(self.W), G, N, K, RC, 1, P(self.wq), P(self.ws),
+                                                      P(self.wTq), P(self.wTs), st)),
+            ("fwd", L.mxfp8_grouped_mm_fwd, (P(self.aq), P(self.as_), P(self.wq), P(self.ws), P(self.offs), G, M,
+                                             N, K, P(self.out), st)),
+            ("quant_dOut", L.mxfp8_quantize_2d, (P(self.D), M, N, RC, 1, P(self.offs), G, P(self.dq), P(self.ds),
+                                                 P(self.dTq), P(self.dTs), st)),
+            ("dgrad", L.mxfp8_grouped_mm_dgrad, (P(self.dq), P(self.ds), P(self.wTq), P(self.wTs), P(self.offs), G,
+                                                 M, N, K, P(self.dA), st)),
+            ("wgrad", L.mxfp8_grouped_mm_wgrad, (P(self.dTq), P(self.dTs), P(self.aTq), P(self.aTs), P(self.offs), G,
+                                                 M, N, K, P(self.dW), st)),
+        ]
+        # kernels each call launches (quantize: tile kernel + blocked-padding kernels)
+        self.launches = {"quant_A": 3, "quant_W": 3, "fwd": 1, "quant_dOut": 3, "dgrad": 1, "wgrad": 1}
+        self.flops = 3 * 2.0 * M * N * K
+        self.bytes = {"quant_A": M * K * (2 + 1 + 1 + 2 / 32), "quant_W": G * N * K * (2 + 1 + 1 + 2 / 32),
+                      "quant_dOut": M * N * (2 + 1 + 1 + 2 / 32)}
+        self.gemm_flops = {"fwd": 2.0 * M * N * K, "dgrad": 2.0 * M * N * K, "wgrad": 2.0 * M * N * K}
+
+    def run(self, stream, events=None):
+        for name, fn, args in self.calls:
+            if events is not None:
+                events[name][0].record(stream)
+            rc = fn(*args, ctypes.c_void_p(stream.cuda_stream))
+            if rc != 0:
+                raise RuntimeError(f"{name}: {self.mx._lib.STATUS_NAMES.get(rc, rc)}")
+            if events is not None:
+                events[name][1].record(stream)
+
+    def check_status(self):
+        self.mx.read_status(self.status, "bench step")
+
+
+# ---------------------------------------------------------------- oracle sample (CPU baseline / reference arm)
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+class OracleProbe:
+    """Sampled outputs of the three GEMMs computed by the CPU oracle from the bf16
+    inputs (quantization included): one probe = one element of out, one of dA
+    and one of dW.  Algorithmic FLOPs of a probe: 2*(K + N + M_g)."""
+
+    def __init__(self, w_cpu: dict, seed: int = 0):
+        import oracle
+
+        oracle.lib()
+        self.o = oracle
+        self.w = w_cpu
+        self.ends = np.cumsum(w_cpu["sizes"])
+        self.starts = self.ends - np.asarray(w_cpu["sizes"])
+        self.nonempty = [g for g, s in enumerate(w_cpu["sizes"]) if s > 0]
+        self.rng = np.random.default_rng(seed)
+
+    def probe(self) -> float:
+        o, w, rng = self.o, self.w, self.rng
+        M, N, K = w["M"], w["N"], w["K"]
+        m = int(rng.integers(0, M))
+        g = int(np.searchsorted(self.ends, m, side="right"))
+        n, k = int(rng.integers(0, N)), int(rng.integers(0, K))
+        qa, sa = o.quantize_vec(_bits(w["A"][m]))
+        qw, sw = o.quantize_vec(_bits(w["W"][g, n]))
+        o.dot(qa, sa, qw, sw)                                   # out[m, n]
+        qd, sd = o.quantize_vec(_bits(w["dOut"][m]))
+        qt, st = o.quantize_vec(_bits(w["W"][g, :, k]))
+        o.dot(qd, sd, qt, st)                                   # dA[m, k]
+        gg = self.nonempty[int(rng.integers(0, len(self.nonempty)))]
+        lo, hi = int(self.starts[gg]), int(self.ends[gg])
+        q1, s1 = o.quantize_vec(_bits(w["dOut"][lo:hi, n]))
+        q2, s2 = o.quantize_vec(_bits(w["A"][lo:hi, k]))
+        o.dot(q1, s1, q2, s2)                                   # dW[gg][n, k]
+        return 2.0 * (K + N + (hi - lo))
+
+
+def oracle_rate(w_cpu: dict, seconds: float, seed: int = 0):
+    """Run probes for about `seconds`; return (TFLOP/s, probes, elapsed)."""
+    pr = OracleProbe(w_cpu, seed)
+    flops, n, t0 = 0.0, 0, time.perf_counter()
+    while True:
+        flops += pr.probe()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return flops / el / 1e12, n, el
+
+
+def cpu_cores_used() -> int:
+    return 1  # the probes call the oracle's single-threaded scalar routines
+
+
+# ---------------------------------------------------------------- native (GPU) arm
+def run_native(args, rank, world, local):
+    from mxfp8_precision_moe_gb300 import synth
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    w = synth.workload("scout", seed=0, device=dev)
+    step = Step(w, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        step.run(stream)
+    torch.cuda.synchronize()
+    step.check_status()
+
+    names = [c[0] for c in step.calls]
+    ev = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
+          for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    time.sleep(0.3)  # let the sampler start
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step.run(stream, ev[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall1 = time.time()
+    sampler.stop()
+    step.check_status()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    per = {n: float(np.mean([e[n][0].elapsed_time(e[n][1]) for e in ev])) for n in names}
+    clocks = sampler.summary(wall0, wall1)
+
+    # bf16 baseline: per-group cuBLAS torch.mm loop for the forward (same bf16 inputs)
+    base = None
+    if rank == 0 and not args.no_baseline:
+        ends = np.cumsum(w["sizes"])
+        out_b = torch.empty_like(step.out)
+
+        def bf16_fwd():
+            lo = 0
+            for g, hi in enumerate(ends):
+                if hi > lo:
+                    torch.mm(step.A[lo:hi], step.W[g].t(), out=out_b[lo:hi])
+                lo = int(hi)
+
+        for _ in range(3):
+            bf16_fwd()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(20):
+            bf16_fwd()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bms = b0.elapsed_time(b1) / 20
+        base = {"kernel": "cuBLAS bf16 per-group torch.mm loop, forward", "ms": round(bms, 4),
+                "tflops": round(step.gemm_flops["fwd"] / bms / 1e9, 1)}
+
+    # end to end: host (pinned) inputs copied in and results copied out inside every step
+    e2e = None
+    if not args.no_e2e:
+        hA, hW, hD = (t.cpu().pin_memory() for t in (step.A, step.W, step.D))
+        hoffs = step.offs.cpu().pin_memory()
+        ho, hdA, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (step.out, step.dA, step.dW))
+        n_e2e = max(3, min(20, args.steps // 10))
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(n_e2e):
+            step.A.copy_(hA, non_blocking=True)
+            step.W.copy_(hW, non_blocking=True)
+            step.D.copy_(hD, non_blocking=True)
+            step.offs.copy_(hoffs, non_blocking=True)
+            step.run(stream)
+            ho.copy_(step.out, non_blocking=True)
+            hdA.copy_(step.dA, non_blocking=True)
+            hdW.copy_(step.dW, non_blocking=True)
+        x1.record(stream)
+        torch.cuda.synchronize()
+        xms = x0.elapsed_time(x1) / n_e2e
+        if world > 1:
+            t = torch.tensor([xms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            xms = float(t.item())
+        bi = sum(t.numel() * t.element_size() for t in (hA, hW, hD, hoffs))
+        bo = sum(t.numel() * t.element_size() for t in (ho, hdA, hdW))
+        e2e = {"value": round(world * step.flops / xms / 1e9, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_e2e}
+
+    if rank != 0:
+        return None
+    ms_step = ms / args.steps
+    fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
+    fwd_ms = per["fwd"]
+    achieved = step.gemm_flops["fwd"] / fwd_ms / 1e9
+    traffic = FWD_TRAFFIC["bytes"] if FWD_TRAFFIC["src_sha"] == kernel_src_sha() else None
+    kernels = {}
+    for n in names:
+        d = {"ms": round(per[n], 4)}
+        if n in step.gemm_flops:
+            tf = step.gemm_flops[n] / per[n] / 1e9
+            d.update(tflops=round(tf, 1), frac_fp8_peak=round(tf / fp8_peak, 3))
+        else:
+            gbs = step.bytes[n] / per[n] / 1e6
+            d.update(gbs=round(gbs, 1), frac_hbm=round(gbs / pk["hbm"], 3))
+        kernels[n] = d
+    line = {
+        "metric": METRIC,
+        "value": round(world * step.flops / ms_step / 1e9, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "G": step.G, "M": step.M, "N": step.N, "K": step.K,
+                   "group_sizes": list(map(int, w["sizes"])), "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({L2_BYTES // 2**20} MiB): A, W, dOut = "
+                         f"{(step.A.numel() + step.W.numel() + step.D.numel()) * 2 // 2**20} MiB bf16 per step",
+                   "frac_fp8_peak_step": round(step.flops / ms_step / 1e9 / fp8_peak, 3)},
+        "roofline": {"bound": "tensor", "kernel": "grouped_mm_fwd", "achieved": round(achieved, 1),
+                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 3),
+                     "traffic": traffic,
+                     "peak_note": f"{pk['src']} sustained bf16 {pk['bf16_sus']} TFLOP/s x {FP8_OVER_BF16} "
+                                  "(nominal dense fp8/bf16 ratio)"},
+        "kernels": kernels,
+        "hbm_peak_gbs": pk["hbm"],
+        "baseline_bf16": base,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps * sum(step.launches.values()),
+    }
+    return line, w
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    res = run_native(args, rank, world, local)
+    if rank == 0 and res is not None:
+        line, w = res
+        if not args.no_cpu and world == 1:
+            w_cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in w.items()}
+            rate, n, el = oracle_rate(w_cpu, 15.0)
+            line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
+                                    "sample": f"{n} probes (one element each of out, dA, dW, quantization "
+                                              f"included) in {el:.1f} s"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on the machine's host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    from mxfp8_precision_moe_gb300 import synth
+
+    w = synth.workload("scout", seed=0, device="cpu")
+    pr = OracleProbe(w, seed=1)
+    t0 = time.perf_counter()
+    pr.probe()
+    t_probe = time.perf_counter() - t0
+    per_step = max(1, int(90.0 / ((args.steps + args.warmup) * max(t_probe, 1e-3))))
+    for _ in range(args.warmup):
+        for _ in range(per_step):
+            pr.probe()
+    flops, t0 = 0.0, time.perf_counter()
+    for _ in range(args.steps):
+        for _ in range(per_step):
+            flops += pr.probe()
+    el = time.perf_counter() - t0
+    val = flops / el / 1e12
+    sample = f"{per_step} probe(s) per step (one element each of out, dA, dW from the bf16 inputs)"
+    line = {
+        "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
