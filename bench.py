@@ -196,8 +196,8 @@ class Step:
             ("wgrad", L.mxfp8_grouped_mm_wgrad, (P(self.dTq), P(self.dTs), P(self.aTq), P(self.aTs), P(self.offs), G,
                                                  M, N, K, P(self.dW), st)),
         ]
-        # kernels each call launches (quantize: tile kernel + blocked-padding kernels)
-        self.launches = {"quant_A": 3, "quant_W": 3, "fwd": 1, "quant_dOut": 3, "dgrad": 1, "wgrad": 1}
+        # kernels each call launches (one each: the quantize kernels also write the blocked padding)
+        self.launches = {"quant_A": 1, "quant_W": 1, "fwd": 1, "quant_dOut": 1, "dgrad": 1, "wgrad": 1}
         self.flops = 3 * 2.0 * M * N * K
         self.bytes = {"quant_A": M * K * (2 + 1 + 1 + 2 / 32), "quant_W": G * N * K * (2 + 1 + 1 + 2 / 32),
                       "quant_dOut": M * N * (2 + 1 + 1 + 2 / 32)}

@@ -370,23 +370,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!mbar_wait_bounded(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN + c, v);
+                // Drain the whole accumulator row into registers as bf16 pairs, then hand the
+                // columns back to the MMA warp before any global store is issued.
+                uint32_t packed[BN / 2];
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+#pragma unroll
+                for (int c = 0; c < BN; c += 64) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(taddr + c, v0);
+                    tmem_ld_32x32b_x32(taddr + c + 32, v1);
                     tmem_ld_wait();
-                    if (row_ok && c < ti.valid_cols) {
-                        uint32_t w[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                        uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    for (int i = 0; i < 16; ++i) {
+                        packed[c / 2 + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+                        packed[c / 2 + 16 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (row_ok) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+                    for (int i = 0; i < BN / 8; ++i)
+                        if (i * 8 < ti.valid_cols)
+                            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                }
                 if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
             }
         }
@@ -400,26 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
 // 2D uint8 tensor [rows][cols] (row pitch = cols bytes), box = box_rows x 128 bytes, 128-byte swizzle.
 static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
+    host::EncodeTiledFn fn = host::encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols};
@@ -436,13 +428,9 @@ static mxfp8_status_t launch_gemm(const void* a, int64_t a_rows, int64_t a_cols,
     using C = Cfg<BN>;
     CUtensorMap ma, mb;
     if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, BN)) return MXFP8_ERR_DRIVER;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(grouped_mm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-            cudaSuccess)
-            return MXFP8_ERR_LAUNCH;
-        attr_set = true;
-    }
+    static std::atomic<int> attr_set[host::kMaxDevices];
+    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_kernel<BN>), C::kSmem, attr_set))
+        return MXFP8_ERR_LAUNCH;
     const int grid = (int)max64(1, min64(tiles_bound, host::num_sms()));
     grouped_mm_kernel<BN><<<grid, kThreads, C::kSmem, st>>>(ma, mb, p);
     return host::last_launch_status();

@@ -2,6 +2,7 @@
 // device, the sm_103 architecture check, launch-status mapping, alignment.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,10 +36,18 @@ inline int num_sms() {
 }
 
 // The kernels are built for sm_103a only: refuse other devices up front.
+// Also make sure the device's primary context is current in the calling host
+// thread (a fresh thread, e.g. an autograd worker that has issued no CUDA call
+// yet, has none, and encoding a TMA descriptor needs one).
 inline mxfp8_status_t check_arch() {
     static std::atomic<int> cache[kMaxDevices];  // 0 unknown, 1 ok, 2 wrong arch
+    static thread_local int bound = -1;
     const int d = current_device();
     if (d < 0 || d >= kMaxDevices) return MXFP8_ERR_ARCH;
+    if (bound != d) {
+        if (cudaSetDevice(d) != cudaSuccess) return MXFP8_ERR_LAUNCH;
+        bound = d;
+    }
     int v = cache[d].load(std::memory_order_relaxed);
     if (v == 0) {
         int major = 0, minor = 0;
@@ -56,6 +65,37 @@ inline mxfp8_status_t last_launch_status() {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled, looked up through the runtime (no -lcuda needed).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_relaxed);
+    if (!f) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<EncodeTiledFn>(ptr);
+            fn.store(f, std::memory_order_relaxed);
+        }
+    }
+    return f;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+inline bool ensure_smem(const void* func, int bytes, std::atomic<int>* flags) {
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return false;
+    if (flags[d].load(std::memory_order_relaxed)) return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    flags[d].store(1, std::memory_order_relaxed);
+    return true;
+}
 
 }  // namespace host
 }  // namespace mx

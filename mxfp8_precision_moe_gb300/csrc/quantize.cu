@@ -28,6 +28,8 @@
 
 namespace mx {
 
+constexpr uint64_t kQTimeoutNs = 2000000000ull;  // bounded waits: 2 s
+
 struct QParams {
     const uint16_t* x;   // [batch][R][C] bf16 bits
     int64_t R, C;        // per-batch matrix
@@ -104,11 +106,30 @@ __device__ __forceinline__ uint32_t shfl_xor_max16x2(uint32_t v, int m) {
     return vmax_u16x2(v, __shfl_xor_sync(0xffffffffu, v, m));
 }
 
+// (a*f, c*f) with one packed fp32x2 multiply (exact: f is a power of two).
+__device__ __forceinline__ float2 mul2(float a, float c, float f) {
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, d;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %4};\n\t"
+        "mul.rn.f32x2 d, x, y;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a), "f"(c), "f"(f));
+    return r;
+}
+
+// One bf16 pair times f -> two E4M3 codes (16 bits).
+__device__ __forceinline__ uint32_t quant2(uint32_t w, float f) {
+    const float2 y = mul2(bf16lo(w), bf16hi(w), f);
+    return cvt_e4m3x2(y.x, y.y);
+}
+
 // Eight bf16 (4 packed words) times f -> eight E4M3 codes (little-endian in a u64).
 __device__ __forceinline__ uint2 quant8(const uint32_t (&w)[4], float f) {
     uint2 r;
-    r.x = cvt_e4m3x2(bf16lo(w[0]) * f, bf16hi(w[0]) * f) | (cvt_e4m3x2(bf16lo(w[1]) * f, bf16hi(w[1]) * f) << 16);
-    r.y = cvt_e4m3x2(bf16lo(w[2]) * f, bf16hi(w[2]) * f) | (cvt_e4m3x2(bf16lo(w[3]) * f, bf16hi(w[3]) * f) << 16);
+    r.x = quant2(w[0], f) | (quant2(w[1], f) << 16);
+    r.y = quant2(w[2], f) | (quant2(w[3], f) << 16);
     return r;
 }
 
@@ -122,112 +143,190 @@ __device__ __forceinline__ uint2 signs8(const uint32_t (&w)[4]) {
     return r;
 }
 
+constexpr int kQStages = 3;                    // SMEM ring depth (tiles in flight per CTA)
+constexpr int kQTileBytes = 128 * 128 * 2;     // one 128 x 128 bf16 tile
+constexpr int kQThreads = 288;                 // 8 consumer warps + 1 TMA producer warp
+constexpr int kQSmem = kQStages * kQTileBytes + 128;
+
 template <unsigned DIRS>
-__global__ void __launch_bounds__(256) quant_tile_kernel(QParams p) {
+__global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
     constexpr bool kRow = (DIRS & MXFP8_ROW) != 0;
     constexpr bool kCol = (DIRS & MXFP8_COL) != 0;
     constexpr bool kB32 = (DIRS & MXFP8_BLOCK32X32) != 0;
+    extern __shared__ uint8_t qsmem_raw[];
     __shared__ int32_t ends_s[kMaxGroups];
     __shared__ int32_t pstart_s[kMaxGroups];
     __shared__ int32_t ptotal_s;
+    __shared__ __align__(8) uint64_t full[kQStages];
+    __shared__ __align__(8) uint64_t empty[kQStages];
+    __shared__ int abort_s;
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 127) & ~uintptr_t(127));
 
     const bool grouped = p.offs != nullptr && p.G > 1;
-    if (grouped && p.blocked) {
-        if (threadIdx.x < 32) build_group_table(p.offs, p.G, p.R, ends_s, pstart_s, &ptotal_s);
-        __syncthreads();
+    if (grouped && p.blocked && threadIdx.x < 32) build_group_table(p.offs, p.G, p.R, ends_s, pstart_s, &ptotal_s);
+    if (threadIdx.x == 256) {
+        for (int s = 0; s < kQStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 8);
+        }
+        abort_s = 0;
+        fence_barrier_init();
+        prefetch_tmap(&xmap);
     }
+    __syncthreads();
+    volatile int* abort_flag = &abort_s;
     const int64_t R = p.R, C = p.C;
     const int64_t Cb = C / kBlk;
     const int64_t ct_row = (C + 127) / 128;                                  // row-scale column tiles
     const int64_t ct_col = grouped ? (int64_t)ptotal_s / 128 : (R + 127) / 128;  // col-scale column tiles
+    const int64_t per_b = p.tiles_r * p.tiles_c;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 8) {
+        // ------------------------------------------------ TMA producer: whole 128x128 tiles, OOB zero-filled
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_phase = 0;
+            for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kQTimeoutNs, abort_flag, p.dev_status)) {
+                    for (int s = 0; s < kQStages; ++s)
+                        if (issued & (1u << s)) {
+                            volatile int no_abort = 0;
+                            mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kQTimeoutNs, &no_abort, nullptr);
+                        }
+                    break;
+                }
+                const int64_t b = t / per_b, rem = t - b * per_b;
+                const int64_t tr = rem / p.tiles_c, tc = rem - tr * p.tiles_c;
+                mbar_arrive_expect_tx(&full[stage], kQTileBytes);
+                tma_load_3d(tiles + stage * kQTileBytes, &xmap, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
+                            &full[stage]);
+                issued |= 1u << stage;
+                last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == kQStages) { stage = 0; phase ^= 1u; }
+            }
+        }
+        return;
+    }
+
     const int wi = warp >> 1, wj = warp & 1;
     const int li = lane >> 3, lj = lane & 7;
+    int stage = 0;
+    uint32_t phase = 0;
 
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const int64_t per_b = p.tiles_r * p.tiles_c;
         const int64_t b = t / per_b;
         const int64_t rem = t - b * per_b;
         const int64_t tr = rem / p.tiles_c, tc = rem - tr * p.tiles_c;
         const int64_t row0 = tr * 128 + wi * 32, col0 = tc * 128 + wj * 64;
-        if (row0 >= R || col0 >= C) continue;  // warp-uniform
-
-        const uint16_t* xb = p.x + b * R * C;
-        const int64_t c8 = col0 + 8 * lj;  // first column of this lane
-        const bool cval = c8 < C;          // C % 32 == 0: 8-column chunks are all-in or all-out
+        if (!mbar_wait_bounded(&full[stage], phase, kQTimeoutNs, abort_flag, p.dev_status)) break;
+        // this warp's 32 x 64 sub-tile: lane rows 8li..8li+7, columns 8lj..8lj+7 (16 bytes each)
+        const uint8_t* src = tiles + stage * kQTileBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
         uint32_t v[8][4];
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) {
-            const int64_t row = row0 + 8 * li + rr;
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (cval && row < R) u = __ldg(reinterpret_cast<const uint4*>(xb + row * C + c8));
+            const uint4 u = *reinterpret_cast<const uint4*>(src + rr * 256);
             v[rr][0] = u.x; v[rr][1] = u.y; v[rr][2] = u.z; v[rr][3] = u.w;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == kQStages) { stage = 0; phase ^= 1u; }
+        if (row0 >= R || col0 >= C) continue;  // warp-uniform
+
+        const int64_t c8 = col0 + 8 * lj;  // first column of this lane
+        const bool cval = c8 < C;          // C % 32 == 0: 8-column chunks are all-in or all-out
+        int wg0 = 0, wg1 = 0;              // groups of the warp's first and last row (warp-uniform)
+        if (grouped && p.blocked) {
+            wg0 = find_group(ends_s, p.G, row0);
+            wg1 = find_group(ends_s, p.G, min64(row0 + 31, R - 1));
+        }
+
+        // magnitude bits of every element (bf16 pairs), shared by both directions
+        uint32_t mg[8][4];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mg[rr][k] = v[rr][k] & 0x7FFF7FFFu;
 
         if constexpr (kRow || kB32) {
-            uint32_t rmax[8];  // per-row amax over this lane's 8 columns (16-bit)
+            // two rows per word: pp[k] = (amax of row 2k, amax of row 2k+1) over this lane's 8 columns
+            uint32_t pp[4];
 #pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                uint32_t m = vmax_u16x2(vmax_u16x2(v[rr][0] & 0x7FFF7FFFu, v[rr][1] & 0x7FFF7FFFu),
-                                        vmax_u16x2(v[rr][2] & 0x7FFF7FFFu, v[rr][3] & 0x7FFF7FFFu));
-                rmax[rr] = max(m & 0xFFFFu, m >> 16);
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t a = vmax_u16x2(vmax_u16x2(mg[2 * k][0], mg[2 * k][1]), vmax_u16x2(mg[2 * k][2], mg[2 * k][3]));
+                const uint32_t c = vmax_u16x2(vmax_u16x2(mg[2 * k + 1][0], mg[2 * k + 1][1]),
+                                              vmax_u16x2(mg[2 * k + 1][2], mg[2 * k + 1][3]));
+                pp[k] = vmax_u16x2(__byte_perm(a, c, 0x5410), __byte_perm(a, c, 0x7632));
             }
             uint32_t s8[8];
             if constexpr (kB32) {
-                // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1)
-                // and 4 lanes down (li, lane bits 3-4)
-                uint32_t m = 0;
-#pragma unroll
-                for (int rr = 0; rr < 8; ++rr) m = max(m, rmax[rr]);
-                m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                const uint32_t s = e8m0_from_absbits(m);
+                // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1), 4 down (li)
+                uint32_t m = vmax_u16x2(vmax_u16x2(pp[0], pp[1]), vmax_u16x2(pp[2], pp[3]));
+                m = shfl_xor_max16x2(m, 1);
+                m = shfl_xor_max16x2(m, 2);
+                m = shfl_xor_max16x2(m, 8);
+                m = shfl_xor_max16x2(m, 16);
+                const uint32_t s = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
 #pragma unroll
                 for (int rr = 0; rr < 8; ++rr) s8[rr] = s;
             } else {
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    uint32_t m = rmax[rr];
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    s8[rr] = e8m0_from_absbits(m);
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t m = shfl_xor_max16x2(pp[k], 1);
+                    m = shfl_xor_max16x2(m, 2);
+                    s8[2 * k] = e8m0_from_absbits(m & 0xFFFFu);
+                    s8[2 * k + 1] = e8m0_from_absbits(m >> 16);
                 }
             }
+            bool nonfinite = false;
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) nonfinite |= s8[rr] == 0xFFu;
+            const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
             uint8_t* qb = p.q_row + b * R * C;
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
                 const int64_t row = row0 + 8 * li + rr;
                 uint2 q = quant8(v[rr], inv_scale_from_e8m0(s8[rr]));
-                if (s8[rr] == 0xFFu) { uint2 sg = signs8(v[rr]); q.x = 0x7F7F7F7Fu | sg.x; q.y = 0x7F7F7F7Fu | sg.y; }
+                if (any_nonfinite && s8[rr] == 0xFFu) {
+                    const uint2 sg = signs8(v[rr]);
+                    q.x = 0x7F7F7F7Fu | sg.x;
+                    q.y = 0x7F7F7F7Fu | sg.y;
+                }
                 if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
             }
-            // scales: one lane per 32-column block writes
-            if (cval && (lj & 3) == 0) {
+            // scales: the 4 lanes of a 32-column block each write two of the 8 rows
+            if (cval) {
                 uint8_t* sb = p.s_row + b * p.s_row_bstride;
                 const int64_t cb = c8 / kBlk;
+                const int q4 = lj & 3;
                 if constexpr (kB32) {
-                    if (li == 0) sb[(row0 / kBlk) * Cb + cb] = (uint8_t)s8[0];
+                    if (li == 0 && q4 == 0) sb[(row0 / kBlk) * Cb + cb] = (uint8_t)s8[0];
                 } else {
-                    int g = 0;
-                    if (grouped && p.blocked) g = find_group(ends_s, p.G, row0 + 8 * li);
+                    // this lane's two rows 2*q4, 2*q4+1 (register selects, no local-memory indexing)
+                    const uint32_t my_s[2] = {q4 == 0 ? s8[0] : q4 == 1 ? s8[2] : q4 == 2 ? s8[4] : s8[6],
+                                              q4 == 0 ? s8[1] : q4 == 1 ? s8[3] : q4 == 2 ? s8[5] : s8[7]};
 #pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) {
+                    for (int h = 0; h < 2; ++h) {
+                        const int rr = 2 * q4 + h;
                         const int64_t row = row0 + 8 * li + rr;
-                        if (row >= R) break;
+                        if (row >= R) continue;
+                        const uint8_t sv = (uint8_t)my_s[h];
                         if (!p.blocked) {
-                            sb[row * Cb + cb] = (uint8_t)s8[rr];
-                        } else if (!grouped) {
-                            sb[blocked_off(row, cb, ct_row)] = (uint8_t)s8[rr];
-                        } else {
-                            while (g < p.G && row >= ends_s[g]) ++g;
-                            if (g < p.G) {
-                                const int64_t start = g ? ends_s[g - 1] : 0;
-                                sb[blocked_off(pstart_s[g] + (row - start), cb, ct_row)] = (uint8_t)s8[rr];
-                            }
+                            sb[row * Cb + cb] = sv;
+                            continue;
                         }
+                        int64_t pr = row;
+                        if (grouped) {
+                            int g = wg0;
+                            if (wg0 != wg1) g = find_group(ends_s, p.G, row);
+                            if (g >= p.G) continue;
+                            pr = pstart_s[g] + (row - (g ? ends_s[g - 1] : 0));
+                        }
+                        const int64_t off = blocked_off(pr, cb, ct_row);
+                        sb[off] = sv;
+                        // last block-column of a row whose K/32 is not a multiple of 4: zero the rest of the word
+                        if (cb == Cb - 1)
+                            for (int64_t z = (Cb & 3); z != 0 && z < 4; ++z) sb[off + z - (Cb & 3) + 1] = 0;
                     }
                 }
             }
@@ -238,20 +337,22 @@ __global__ void __launch_bounds__(256) quant_tile_kernel(QParams p) {
             uint32_t cm[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                uint32_t m = v[0][k] & 0x7FFF7FFFu;
-#pragma unroll
-                for (int rr = 1; rr < 8; ++rr) m = vmax_u16x2(m, v[rr][k] & 0x7FFF7FFFu);
+                uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mg[0][k], mg[1][k]), vmax_u16x2(mg[2][k], mg[3][k])),
+                                        vmax_u16x2(vmax_u16x2(mg[4][k], mg[5][k]), vmax_u16x2(mg[6][k], mg[7][k])));
                 m = shfl_xor_max16x2(m, 8);
-                m = shfl_xor_max16x2(m, 16);
-                cm[k] = m;
+                cm[k] = shfl_xor_max16x2(m, 16);
             }
-            uint8_t* qb = p.q_col + b * R * C;
             uint32_t sc[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 sc[2 * k] = e8m0_from_absbits(cm[k] & 0xFFFFu);
                 sc[2 * k + 1] = e8m0_from_absbits(cm[k] >> 16);
             }
+            bool nonfinite = false;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) nonfinite |= sc[cc] == 0xFFu;
+            const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
+            uint8_t* qb = p.q_col + b * R * C;
             if (cval) {
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
@@ -262,12 +363,13 @@ __global__ void __launch_bounds__(256) quant_tile_kernel(QParams p) {
                     for (int rr = 0; rr < 8; rr += 2) {
                         const float a = (cc & 1) ? bf16hi(v[rr][k]) : bf16lo(v[rr][k]);
                         const float c = (cc & 1) ? bf16hi(v[rr + 1][k]) : bf16lo(v[rr + 1][k]);
-                        w[rr >> 1] = cvt_e4m3x2(a * f, c * f);
+                        const float2 y = mul2(a, c, f);
+                        w[rr >> 1] = cvt_e4m3x2(y.x, y.y);
                     }
                     uint2 q;
                     q.x = w[0] | (w[1] << 16);
                     q.y = w[2] | (w[3] << 16);
-                    if (sc[cc] == 0xFFu) {
+                    if (any_nonfinite && sc[cc] == 0xFFu) {
                         uint32_t sg[4];
 #pragma unroll
                         for (int rr = 0; rr < 8; rr += 2) {
@@ -280,109 +382,74 @@ __global__ void __launch_bounds__(256) quant_tile_kernel(QParams p) {
                     }
                     *reinterpret_cast<uint2*>(qb + (c8 + cc) * R + row0 + 8 * li) = q;
                 }
-                if (li == 0) {
-                    uint8_t* sb = p.s_col + b * p.s_col_bstride;
-                    const int64_t rb = row0 / kBlk;
-                    int64_t pc = rb;
-                    bool ok = true;
-                    if (p.blocked && grouped) {
-                        const int g = find_group(ends_s, p.G, row0);
-                        ok = g < p.G;
-                        if (ok) pc = pstart_s[g] / kBlk + (row0 - (g ? ends_s[g - 1] : 0)) / kBlk;
-                    }
+                // scales: each of the 4 lanes li writes two of this lane-column's 8 columns
+                uint8_t* sb = p.s_col + b * p.s_col_bstride;
+                const int64_t rb = row0 / kBlk;
+                int64_t pc = rb;
+                bool ok = true;
+                if (p.blocked && grouped) {
+                    ok = wg0 < p.G;
+                    if (ok) pc = pstart_s[wg0] / kBlk + (row0 - (wg0 ? ends_s[wg0 - 1] : 0)) / kBlk;
+                }
+                const uint32_t my_s[2] = {li == 0 ? sc[0] : li == 1 ? sc[2] : li == 2 ? sc[4] : sc[6],
+                                          li == 0 ? sc[1] : li == 1 ? sc[3] : li == 2 ? sc[5] : sc[7]};
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const int64_t c = c8 + cc;
-                        if (!p.blocked) sb[c * (R / kBlk) + rb] = (uint8_t)sc[cc];
-                        else if (ok) sb[blocked_off(c, pc, ct_col)] = (uint8_t)sc[cc];
-                    }
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t c = c8 + 2 * li + h;
+                    if (!p.blocked) sb[c * (R / kBlk) + rb] = (uint8_t)my_s[h];
+                    else if (ok) sb[blocked_off(c, pc, ct_col)] = (uint8_t)my_s[h];
                 }
             }
         }
     }
-}
 
-// ---------------------------------------------------------------- padding of blocked layouts
-// Row-grouped blocked scales of a [R x Cb] scale matrix: zero every byte that
-// is not a scale -- the padding rows of each group (up to its next multiple of
-// 128) and the block-columns Cb..4*ct-1.  One thread per padded row.
-__global__ void __launch_bounds__(256) pad_rowgroups_kernel(uint8_t* s, int64_t bstride, const int32_t* offs,
-                                                            int32_t G, int64_t R, int64_t Cb, int64_t rows_bound) {
-    __shared__ int32_t ends_s[kMaxGroups];
-    __shared__ int32_t pstart_s[kMaxGroups];
-    __shared__ int32_t ptotal_s;
-    const bool grouped = offs != nullptr && G > 1;
-    if (grouped) {
-        if (threadIdx.x < 32) build_group_table(offs, G, R, ends_s, pstart_s, &ptotal_s);
-        __syncthreads();
-    }
-    const int64_t ct = (Cb + 3) / 4;
-    const int64_t ptotal = grouped ? ptotal_s : ((R + 127) / 128) * 128;
-    uint8_t* sb = s + blockIdx.y * bstride;
-    for (int64_t pr = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; pr < min(ptotal, rows_bound);
-         pr += (int64_t)gridDim.x * blockDim.x) {
-        int64_t local = pr, size = R;
-        if (grouped) {
-            // group whose padded range holds pr: last g with pstart_s[g] <= pr and a non-empty range
-            int lo = 0, hi = G;
-            while (lo < hi) {
-                int mid = (lo + hi) >> 1;
-                if (pstart_s[mid] <= pr) lo = mid + 1;
-                else hi = mid;
+    // ---- zero padding of the blocked layouts (bytes no tile writes), spread over the CTAs
+    if (p.blocked && !kB32) {
+        const int G_eff = grouped ? p.G : 1;
+        const int64_t units_row = kRow ? (int64_t)p.batch * G_eff : 0;
+        const int64_t units_col = kCol ? (int64_t)p.batch * (G_eff + 1) : 0;
+        const int tid = threadIdx.x;  // 256 consumer threads
+        for (int64_t u = blockIdx.x; u < units_row + units_col; u += gridDim.x) {
+            if (u < units_row) {
+                // padding rows of group g: [P_g + size_g, P_g + ceil(size_g/128)*128), every column tile
+                const int64_t bb = u / G_eff;
+                const int g = (int)(u - bb * G_eff);
+                const int64_t start = grouped ? (g ? ends_s[g - 1] : 0) : 0;
+                const int64_t size = grouped ? ends_s[g] - start : R;
+                const int64_t P = grouped ? pstart_s[g] : 0;
+                const int64_t npad = ((size + 127) / 128) * 128 - size;
+                uint8_t* sb = p.s_row + bb * p.s_row_bstride;
+                for (int64_t i = tid; i < npad * ct_row; i += 256) {
+                    const int64_t pr = P + size + i / ct_row, t = i % ct_row;
+                    *reinterpret_cast<uint32_t*>(sb + ((pr >> 7) * ct_row + t) * 512 + (pr & 31) * 16 +
+                                                 ((pr >> 5) & 3) * 4) = 0u;
+                }
+            } else {
+                const int64_t u2 = u - units_row;
+                const int64_t bb = u2 / (G_eff + 1);
+                const int g = (int)(u2 - bb * (G_eff + 1));
+                uint8_t* sb = p.s_col + bb * p.s_col_bstride;
+                const int64_t rows_p = ((C + 127) / 128) * 128;
+                if (g < G_eff) {
+                    // padding block-columns of group g, every (real) scale row
+                    const int64_t start = grouped ? (g ? ends_s[g - 1] : 0) : 0;
+                    const int64_t size = grouped ? ends_s[g] - start : R;
+                    const int64_t Q = grouped ? pstart_s[g] / kBlk : 0;
+                    const int64_t c0 = Q + size / kBlk, c1 = Q + ((size + 127) / 128) * 4;
+                    for (int64_t i = tid; i < C * (c1 - c0); i += 256) {
+                        const int64_t r = i / (c1 - c0), c = c0 + i % (c1 - c0);
+                        sb[blocked_off(r, c, ct_col)] = 0;
+                    }
+                } else {
+                    // padding rows C .. ceil(C/128)*128 of the scale matrix, every column tile
+                    for (int64_t i = tid; i < (rows_p - C) * ct_col; i += 256) {
+                        const int64_t r = C + i / ct_col, t = i % ct_col;
+                        *reinterpret_cast<uint32_t*>(sb + ((r >> 7) * ct_col + t) * 512 + (r & 31) * 16 +
+                                                     ((r >> 5) & 3) * 4) = 0u;
+                    }
+                }
             }
-            int g = lo - 1;
-            local = pr - pstart_s[g];
-            size = ends_s[g] - (g ? ends_s[g - 1] : 0);
         }
-        const int64_t base = (pr >> 7) * ct * 512 + (pr & 31) * 16 + ((pr >> 5) & 3) * 4;
-        if (local >= size) {
-            for (int64_t t = 0; t < ct; ++t) *reinterpret_cast<uint32_t*>(sb + base + t * 512) = 0u;
-        } else if (Cb & 3) {
-            for (int64_t c = Cb; c < ct * 4; ++c) sb[base + (ct - 1) * 512 + (c & 3)] = 0;
-        }
-    }
-}
-
-// Column-grouped blocked scales of a [Rs x (tokens/32)] scale matrix (Rs = the
-// rows of the transposed operand): zero the padding block-columns of each group
-// and the padding rows Rs..ceil(Rs/128)*128.  One thread per (row, column tile).
-__global__ void __launch_bounds__(256) pad_colgroups_kernel(uint8_t* s, int64_t bstride, const int32_t* offs,
-                                                            int32_t G, int64_t M, int64_t Rs, int64_t tiles_bound) {
-    __shared__ int32_t ends_s[kMaxGroups];
-    __shared__ int32_t pstart_s[kMaxGroups];
-    __shared__ int32_t ptotal_s;
-    const bool grouped = offs != nullptr && G > 1;
-    if (grouped) {
-        if (threadIdx.x < 32) build_group_table(offs, G, M, ends_s, pstart_s, &ptotal_s);
-        __syncthreads();
-    }
-    const int64_t ct = grouped ? ptotal_s / 128 : (M + 127) / 128;
-    const int64_t rows_p = ((Rs + 127) / 128) * 128;
-    uint8_t* sb = s + blockIdx.y * bstride;
-    const int64_t n = rows_p * min(ct, tiles_bound);
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = idx / ct, t = idx - r * ct;
-        const int64_t base = (r >> 7) * ct * 512 + t * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-        if (r >= Rs) {
-            *reinterpret_cast<uint32_t*>(sb + base) = 0u;
-            continue;
-        }
-        // the group owning column tile t, and how many of its 4 block-columns hold scales
-        int64_t valid;
-        if (grouped) {
-            int lo = 0, hi = G;
-            while (lo < hi) {
-                int mid = (lo + hi) >> 1;
-                if (pstart_s[mid] <= t * 128) lo = mid + 1;
-                else hi = mid;
-            }
-            const int g = lo - 1;
-            const int64_t size = ends_s[g] - (g ? ends_s[g - 1] : 0);
-            valid = size / kBlk - (t * 128 - pstart_s[g]) / kBlk;
-        } else {
-            valid = M / kBlk - t * 4;
-        }
-        for (int64_t c = valid > 0 ? valid : 0; c < 4; ++c) sb[base + c] = 0;
     }
 }
 
@@ -399,35 +466,40 @@ __global__ void check_offsets_kernel(const int32_t* offs, int32_t G, int64_t M, 
 }
 
 // ---------------------------------------------------------------- host side
+// x viewed as [batch][R][C] bf16 with 128 x 128 boxes, no swizzle, zero fill outside.
+static bool make_x_map(CUtensorMap* m, const QParams& p) {
+    host::EncodeTiledFn fn = host::encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)p.C, (cuuint64_t)p.R, (cuuint64_t)p.batch};
+    cuuint64_t strides[2] = {(cuuint64_t)(p.C * 2), (cuuint64_t)(p.R * p.C * 2)};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(p.x), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <unsigned DIRS>
+static mxfp8_status_t launch_dirs(const CUtensorMap& m, const QParams& p, int64_t grid, cudaStream_t st) {
+    static std::atomic<int> attr_set[host::kMaxDevices];
+    if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS>), kQSmem, attr_set))
+        return MXFP8_ERR_LAUNCH;
+    quant_tile_kernel<DIRS><<<(unsigned)grid, kQThreads, kQSmem, st>>>(m, p);
+    return host::last_launch_status();
+}
+
 static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t st) {
     if (p.ntiles == 0) return MXFP8_OK;
-    const int sms = host::num_sms();
-    const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)sms * 8);
+    CUtensorMap m;
+    if (!make_x_map(&m, p)) return MXFP8_ERR_DRIVER;
+    const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms() * 2);
     switch (dirs) {
-        case MXFP8_ROW: quant_tile_kernel<MXFP8_ROW><<<grid, 256, 0, st>>>(p); break;
-        case MXFP8_COL: quant_tile_kernel<MXFP8_COL><<<grid, 256, 0, st>>>(p); break;
-        case MXFP8_ROW | MXFP8_COL: quant_tile_kernel<MXFP8_ROW | MXFP8_COL><<<grid, 256, 0, st>>>(p); break;
-        case MXFP8_BLOCK32X32: quant_tile_kernel<MXFP8_BLOCK32X32><<<grid, 256, 0, st>>>(p); break;
+        case MXFP8_ROW: return launch_dirs<MXFP8_ROW>(m, p, grid, st);
+        case MXFP8_COL: return launch_dirs<MXFP8_COL>(m, p, grid, st);
+        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL>(m, p, grid, st);
+        case MXFP8_BLOCK32X32: return launch_dirs<MXFP8_BLOCK32X32>(m, p, grid, st);
         default: return MXFP8_ERR_LAYOUT;
     }
-    return host::last_launch_status();
-}
-
-static mxfp8_status_t pad_rows(uint8_t* s, int64_t bstride, int32_t batch, const int32_t* offs, int32_t G, int64_t R,
-                               int64_t Cb, cudaStream_t st) {
-    const int64_t bound = ((R + 127) / 128 + (offs && G > 1 ? G : 1)) * 128;
-    const int64_t blocks = std::min<int64_t>((bound + 255) / 256, (int64_t)host::num_sms() * 4);
-    pad_rowgroups_kernel<<<dim3((unsigned)blocks, (unsigned)batch), 256, 0, st>>>(s, bstride, offs, G, R, Cb, bound);
-    return host::last_launch_status();
-}
-
-static mxfp8_status_t pad_cols(uint8_t* s, int64_t bstride, int32_t batch, const int32_t* offs, int32_t G, int64_t M,
-                               int64_t Rs, cudaStream_t st) {
-    const int64_t tb = (M + 127) / 128 + (offs && G > 1 ? G : 1);
-    const int64_t n = ((Rs + 127) / 128) * 128 * tb;
-    const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)host::num_sms() * 4);
-    pad_colgroups_kernel<<<dim3((unsigned)blocks, (unsigned)batch), 256, 0, st>>>(s, bstride, offs, G, M, Rs, tb);
-    return host::last_launch_status();
 }
 
 }  // namespace mx
@@ -465,12 +537,6 @@ extern "C" mxfp8_status_t mxfp8_quantize_2d(const void* x_bf16, int64_t M, int64
     p.dev_status = dev_status;
     p.tiles_r = (M + 127) / 128; p.tiles_c = (K + 127) / 128; p.ntiles = p.tiles_r * p.tiles_c;
     if (mxfp8_status_t s = launch_tiles(dirs, p, st); s != MXFP8_OK) return s;
-    if (blocked && row) {
-        if (mxfp8_status_t s = pad_rows(p.s_row, 0, 1, p.offs, p.G, M, K / 32, st); s != MXFP8_OK) return s;
-    }
-    if (blocked && col) {
-        if (mxfp8_status_t s = pad_cols(p.s_col, 0, 1, p.offs, p.G, M, K, st); s != MXFP8_OK) return s;
-    }
     return MXFP8_OK;
 }
 
@@ -503,12 +569,6 @@ extern "C" mxfp8_status_t mxfp8_quantize_3d_experts(const void* w_bf16, int32_t 
     p.dev_status = dev_status;
     p.tiles_r = (N + 127) / 128; p.tiles_c = (K + 127) / 128; p.ntiles = p.tiles_r * p.tiles_c * G;
     if (mxfp8_status_t r = launch_tiles(dirs, p, st); r != MXFP8_OK) return r;
-    if (blocked && row) {
-        if (mxfp8_status_t r = pad_rows(p.s_row, p.s_row_bstride, G, nullptr, 0, N, K / 32, st); r != MXFP8_OK) return r;
-    }
-    if (blocked && col) {
-        if (mxfp8_status_t r = pad_cols(p.s_col, p.s_col_bstride, G, nullptr, 0, N, K, st); r != MXFP8_OK) return r;
-    }
     return MXFP8_OK;
 }
 

@@ -194,6 +194,30 @@ def test_single_direction_matches_fused(mx):
     assert np.array_equal(a[2], c[2]) and np.array_equal(a[3][:n_col], c[3][:n_col])
 
 
+def test_call_from_fresh_host_thread(mx, oracle_lib):
+    """A host thread that has made no CUDA call yet (like an autograd worker)."""
+    import threading
+
+    x = mixed_input(256, 128, seed=77)
+    xd = x.cuda()
+    torch.cuda.synchronize()
+    box = {}
+
+    def work():
+        try:
+            box["res"] = mx.mxfp8_quantize_2d(xd, mx.ROW | mx.COL, mx.SCALES_COMPACT)
+            torch.cuda.synchronize()
+        except Exception as e:  # reported in the main thread
+            box["err"] = e
+
+    th = threading.Thread(target=work)
+    th.start()
+    th.join()
+    assert "err" not in box, box.get("err")
+    qo, so = oracle_lib.quantize_rows(u16(x))
+    assert np.array_equal(u8(box["res"][0]), qo) and np.array_equal(u8(box["res"][1]), so)
+
+
 def test_argument_errors(mx):
     x = torch.zeros((64, 48), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(mx.Mxfp8Error, match="ALIGN"):
