@@ -57,7 +57,9 @@ struct Cfg {
     static constexpr int kOffB = kStages * kABytes;
     static constexpr int kOffSfa = kOffB + kStages * kBBytes;
     static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
-    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+    static constexpr int kOffStage = kOffSfb + kStages * kSfbBytes;  // epilogue staging: 4 warps x 32 rows x 128 B
+    static constexpr int kStageBytes = 4 * 32 * 128;
+    static constexpr int kOffBar = kOffStage + kStageBytes;
     static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
     static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
 };
@@ -320,29 +322,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + acc * BN;
+                // scale tiles of stage st: SMEM -> the stage's own tensor-memory columns
+                auto copy_scales = [&](int st) {
+                    const uint32_t sfa_t = tmem + C::kSfCol0 + st * C::kSfCols;
+                    const uint32_t sfa_s = smem_u32(smem + C::kOffSfa + st * C::kSfaBytes);
+                    const uint32_t sfb_s = smem_u32(smem + C::kOffSfb + st * C::kSfbBytes);
+                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sfa_s, 0, 128, 0));
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        tc_cp_32x128b_warpx4(sfa_t + 4 + 4 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
+                };
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
-                    if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    const int cur = stage;
+                    if (!mbar_wait_bounded(&full[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem + C::kSfCol0 + stage * C::kSfCols;
+                    copy_scales(cur);
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    const uint32_t sfa_t = tmem + C::kSfCol0 + cur * C::kSfCols;
                     const uint32_t sfb_t = sfa_t + 4;
-                    const uint32_t a_s = smem_u32(smem + stage * C::kABytes);
-                    const uint32_t b_s = smem_u32(smem + C::kOffB + stage * C::kBBytes);
-                    const uint32_t sfa_s = smem_u32(smem + C::kOffSfa + stage * C::kSfaBytes);
-                    const uint32_t sfb_s = smem_u32(smem + C::kOffSfb + stage * C::kSfbBytes);
-                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sfa_s, 0, 128, 0));
-#pragma unroll
-                    for (int j = 0; j < BN / 128; ++j) tc_cp_32x128b_warpx4(sfb_t + 4 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
+                    const uint32_t a_s = smem_u32(smem + cur * C::kABytes);
+                    const uint32_t b_s = smem_u32(smem + C::kOffB + cur * C::kBBytes);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k) {
                         const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
                         const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
                         tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, k, k), sfa_t, sfb_t, (kt | k) != 0);
                     }
-                    tc_commit(&empty[stage]);
-                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    tc_commit(&empty[cur]);
                 }
                 if (!ok) break;
                 tc_commit(&tfull[acc]);
@@ -356,12 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------ epilogue
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
+            uint8_t* stg = smem + C::kOffStage + (warp - 2) * (32 * 128);
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
                 const TileInfo ti = tile_info<BN>(p, t, ends_s, pstart_s, ptotal);
                 const bool row_ok = r < ti.valid_rows;
                 __nv_bfloat16* orow = ti.out + (int64_t)r * ti.ldo;
+                __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo;  // first row of this warp
                 if (ti.k_tiles == 0) {
                     if (row_ok)
                         for (int c = 0; c < ti.valid_cols; c += 8)
@@ -389,12 +400,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[acc]);
-                if (row_ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow);
+                // Coalesced stores: per 64-column chunk, each lane parks its row's eight 16-byte pieces in
+                // the warp's 32 x 128 B staging buffer (piece j of row r at slot j ^ (r & 7): no bank
+                // conflicts), then every store instruction writes 4 full 128-byte row segments.
+                const int vrows = ti.valid_rows - quarter * 32;  // rows of this warp inside the group
 #pragma unroll
-                    for (int i = 0; i < BN / 8; ++i)
-                        if (i * 8 < ti.valid_cols)
-                            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                for (int ch = 0; ch < BN / 64; ++ch) {
+                    if (ch * 64 >= ti.valid_cols) break;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) * 16),
+                                     make_uint4(packed[ch * 32 + 4 * j], packed[ch * 32 + 4 * j + 1],
+                                                packed[ch * 32 + 4 * j + 2], packed[ch * 32 + 4 * j + 3]));
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rl = (lane >> 3) + 4 * i, piece = lane & 7;
+                        const uint4 val = ld_shared_v4(stg + rl * 128 + ((piece ^ (rl & 7)) * 16));
+                        if (rl < vrows && ch * 64 + piece * 8 < ti.valid_cols)
+                            *reinterpret_cast<uint4*>(wout + (int64_t)rl * ti.ldo + ch * 64 + piece * 8) = val;
+                    }
+                    __syncwarp();
                 }
                 if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
             }
