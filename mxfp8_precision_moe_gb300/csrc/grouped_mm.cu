@@ -434,6 +434,366 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+
+// ============================================================================================
+// CTA-pair variant (cluster of 2, tcgen05 cta_group::2): a 256 x 256 output tile per pair.
+// Each CTA stages its own 128 rows of A and its own 128 rows of B (half of N) per k-tile, so a
+// stage is 33.5 KB instead of 49.5 KB and the ring holds 5 stages; the even CTA issues one
+// M=256 x N=256 x K=32 MMA per 32-wide K block that reads A and B from both CTAs' shared
+// memory and writes rows 0-127 to its own tensor memory, rows 128-255 to the odd CTA's.
+// Every copy of the pair completes on the even CTA's stage barrier (TMA cta_group::2 form),
+// so the scale tiles are moved by TMA as well (tensor maps over the scale buffers, 512-byte
+// boxes).  Stage and accumulator release are multicast commits to both CTAs; the odd CTA's
+// epilogue reports a drained accumulator to the even CTA with a remote mbarrier arrive.
+// ============================================================================================
+constexpr int kPairStages = 5;
+
+struct CfgPair {
+    static constexpr int BN = 256;
+    static constexpr int kStages = kPairStages;
+    static constexpr int kABytes = BM * BK;          // this CTA's 128 rows of A
+    static constexpr int kBBytes = 128 * BK;         // this CTA's 128 rows of B
+    static constexpr int kSfaBytes = 512;
+    static constexpr int kSfbBytes = 2 * 512;        // both 128-row scale tiles of the 256 B rows
+    static constexpr int kTx = 2 * (kABytes + kBBytes + kSfaBytes + kSfbBytes);  // both CTAs' bytes
+    static constexpr int kSfCols = 4 + BN / 32;
+    static constexpr int kSfCol0 = BN;
+    static constexpr int kTmemCols = 512;
+    static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "tensor memory overflow");
+    static constexpr int kOffB = kStages * kABytes;
+    static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+    static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
+    static constexpr int kOffStage = kOffSfb + kStages * kSfbBytes;
+    static constexpr int kStageBytes = 4 * 32 * 128;
+    static constexpr int kOffBar = kOffStage + kStageBytes;
+    static constexpr int kBarBytes = (2 * kStages + 2 + 1) * 8 + 16;
+    static constexpr int kSmem = kOffBar + kBarBytes + 1024;
+};
+
+struct PairTile {
+    int g;
+    int64_t a_row, b_row, a_x0;
+    int k_tiles;
+    int64_t sfa_chunk, sfb_chunk[2];  // 512-byte scale tiles of k-tile 0 (index = byte offset / 512)
+    __nv_bfloat16* out;               // first element of this CTA's 128 rows
+    int64_t ldo;
+    int valid_rows, valid_cols;
+};
+
+// Tile t of the pair schedule, seen from CTA `half` (0: rows 0-127 of the pair tile, 1: 128-255).
+__device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, int half, const int32_t* ends_s,
+                                              const int32_t* pstart_s, const int32_t* tstart_s, int64_t ptotal) {
+    constexpr int BN = 256;
+    PairTile ti;
+    const int64_t ntb = (p.nb + BN - 1) / BN;
+    const int64_t last_chunk = (p.nb + 127) / 128 - 1;
+    if (p.mode == ROWGROUPED) {
+        int lo = 0, hi = p.G;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((int64_t)tstart_s[mid] * ntb <= t) lo = mid + 1;
+            else hi = mid;
+        }
+        const int g = lo - 1;
+        const int64_t start = g ? ends_s[g - 1] : 0, size = ends_s[g] - start;
+        int64_t m2, n;
+        band_split(t - (int64_t)tstart_s[g] * ntb, (size + 255) / 256, ntb, m2, n);
+        const int64_t rows0 = m2 * 256 + half * 128;
+        ti.g = g;
+        ti.a_row = start + rows0;
+        ti.b_row = (int64_t)g * p.nb + n * BN + half * 128;
+        ti.a_x0 = 0;
+        ti.k_tiles = (int)((p.kc + BK - 1) / BK);
+        const int64_t cA = min64(2 * m2 + half, (size + 127) / 128 - 1);  // clamp: rows past the group are masked
+        ti.sfa_chunk = (pstart_s[g] / 128 + cA) * p.sfa_ct;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t ch = min64(n * 2 + j, last_chunk);
+            ti.sfb_chunk[j] = (int64_t)g * (p.sfb_estride / 512) + ch * p.sfb_ct;
+        }
+        ti.out = p.out + ti.a_row * p.ldo + n * BN;
+        ti.ldo = p.ldo;
+        ti.valid_rows = (int)max64(-1, min64(128, size - rows0));
+        ti.valid_cols = (int)min64(BN, p.nb - n * BN);
+    } else {
+        const int64_t nta2 = (p.na + 255) / 256;
+        const int64_t per_g = nta2 * ntb;
+        const int g = (int)(t / per_g);
+        int64_t m2, n;
+        band_split(t - g * per_g, nta2, ntb, m2, n);
+        const int64_t start = g ? ends_s[g - 1] : 0, size = ends_s[g] - start;
+        const int64_t ct = ptotal / 128, kt0 = pstart_s[g] / 128;
+        const int64_t rows0 = m2 * 256 + half * 128;
+        ti.g = g;
+        ti.a_row = rows0;
+        ti.b_row = n * BN + half * 128;
+        ti.a_x0 = start;
+        ti.k_tiles = (int)((size + BK - 1) / BK);
+        const int64_t cA = min64(2 * m2 + half, (p.na + 127) / 128 - 1);
+        ti.sfa_chunk = cA * ct + kt0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) ti.sfb_chunk[j] = min64(n * 2 + j, last_chunk) * ct + kt0;
+        ti.out = p.out + ((int64_t)g * p.na + rows0) * p.nb + n * BN;
+        ti.ldo = p.nb;
+        ti.valid_rows = (int)max64(-1, min64(128, p.na - rows0));
+        ti.valid_cols = (int)min64(BN, p.nb - n * BN);
+    }
+    return ti;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                           const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
+                           const GemmParams p) {
+    using C = CfgPair;
+    constexpr int BN = 256;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ int32_t ends_s[kMaxGroups];
+    __shared__ int32_t pstart_s[kMaxGroups];
+    __shared__ int32_t tstart_s[kMaxGroups];  // ROWGROUPED: first pair tile (256 rows) of each group
+    __shared__ int32_t ptotal_s;
+    __shared__ int32_t bad_s;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* tfull = empty + C::kStages;
+    uint64_t* tempty = tfull + 1;
+    uint64_t* drain = tempty + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
+    const int half = (int)(rank & 1u);
+    const bool leader = half == 0;
+
+    if (warp == 0) {
+        const int G = p.G;
+        const int per = (G + 31) / 32;
+        const int g0 = lane * per, g1 = min(G, g0 + per);
+        const int32_t Mc = (int32_t)p.M;
+        int32_t mx = 0;
+        for (int g = g0; g < g1; ++g) mx = max(mx, min(max(p.offs[g], 0), Mc));
+        int32_t incl = mx;
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl = max(incl, o);
+        }
+        int32_t run = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) run = 0;
+        int32_t prev = run, psum = 0, tsum = 0, bad = 0;
+        for (int g = g0; g < g1; ++g) {
+            const int32_t e = max(prev, min(max(p.offs[g], 0), Mc));
+            ends_s[g] = e;
+            if (p.mode == KGROUPED && (e - prev) % 32 != 0) bad = 1;
+            psum += ((e - prev + 127) / 128) * 128;
+            tsum += (e - prev + 255) / 256;
+            prev = e;
+        }
+        int32_t sincl = psum, tincl = tsum;
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, sincl, d);
+            const int32_t q = __shfl_up_sync(0xffffffffu, tincl, d);
+            if (lane >= d) {
+                sincl += o;
+                tincl += q;
+            }
+        }
+        int32_t sexcl = sincl - psum, texcl = tincl - tsum;
+        prev = run;
+        for (int g = g0; g < g1; ++g) {
+            pstart_s[g] = sexcl;
+            tstart_s[g] = texcl;
+            const int32_t e = ends_s[g];
+            sexcl += ((e - prev + 127) / 128) * 128;
+            texcl += (e - prev + 255) / 256;
+            prev = e;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 31) ptotal_s = sincl;
+        if (lane == 0) {
+            bad_s = bad;
+            abort_s = 0;
+            prefetch_tmap(&tmap_a);
+            prefetch_tmap(&tmap_b);
+            prefetch_tmap(&tmap_sfa);
+            prefetch_tmap(&tmap_sfb);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int s = 0; s < C::kStages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], 1);
+            }
+            mbar_init(tfull, 1);
+            mbar_init(tempty, 8);  // 4 epilogue warps in each CTA of the pair
+            mbar_init(drain, 1);
+            fence_barrier_init();
+        }
+        __syncwarp();
+        tmem_alloc_pair(&tmem_base_s, C::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer may signal this CTA's barriers from here on
+    tc_fence_after();
+
+    const uint32_t tmem = tmem_base_s;
+    volatile int* abort_flag = &abort_s;
+    const int64_t ptotal = ptotal_s;
+    if (bad_s) {
+        if (threadIdx.x == 0 && leader) report(p.dev_status, MXFP8_ERR_OFFSETS);
+    } else {
+        const int64_t ntb = (p.nb + BN - 1) / BN;
+        int64_t ntiles;
+        if (p.mode == ROWGROUPED) {
+            ntiles = (int64_t)tstart_s[p.G - 1] + (ends_s[p.G - 1] - (p.G > 1 ? ends_s[p.G - 2] : 0) + 255) / 256;
+            ntiles *= ntb;
+        } else {
+            ntiles = (int64_t)p.G * ((p.na + 255) / 256) * ntb;
+        }
+        const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t t = cid; t < ntiles; t += ncl) {
+                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal);
+                bool ok = true;
+                for (int kt = 0; kt < ti.k_tiles; ++kt) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = cluster_addr(&full[stage], 0);  // the even CTA's stage barrier
+                    if (leader) mbar_arrive_expect_tx(&full[stage], C::kTx);
+                    const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kt * BK);
+                    tma_load_2d_pair(smem + stage * C::kABytes, &tmap_a, kx, (int32_t)ti.a_row, fb);
+                    tma_load_2d_pair(smem + C::kOffB + stage * C::kBBytes, &tmap_b, kx, (int32_t)ti.b_row, fb);
+                    tma_load_2d_pair(smem + C::kOffSfa + stage * C::kSfaBytes, &tmap_sfa, 0,
+                                     (int32_t)(2 * (ti.sfa_chunk + kt)), fb);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        tma_load_2d_pair(smem + C::kOffSfb + stage * C::kSfbBytes + 512 * j, &tmap_sfb, 0,
+                                         (int32_t)(2 * (ti.sfb_chunk[j] + kt)), fb);
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+            }
+        } else if (warp == 1 && lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (even CTA only)
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            constexpr uint32_t idesc0 = idesc_mxf8(256, BN, 0, 0);
+            for (int64_t t = cid; t < ntiles && ok; t += ncl) {
+                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal);
+                if (ti.k_tiles == 0) continue;
+                if (!mbar_wait_bounded(tempty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
+                tc_fence_after();
+                for (int kt = 0; kt < ti.k_tiles; ++kt) {
+                    const int cur = stage;
+                    if (!mbar_wait_bounded(&full[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    const uint32_t sfa_t = tmem + C::kSfCol0 + cur * C::kSfCols;
+                    const uint32_t sfb_t = sfa_t + 4;
+                    tc_cp_pair_32x128b_warpx4(sfa_t, smem_desc(smem_u32(smem + C::kOffSfa + cur * C::kSfaBytes), 0, 128, 0));
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        tc_cp_pair_32x128b_warpx4(
+                            sfb_t + 4 * j, smem_desc(smem_u32(smem + C::kOffSfb + cur * C::kSfbBytes + 512 * j), 0, 128, 0));
+                    const uint32_t a_s = smem_u32(smem + cur * C::kABytes);
+                    const uint32_t b_s = smem_u32(smem + C::kOffB + cur * C::kBBytes);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k) {
+                        const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
+                        const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
+                        tc_mma_pair_mxf8(tmem, ad, bd, idesc0 | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa_t, sfb_t,
+                                         (kt | k) != 0);
+                    }
+                    tc_commit_pair(&empty[cur], 0x3);
+                }
+                if (!ok) break;
+                tc_commit_pair(tfull, 0x3);
+                acc_phase ^= 1u;
+            }
+            tc_commit_pair(drain, 0x1);
+            volatile int no_abort = 0;
+            mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
+        } else if (warp >= 2) {
+            // ------------------------------------------------ epilogue (both CTAs: own 128 rows)
+            const int quarter = warp & 3;
+            uint8_t* stg = smem + C::kOffStage + (warp - 2) * (32 * 128);
+            const uint32_t tempty_leader = cluster_addr(tempty, 0);
+            uint32_t acc_phase = 0;
+            for (int64_t t = cid; t < ntiles; t += ncl) {
+                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal);
+                __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo;
+                const int vrows = ti.valid_rows - quarter * 32;
+                if (ti.k_tiles == 0) {
+                    for (int rl = 0; rl < 32; ++rl)
+                        if (rl < vrows)
+                            for (int c = lane * 8; c < ti.valid_cols; c += 256)
+                                *reinterpret_cast<uint4*>(wout + (int64_t)rl * ti.ldo + c) = make_uint4(0, 0, 0, 0);
+                    continue;
+                }
+                if (!mbar_wait_bounded(tfull, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+                acc_phase ^= 1u;
+                tc_fence_after();
+                uint32_t packed[BN / 2];
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+                for (int c = 0; c < BN; c += 64) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(taddr + c, v0);
+                    tmem_ld_32x32b_x32(taddr + c + 32, v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        packed[c / 2 + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+                        packed[c / 2 + 16 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader);
+#pragma unroll
+                for (int ch = 0; ch < BN / 64; ++ch) {
+                    if (ch * 64 >= ti.valid_cols) break;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) * 16),
+                                     make_uint4(packed[ch * 32 + 4 * j], packed[ch * 32 + 4 * j + 1],
+                                                packed[ch * 32 + 4 * j + 2], packed[ch * 32 + 4 * j + 3]));
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rl = (lane >> 3) + 4 * i, piece = lane & 7;
+                        const uint4 val = ld_shared_v4(stg + rl * 128 + ((piece ^ (rl & 7)) * 16));
+                        if (rl < vrows && ch * 64 + piece * 8 < ti.valid_cols)
+                            *reinterpret_cast<uint4*>(wout + (int64_t)rl * ti.ldo + ch * 64 + piece * 8) = val;
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // neither CTA frees tensor memory or exits while the pair still works
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, C::kTmemCols);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 // 2D uint8 tensor [rows][cols] (row pitch = cols bytes), box = box_rows x 128 bytes, 128-byte swizzle.
 static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
@@ -464,6 +824,70 @@ static mxfp8_status_t launch_gemm(const void* a, int64_t a_rows, int64_t a_cols,
 
 static uint64_t default_timeout_ns() { return 2000000000ull; }
 
+// Kernel choice (measured on the 8-expert Scout-like workload, TFLOP/s single / pair):
+// fwd 2890 / 2780, dgrad 2890 / 2890, wgrad 2468 / 2540.  The pair kernel pads ragged token
+// groups to 256 rows (vs 128), which costs the forward more than its smaller stages save; the
+// wgrad's groups own whole output matrices, so it takes the pair kernel.
+constexpr bool kPairForRowGrouped = false;
+constexpr bool kPairForKGrouped = true;
+
+// A scale buffer as [bytes/256][256] uint8, 2 x 256 B boxes (= one 512-byte scale tile).
+static bool make_scale_map(CUtensorMap* m, const void* base, int64_t bytes) {
+    host::EncodeTiledFn fn = host::encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {256, (cuuint64_t)(bytes / 256)};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, 2};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int max_pair_clusters(const cudaLaunchConfig_t& cfg) {
+    static std::atomic<int> cache[host::kMaxDevices];
+    const int d = host::current_device();
+    if (d < 0 || d >= host::kMaxDevices) return 1;
+    int v = cache[d].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaOccupancyMaxActiveClusters(&v, grouped_mm_pair_kernel, &cfg) != cudaSuccess || v <= 0)
+            v = host::num_sms() / 2;
+        cudaGetLastError();
+        cache[d].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// sfa_bytes / sfb_bytes: extents of the scale buffers the maps may address (the ABI's sizing bounds).
+static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
+                                  int64_t b_cols, int64_t sfa_bytes, int64_t sfb_bytes, GemmParams& p,
+                                  int64_t pair_tiles_bound, cudaStream_t st) {
+    using C = CfgPair;
+    CUtensorMap ma, mb, msa, msb;
+    if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, 128) ||
+        !make_scale_map(&msa, p.sfa, sfa_bytes) || !make_scale_map(&msb, p.sfb, sfb_bytes))
+        return MXFP8_ERR_DRIVER;
+    static std::atomic<int> attr_set[host::kMaxDevices];
+    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_pair_kernel), C::kSmem, attr_set))
+        return MXFP8_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2 * host::num_sms() / 2);
+    const int clusters = (int)max64(1, min64(pair_tiles_bound, max_pair_clusters(cfg)));
+    cfg.gridDim = dim3(2 * clusters);
+    if (cudaLaunchKernelEx(&cfg, grouped_mm_pair_kernel, ma, mb, msa, msb, p) != cudaSuccess) return MXFP8_ERR_LAUNCH;
+    return host::last_launch_status();
+}
+
 // fwd and dgrad: token operand tok_q [M, Kc], expert operand ex_q [G, Nb, Kc].
 static mxfp8_status_t rowgrouped(const void* tok_q, const void* tok_s, const void* ex_q, const void* ex_s,
                                  const int32_t* offs, int32_t G, int64_t M, int64_t Nb, int64_t Kc, void* out,
@@ -493,6 +917,12 @@ static mxfp8_status_t rowgrouped(const void* tok_q, const void* tok_s, const voi
     p.mode = ROWGROUPED;
     p.dev_status = dev_status;
     p.timeout_ns = default_timeout_ns();
+    if (Nb >= 256 && kPairForRowGrouped) {
+        const int64_t bound = ((M + 255) / 256 + G) * ((Nb + 255) / 256);
+        const int64_t sfa_bytes = ((M + 127) / 128 + G) * 128 * p.sfa_ct * 4;
+        return launch_pair(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, sfa_bytes, (int64_t)G * p.sfb_estride, p, bound,
+                           st);
+    }
     if (Nb >= 256) {
         const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 255) / 256);
         return launch_gemm<256>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st);
@@ -549,6 +979,12 @@ extern "C" mxfp8_status_t mxfp8_grouped_mm_wgrad(const void* doutT_q, const void
     p.mode = KGROUPED;
     p.dev_status = dev_status;
     p.timeout_ns = default_timeout_ns();
+    if (K >= 256 && kPairForKGrouped) {
+        const int64_t bound = (int64_t)G * ((N + 255) / 256) * ((K + 255) / 256);
+        const int64_t tiles_m = (M + 127) / 128 + G;
+        return launch_pair(doutT_q, N, M, aT_q, K, M, ((N + 127) / 128) * 128 * tiles_m * 4,
+                           ((K + 127) / 128) * 128 * tiles_m * 4, p, bound, st);
+    }
     if (K >= 256) {
         const int64_t bound = (int64_t)G * ((N + BM - 1) / BM) * ((K + 255) / 256);
         return launch_gemm<256>(doutT_q, N, M, aT_q, K, M, p, bound, st);
