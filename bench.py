@@ -48,6 +48,33 @@ L2_BYTES = 129 * 2 ** 20
 FWD_TRAFFIC = {"bytes": 767414016, "src_sha": "b50fc714afeb0665"}
 
 
+WORKLOAD_TEXT = {
+    "scout": WORKLOAD,
+    "imbalanced": "Fine-grained imbalanced experts fwd+bwd: G=16, K=7168, N=2048, M=32768, group 1 = 13120 tokens, "
+                  "groups 0/7/15 empty, 1% x100 activation outliers",
+    "swiglu": "SwiGLU routed expert fwd+bwd GEMMs: G=2, M=65600 (39360/26240), gate/up W[2,8192,5120], "
+              "down W[2,5120,8192]; 9 grouped GEMMs, synthetic stand-ins for the SwiGLU intermediates",
+    "tiny": "Tiny: G=2, A[256,256], offs [128,256], W[2,128,256] (latency-bound; parity case)",
+}
+
+
+def workload_parts(name: str, dev) -> list:
+    """The grouped-GEMM problems one step of a workload runs (each: quantize A, W, dOut; fwd, dgrad, wgrad)."""
+    from mxfp8_precision_moe_gb300 import synth
+
+    if name in ("scout", "imbalanced", "tiny"):
+        return [synth.workload(name, seed=0, device=dev)]
+    s = synth.workload("swiglu", seed=0, device=dev)
+    G, M, D, H = s["G"], s["M"], s["D"], s["H"]
+    h = synth.randn_bf16((M, H), 1.0, seed=50, device=dev)      # stands in for silu(x Wg^T) * (x Wu^T)
+    dh1 = synth.randn_bf16((M, H), 1e-3, seed=51, device=dev)   # stands in for the gate-branch gradient
+    dh3 = synth.randn_bf16((M, H), 1e-3, seed=52, device=dev)   # stands in for the up-branch gradient
+    common = dict(G=G, M=M, sizes=s["sizes"], offs=s["offs"])
+    return [dict(common, N=H, K=D, A=s["x"], W=s["Wg"], dOut=dh1),
+            dict(common, N=H, K=D, A=s["x"], W=s["Wu"], dOut=dh3),
+            dict(common, N=D, K=H, A=h, W=s["Wd"], dOut=s["dY"])]
+
+
 def kernel_src_sha() -> str:
     h = hashlib.sha256()
     for f in ("grouped_mm.cu", "common.cuh"):
@@ -65,6 +92,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--no-baseline", action="store_true", help="skip the cuBLAS bf16 comparison leg")
+    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "tiny", "sweep"],
+                    help="scout (default, the reported line); the others are extra measurements")
     return ap.parse_args()
 
 
@@ -217,6 +246,40 @@ class Step:
         self.mx.read_status(self.status, "bench step")
 
 
+class StepGroup:
+    """Several grouped-GEMM problems run back to back as one step (the SwiGLU expert's three)."""
+
+    def __init__(self, parts: list, device):
+        self.parts = [Step(w, device) for w in parts]
+        self.calls, self.gemm_flops, self.bytes, self.launches = [], {}, {}, {}
+        for i, st in enumerate(self.parts):
+            for name, fn, argv in st.calls:
+                key = f"p{i}.{name}"
+                self.calls.append((key, fn, argv))
+                self.launches[key] = st.launches[name]
+                if name in st.gemm_flops:
+                    self.gemm_flops[key] = st.gemm_flops[name]
+                else:
+                    self.bytes[key] = st.bytes[name]
+        self.flops = sum(st.flops for st in self.parts)
+        p0 = self.parts[0]
+        self.G, self.M, self.N, self.K, self.mx = p0.G, p0.M, p0.N, p0.K, p0.mx
+
+    def run(self, stream, events=None):
+        for name, fn, args in self.calls:
+            if events is not None:
+                events[name][0].record(stream)
+            rc = fn(*args, ctypes.c_void_p(stream.cuda_stream))
+            if rc != 0:
+                raise RuntimeError(f"{name}: {self.mx._lib.STATUS_NAMES.get(rc, rc)}")
+            if events is not None:
+                events[name][1].record(stream)
+
+    def check_status(self):
+        for st in self.parts:
+            st.check_status()
+
+
 # ---------------------------------------------------------------- oracle sample (CPU baseline / reference arm)
 def _bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -280,8 +343,10 @@ def run_native(args, rank, world, local):
 
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
-    w = synth.workload("scout", seed=0, device=dev)
-    step = Step(w, dev)
+    parts = workload_parts(args.workload, dev)
+    w = parts[0]
+    step = Step(w, dev) if len(parts) == 1 else StepGroup(parts, dev)
+    single = isinstance(step, Step)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(args.warmup, 3)):
@@ -319,7 +384,7 @@ def run_native(args, rank, world, local):
 
     # bf16 baseline: per-group cuBLAS torch.mm loop for the forward (same bf16 inputs)
     base = None
-    if rank == 0 and not args.no_baseline:
+    if rank == 0 and not args.no_baseline and single:
         ends = np.cumsum(w["sizes"])
         out_b = torch.empty_like(step.out)
 
@@ -344,7 +409,7 @@ def run_native(args, rank, world, local):
 
     # end to end: host (pinned) inputs copied in and results copied out inside every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and single:
         hA, hW, hD = (t.cpu().pin_memory() for t in (step.A, step.W, step.D))
         hoffs = step.offs.cpu().pin_memory()
         ho, hdA, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (step.out, step.dA, step.dW))
@@ -379,9 +444,10 @@ def run_native(args, rank, world, local):
         return None
     ms_step = ms / args.steps
     fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
-    fwd_ms = per["fwd"]
-    achieved = step.gemm_flops["fwd"] / fwd_ms / 1e9
-    traffic = FWD_TRAFFIC["bytes"] if FWD_TRAFFIC["src_sha"] == kernel_src_sha() else None
+    fwd_key = "fwd" if single else "p0.fwd"
+    fwd_ms = per[fwd_key]
+    achieved = step.gemm_flops[fwd_key] / fwd_ms / 1e9
+    traffic = FWD_TRAFFIC["bytes"] if (FWD_TRAFFIC["src_sha"] == kernel_src_sha() and args.workload == "scout") else None
     kernels = {}
     for n in names:
         d = {"ms": round(per[n], 4)}
@@ -405,12 +471,13 @@ def run_native(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "e4m3",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "G": step.G, "M": step.M, "N": step.N, "K": step.K,
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "G": step.G, "M": step.M, "N": step.N, "K": step.K,
                    "group_sizes": list(map(int, w["sizes"])), "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({L2_BYTES // 2**20} MiB): A, W, dOut = "
-                         f"{(step.A.numel() + step.W.numel() + step.D.numel()) * 2 // 2**20} MiB bf16 per step",
+                         f"{sum((p['A'].numel() + p['W'].numel() + p['dOut'].numel()) * 2 for p in parts) // 2**20} "
+                         "MiB bf16 per step" if args.workload != "tiny" else "tiny: L2-resident (latency-bound case)",
                    "frac_fp8_peak_step": round(step.flops / ms_step / 1e9 / fp8_peak, 3)},
-        "roofline": {"bound": "tensor", "kernel": "grouped_mm_fwd", "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": "grouped_mm_fwd" + ("" if single else " (gate)"), "achieved": round(achieved, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 3),
                      "traffic": traffic,
                      "peak_note": f"{pk['src']} sustained bf16 {pk['bf16_sus']} TFLOP/s x {FP8_OVER_BF16} "
@@ -431,10 +498,14 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
+    if args.workload == "sweep":
+        if rank == 0:
+            print(json.dumps(run_sweep(args)), flush=True)
+        return
     res = run_native(args, rank, world, local)
     if rank == 0 and res is not None:
         line, w = res
-        if not args.no_cpu and world == 1:
+        if not args.no_cpu and world == 1 and args.workload == "scout":
             w_cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in w.items()}
             rate, n, el = oracle_rate(w_cpu, 15.0)
             line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
@@ -444,6 +515,72 @@ def main():
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
+
+
+def run_sweep(args) -> dict:
+    """Quantization bandwidth over the sweep shapes: bf16 [M,K] row, column, row+column (one read) and
+    32x32 blocks, plus 3D expert weights [16,8192,5120] plain, transposed and both; GB/s of
+    algorithmic bytes (2 read + per direction 1 code + 1/32 scale byte per element)."""
+    import mxfp8_precision_moe_gb300 as mx
+    from mxfp8_precision_moe_gb300 import synth
+
+    L = mx.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    stream = torch.cuda.current_stream(dev)
+    sp = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    rows = []
+
+    def time_call(fn, argv, nbytes, label, shape):
+        for _ in range(3):
+            fn(*argv, ctypes.c_void_p(stream.cuda_stream))
+        torch.cuda.synchronize()
+        n = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            rc = fn(*argv, ctypes.c_void_p(stream.cuda_stream))
+            if rc != 0:
+                raise RuntimeError(f"{label}: status {rc}")
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        gbs = nbytes / ms / 1e6
+        rows.append({"shape": shape, "dirs": label, "us": round(ms * 1e3, 1), "gbs": round(gbs, 1),
+                     "frac_hbm": round(gbs / pk["hbm"], 3)})
+
+    for M in synth.SWEEP_M:
+        for K in synth.SWEEP_K:
+            x = synth.log_uniform_rows(M, K, seed=M + K, device=dev)
+            u8 = lambda *shape: torch.empty(shape, dtype=torch.uint8, device=dev)
+            q, qT = u8(M, K), u8(K, M)
+            s_r, s_c = u8(mx.mxfp8_scale_bytes(M, K, 1, 1)), u8(mx.mxfp8_scale_bytes_colgroups(K, M, 1))
+            s32 = u8(M // 32, K // 32)
+            E = M * K
+            for label, dirs, lay, out in (("row", 1, 1, (q, s_r, None, None)), ("col", 2, 1, (None, None, qT, s_c)),
+                                          ("row+col", 3, 1, (q, s_r, qT, s_c)), ("32x32", 4, 0, (q, s32, None, None))):
+                nb = E * (2 + 1 + 1 / 32) if label in ("row", "col") else \
+                    E * (2 + 2 + 2 / 32) if label == "row+col" else E * (2 + 1 + 1 / 1024)
+                time_call(L.mxfp8_quantize_2d, (sp(x), M, K, dirs, lay, None, 0, *[sp(t) for t in out], None), nb,
+                          label, [M, K])
+            del x, q, qT, s_r, s_c, s32
+    G, N, K = 16, 8192, 5120
+    w = synth.randn_bf16((G, N, K), 1.0, seed=7, device=dev)
+    ce = lambda r, c: ((r + 127) // 128) * 128 * ((c + 127) // 128) * 4
+    q, s3 = torch.empty((G, N, K), dtype=torch.uint8, device=dev), torch.empty((G, ce(N, K)), dtype=torch.uint8, device=dev)
+    qT, sT = torch.empty((G, K, N), dtype=torch.uint8, device=dev), torch.empty((G, ce(K, N)), dtype=torch.uint8, device=dev)
+    E = G * N * K
+    for label, dirs, out in (("3d plain", 1, (q, s3, None, None)), ("3d transposed", 2, (None, None, qT, sT)),
+                             ("3d both", 3, (q, s3, qT, sT))):
+        nb = E * (2 + 2 + 2 / 32) if dirs == 3 else E * (2 + 1 + 1 / 32)
+        time_call(L.mxfp8_quantize_3d_experts, (sp(w), G, N, K, dirs, 1, *[sp(t) for t in out], None), nb, label,
+                  [G, N, K])
+    best = max(r["frac_hbm"] for r in rows)
+    return {"metric": "MXFP8 quantize GB/s (sweep)", "unit": "GB/s", "hbm_peak_gbs": pk["hbm"],
+            "peak_note": f"{pk['src']} copy bandwidth", "data": "synthetic",
+            "config": {"workload": "quantization sweep: [M,K] M in 8192..131072, K in {5120, 8192}; "
+                                   "3D [16,8192,5120]; N(0,1)*10^U(-4,4) per row"},
+            "best_frac_hbm": best, "sweep": rows}
 
 
 def run_reference(args, rank, world):
