@@ -407,38 +407,62 @@ def run_native(args, rank, world, local):
         base = {"kernel": "cuBLAS bf16 per-group torch.mm loop, forward", "ms": round(bms, 4),
                 "tflops": round(step.gemm_flops["fwd"] / bms / 1e9, 1)}
 
-    # end to end: host (pinned) inputs copied in and results copied out inside every step
+    # end to end: host (pinned) inputs copied in and results copied out inside every step, as a
+    # 3-stream pipeline over two device buffer sets: the copy-in of step i+1 and the copy-out of
+    # step i-1 overlap the kernels of step i (events order each buffer set's reuse)
     e2e = None
     if not args.no_e2e and single:
+        sets = [step, Step(w, dev)]
         hA, hW, hD = (t.cpu().pin_memory() for t in (step.A, step.W, step.D))
         hoffs = step.offs.cpu().pin_memory()
-        ho, hdA, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (step.out, step.dA, step.dW))
-        n_e2e = max(3, min(20, args.steps // 10))
+        hout = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (st.out, st.dA, st.dW))
+                for st in sets]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        n_e2e = max(4, min(20, args.steps // 10))
+        mk = lambda: torch.cuda.Event(enable_timing=False)
+        h2d_done = [mk() for _ in range(n_e2e)]
+        comp_done = [mk() for _ in range(n_e2e)]
+        d2h_done = [mk() for _ in range(n_e2e)]
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        x0.record(stream)
-        for _ in range(n_e2e):
-            step.A.copy_(hA, non_blocking=True)
-            step.W.copy_(hW, non_blocking=True)
-            step.D.copy_(hD, non_blocking=True)
-            step.offs.copy_(hoffs, non_blocking=True)
-            step.run(stream)
-            ho.copy_(step.out, non_blocking=True)
-            hdA.copy_(step.dA, non_blocking=True)
-            hdW.copy_(step.dW, non_blocking=True)
-        x1.record(stream)
+        x0.record(s_in)
+        for i in range(n_e2e):
+            st = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[i - 2])       # inputs of set i%2 no longer read
+                st.A.copy_(hA, non_blocking=True)
+                st.W.copy_(hW, non_blocking=True)
+                st.D.copy_(hD, non_blocking=True)
+                st.offs.copy_(hoffs, non_blocking=True)
+                h2d_done[i].record(s_in)
+            stream.wait_event(h2d_done[i])
+            if i >= 2:
+                stream.wait_event(d2h_done[i - 2])           # outputs of set i%2 already copied out
+            st.run(stream)
+            comp_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                for h, d in zip(hout[i % 2], (st.out, st.dA, st.dW)):
+                    h.copy_(d, non_blocking=True)
+                d2h_done[i].record(s_out)
+        s_out.wait_event(d2h_done[n_e2e - 1])
+        x1.record(s_out)
         torch.cuda.synchronize()
+        for st in sets:
+            st.check_status()
         xms = x0.elapsed_time(x1) / n_e2e
         if world > 1:
             t = torch.tensor([xms], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             xms = float(t.item())
         bi = sum(t.numel() * t.element_size() for t in (hA, hW, hD, hoffs))
-        bo = sum(t.numel() * t.element_size() for t in (ho, hdA, hdW))
+        bo = sum(t.numel() * t.element_size() for t in hout[0])
         e2e = {"value": round(world * step.flops / xms / 1e9, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_e2e}
+               "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_e2e,
+               "pipeline": "copy-in, kernels and copy-out on 3 streams over 2 device buffer sets"}
 
     if rank != 0:
         return None

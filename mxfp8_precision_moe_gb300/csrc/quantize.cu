@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
     const int64_t Cb = C / kBlk;
     const int64_t ct_row = (C + 127) / 128;                                  // row-scale column tiles
     const int64_t ct_col = grouped ? (int64_t)ptotal_s / 128 : (R + 127) / 128;  // col-scale column tiles
-    const int64_t per_b = p.tiles_r * p.tiles_c;
+    // tile indices fit in 32 bits (checked on the host): 32-bit divisions, not 64-bit ones, per tile
+    const uint32_t per_b = (uint32_t)(p.tiles_r * p.tiles_c), tiles_c = (uint32_t)p.tiles_c;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == 8) {
@@ -196,8 +197,8 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
                         }
                     break;
                 }
-                const int64_t b = t / per_b, rem = t - b * per_b;
-                const int64_t tr = rem / p.tiles_c, tc = rem - tr * p.tiles_c;
+                const uint32_t tt = (uint32_t)t, b = tt / per_b, rem = tt - b * per_b;
+                const uint32_t tr = rem / tiles_c, tc = rem - tr * tiles_c;
                 mbar_arrive_expect_tx(&full[stage], kQTileBytes);
                 tma_load_3d(tiles + stage * kQTileBytes, &xmap, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
                             &full[stage]);
@@ -209,16 +210,70 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
         return;
     }
 
+    // ---- zero padding of the blocked layouts (bytes no tile writes).  Done before the tile loop, so it
+    // overlaps the producer filling the ring, in small units spread over all CTAs:
+    //   row layout:    (batch, group, 32-row chunk) of the group's padding rows, every column tile;
+    //   column layout: (batch, group, 128-row slice) of the group's padding block-columns, and
+    //                  (batch) the padding rows C .. ceil(C/128)*128, every column tile.
+    if (p.blocked && !kB32) {
+        const int G_eff = grouped ? p.G : 1;
+        const int64_t rslices = (C + 127) / 128;
+        const int64_t units_row = kRow ? (int64_t)p.batch * G_eff * 4 : 0;
+        const int64_t units_colg = kCol ? (int64_t)p.batch * G_eff * rslices : 0;
+        const int64_t units_colr = kCol ? (int64_t)p.batch : 0;
+        const int tid = threadIdx.x;  // 256 consumer threads
+        for (int64_t u = blockIdx.x; u < units_row + units_colg + units_colr; u += gridDim.x) {
+            if (u < units_row) {
+                const int64_t bb = u / (G_eff * 4);
+                const int g = (int)((u / 4) % G_eff), chunk = (int)(u % 4);
+                const int64_t start = grouped ? (g ? ends_s[g - 1] : 0) : 0;
+                const int64_t size = grouped ? ends_s[g] - start : R;
+                const int64_t P = grouped ? pstart_s[g] : 0;
+                const int64_t r0 = size + chunk * 32, r1 = min64(r0 + 32, ((size + 127) / 128) * 128);
+                uint8_t* sb = p.s_row + bb * p.s_row_bstride;
+                for (int64_t i = tid; i < (r1 - r0) * ct_row; i += 256) {
+                    const int64_t pr = P + r0 + i / ct_row, t = i % ct_row;
+                    *reinterpret_cast<uint32_t*>(sb + ((pr >> 7) * ct_row + t) * 512 + (pr & 31) * 16 +
+                                                 ((pr >> 5) & 3) * 4) = 0u;
+                }
+            } else if (u < units_row + units_colg) {
+                const int64_t u2 = u - units_row;
+                const int64_t bb = u2 / (G_eff * rslices);
+                const int g = (int)((u2 / rslices) % G_eff);
+                const int64_t rs = u2 % rslices;
+                const int64_t start = grouped ? (g ? ends_s[g - 1] : 0) : 0;
+                const int64_t size = grouped ? ends_s[g] - start : R;
+                const int64_t Q = grouped ? pstart_s[g] / kBlk : 0;
+                const int64_t c0 = Q + size / kBlk, c1 = Q + ((size + 127) / 128) * 4;
+                const int64_t rlo = rs * 128, rn = min64(128, C - rlo);
+                uint8_t* sb = p.s_col + bb * p.s_col_bstride;
+                for (int64_t i = tid; i < rn * (c1 - c0); i += 256) {
+                    const int64_t r = rlo + i / (c1 - c0), c = c0 + i % (c1 - c0);
+                    sb[blocked_off(r, c, ct_col)] = 0;
+                }
+            } else {
+                const int64_t bb = u - units_row - units_colg;
+                const int64_t rows_p = ((C + 127) / 128) * 128;
+                uint8_t* sb = p.s_col + bb * p.s_col_bstride;
+                for (int64_t i = tid; i < (rows_p - C) * ct_col; i += 256) {
+                    const int64_t r = C + i / ct_col, t = i % ct_col;
+                    *reinterpret_cast<uint32_t*>(sb + ((r >> 7) * ct_col + t) * 512 + (r & 31) * 16 +
+                                                 ((r >> 5) & 3) * 4) = 0u;
+                }
+            }
+        }
+    }
+
     const int wi = warp >> 1, wj = warp & 1;
     const int li = lane >> 3, lj = lane & 7;
     int stage = 0;
     uint32_t phase = 0;
 
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const int64_t b = t / per_b;
-        const int64_t rem = t - b * per_b;
-        const int64_t tr = rem / p.tiles_c, tc = rem - tr * p.tiles_c;
-        const int64_t row0 = tr * 128 + wi * 32, col0 = tc * 128 + wj * 64;
+        const uint32_t tt = (uint32_t)t, b32 = tt / per_b, rem = tt - b32 * per_b;
+        const uint32_t tr = rem / tiles_c, tc = rem - tr * tiles_c;
+        const int64_t b = b32;
+        const int64_t row0 = (int64_t)tr * 128 + wi * 32, col0 = (int64_t)tc * 128 + wj * 64;
         if (!mbar_wait_bounded(&full[stage], phase, kQTimeoutNs, abort_flag, p.dev_status)) break;
         // this warp's 32 x 64 sub-tile: lane rows 8li..8li+7, columns 8lj..8lj+7 (16 bytes each)
         const uint8_t* src = tiles + stage * kQTileBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
@@ -403,54 +458,6 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
         }
     }
 
-    // ---- zero padding of the blocked layouts (bytes no tile writes), spread over the CTAs
-    if (p.blocked && !kB32) {
-        const int G_eff = grouped ? p.G : 1;
-        const int64_t units_row = kRow ? (int64_t)p.batch * G_eff : 0;
-        const int64_t units_col = kCol ? (int64_t)p.batch * (G_eff + 1) : 0;
-        const int tid = threadIdx.x;  // 256 consumer threads
-        for (int64_t u = blockIdx.x; u < units_row + units_col; u += gridDim.x) {
-            if (u < units_row) {
-                // padding rows of group g: [P_g + size_g, P_g + ceil(size_g/128)*128), every column tile
-                const int64_t bb = u / G_eff;
-                const int g = (int)(u - bb * G_eff);
-                const int64_t start = grouped ? (g ? ends_s[g - 1] : 0) : 0;
-                const int64_t size = grouped ? ends_s[g] - start : R;
-                const int64_t P = grouped ? pstart_s[g] : 0;
-                const int64_t npad = ((size + 127) / 128) * 128 - size;
-                uint8_t* sb = p.s_row + bb * p.s_row_bstride;
-                for (int64_t i = tid; i < npad * ct_row; i += 256) {
-                    const int64_t pr = P + size + i / ct_row, t = i % ct_row;
-                    *reinterpret_cast<uint32_t*>(sb + ((pr >> 7) * ct_row + t) * 512 + (pr & 31) * 16 +
-                                                 ((pr >> 5) & 3) * 4) = 0u;
-                }
-            } else {
-                const int64_t u2 = u - units_row;
-                const int64_t bb = u2 / (G_eff + 1);
-                const int g = (int)(u2 - bb * (G_eff + 1));
-                uint8_t* sb = p.s_col + bb * p.s_col_bstride;
-                const int64_t rows_p = ((C + 127) / 128) * 128;
-                if (g < G_eff) {
-                    // padding block-columns of group g, every (real) scale row
-                    const int64_t start = grouped ? (g ? ends_s[g - 1] : 0) : 0;
-                    const int64_t size = grouped ? ends_s[g] - start : R;
-                    const int64_t Q = grouped ? pstart_s[g] / kBlk : 0;
-                    const int64_t c0 = Q + size / kBlk, c1 = Q + ((size + 127) / 128) * 4;
-                    for (int64_t i = tid; i < C * (c1 - c0); i += 256) {
-                        const int64_t r = i / (c1 - c0), c = c0 + i % (c1 - c0);
-                        sb[blocked_off(r, c, ct_col)] = 0;
-                    }
-                } else {
-                    // padding rows C .. ceil(C/128)*128 of the scale matrix, every column tile
-                    for (int64_t i = tid; i < (rows_p - C) * ct_col; i += 256) {
-                        const int64_t r = C + i / ct_col, t = i % ct_col;
-                        *reinterpret_cast<uint32_t*>(sb + ((r >> 7) * ct_col + t) * 512 + (r & 31) * 16 +
-                                                     ((r >> 5) & 3) * 4) = 0u;
-                    }
-                }
-            }
-        }
-    }
 }
 
 __global__ void check_offsets_kernel(const int32_t* offs, int32_t G, int64_t M, int32_t align, int32_t* dev_status) {
@@ -536,6 +543,7 @@ extern "C" mxfp8_status_t mxfp8_quantize_2d(const void* x_bf16, int64_t M, int64
     p.offs = offs; p.G = offs ? G : 0;
     p.dev_status = dev_status;
     p.tiles_r = (M + 127) / 128; p.tiles_c = (K + 127) / 128; p.ntiles = p.tiles_r * p.tiles_c;
+    if (p.ntiles >= INT32_MAX) return MXFP8_ERR_SHAPE;
     if (mxfp8_status_t s = launch_tiles(dirs, p, st); s != MXFP8_OK) return s;
     return MXFP8_OK;
 }
@@ -568,6 +576,7 @@ extern "C" mxfp8_status_t mxfp8_quantize_3d_experts(const void* w_bf16, int32_t 
     p.offs = nullptr; p.G = 0;
     p.dev_status = dev_status;
     p.tiles_r = (N + 127) / 128; p.tiles_c = (K + 127) / 128; p.ntiles = p.tiles_r * p.tiles_c * G;
+    if (p.ntiles >= INT32_MAX) return MXFP8_ERR_SHAPE;
     if (mxfp8_status_t r = launch_tiles(dirs, p, st); r != MXFP8_OK) return r;
     return MXFP8_OK;
 }
