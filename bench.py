@@ -123,6 +123,15 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest value over all ranks (the slowest rank's time sets the job's throughput)."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- clocks during the timed region
 class ClockSampler:
     FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
@@ -374,11 +383,7 @@ def run_native(args, rank, world, local):
     wall1 = time.time()
     sampler.stop()
     step.check_status()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     per = {n: float(np.mean([e[n][0].elapsed_time(e[n][1]) for e in ev])) for n in names}
     clocks = sampler.summary(wall0, wall1)
 
@@ -453,11 +458,7 @@ def run_native(args, rank, world, local):
         torch.cuda.synchronize()
         for st in sets:
             st.check_status()
-        xms = x0.elapsed_time(x1) / n_e2e
-        if world > 1:
-            t = torch.tensor([xms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            xms = float(t.item())
+        xms = max_over_ranks(x0.elapsed_time(x1) / n_e2e, world, dev)
         bi = sum(t.numel() * t.element_size() for t in (hA, hW, hD, hoffs))
         bo = sum(t.numel() * t.element_size() for t in hout[0])
         e2e = {"value": round(world * step.flops / xms / 1e9, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,

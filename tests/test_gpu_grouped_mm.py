@@ -284,6 +284,66 @@ def test_full_size_swiglu_gemm_shapes_sampled(mx):
         del A, W, aq, as_, wq, ws, out
 
 
+def test_wgrad_rejects_misaligned_group_offsets(mx):
+    """Token groups that are not multiples of 32 would put a TMA coordinate off its 16-byte
+    alignment in the wgrad; the kernel checks the offsets before any copy, reports
+    MXFP8_ERR_OFFSETS and issues nothing (host-side fault injection: the offsets are bad, no
+    device fault is provoked)."""
+    M, N, K = 256, 256, 256
+    dTq = torch.zeros((N, M), dtype=torch.uint8, device="cuda")
+    aTq = torch.zeros((K, M), dtype=torch.uint8, device="cuda")
+    s1 = torch.zeros(mx.mxfp8_scale_bytes_colgroups(N, M, 2), dtype=torch.uint8, device="cuda")
+    s2 = torch.zeros(mx.mxfp8_scale_bytes_colgroups(K, M, 2), dtype=torch.uint8, device="cuda")
+    bad = torch.tensor([100, 256], dtype=torch.int32, device="cuda")
+    st = mx.new_status()
+    mx.mxfp8_grouped_mm_wgrad(dTq, s1, aTq, s2, bad, dev_status=st)
+    assert int(st.item()) == 7
+    # the context stays usable
+    x = torch.ones((32, 32), dtype=torch.bfloat16, device="cuda")
+    q, s, _, _ = mx.mxfp8_quantize_2d(x, mx.ROW, mx.SCALES_COMPACT)
+    assert int(q[0, 0].item()) == 0x78
+
+
+def test_full_size_swiglu_dgrad_wgrad_sampled(mx):
+    """The SwiGLU gate shapes (N=8192, K=5120, M=65600 in two groups), dgrad and wgrad, sampled."""
+    sizes = synth.swiglu_group_sizes()
+    M, N, K = sum(sizes), 8192, 5120
+    offs = offs_dev(sizes)
+    ends = sizes_to_ends(sizes)
+    starts = ends - np.asarray(sizes)
+    A = synth.randn_bf16((M, K), 1.0, 5, device="cuda")
+    W = synth.randn_bf16((2, N, K), 0.02, 6, device="cuda")
+    D = synth.randn_bf16((M, N), 1e-3, 7, device="cuda")
+    st = mx.new_status()
+    _, _, aTq, aTs = mx.mxfp8_quantize_2d(A, mx.COL, mx.SCALES_BLOCKED, offs, st)
+    _, _, wTq, wTs = mx.mxfp8_quantize_3d_experts(W, mx.COL, mx.SCALES_BLOCKED, st)
+    dq, ds, dTq, dTs = mx.mxfp8_quantize_2d(D, mx.ROW | mx.COL, mx.SCALES_BLOCKED, offs, st)
+    dA = mx.mxfp8_grouped_mm_dgrad(dq, ds, wTq, wTs, offs, dev_status=st)
+    dW = mx.mxfp8_grouped_mm_wgrad(dTq, dTs, aTq, aTs, offs, dev_status=st)
+    mx.read_status(st)
+    rng = np.random.default_rng(3)
+    ref, got = [], []
+    for r in np.unique(np.concatenate([rng.integers(0, M, 10), [0, ends[0] - 1, ends[0], M - 1]])):
+        g = int(np.searchsorted(ends, r, side="right"))
+        qd, sd = oracle.quantize_rows(u16(D[r:r + 1]))
+        for k in rng.integers(0, K, 4):
+            qw, sw = oracle.quantize_vec(u16(W[g, :, k]))
+            ref.append(oracle.dot(qd[0], sd[0], qw, sw))
+            got.append(float(dA[r, k].item()))
+    assert_gemm_close(np.array(got), np.array(ref), what="swiglu dgrad sampled")
+    for g in range(2):
+        lo, hi = int(starts[g]), int(ends[g])
+        ref, got = [], []
+        for n in rng.integers(0, N, 3):
+            q1, s1 = oracle.quantize_vec(u16(D[lo:hi, n]))
+            for k in rng.integers(0, K, 3):
+                q2, s2 = oracle.quantize_vec(u16(A[lo:hi, k]))
+                ref.append(oracle.dot(q1, s1, q2, s2))
+                got.append(float(dW[g, n, k].item()))
+        assert_gemm_close(np.array(got), np.array(ref), rms=float(np.sqrt(np.mean(np.square(ref)))),
+                          what=f"swiglu wgrad group {g}")
+
+
 def test_bounded_wait_times_out_cleanly(mx):
     """A wait on a barrier nothing arrives on returns MXFP8_ERR_TIMEOUT after its
     limit instead of hanging, and the context stays usable afterwards."""
