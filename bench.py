@@ -55,6 +55,9 @@ WORKLOAD_TEXT = {
     "swiglu": "SwiGLU routed expert fwd+bwd GEMMs: G=2, M=65600 (39360/26240), gate/up W[2,8192,5120], "
               "down W[2,5120,8192]; 9 grouped GEMMs, synthetic stand-ins for the SwiGLU intermediates",
     "tiny": "Tiny: G=2, A[256,256], offs [128,256], W[2,128,256] (latency-bound; parity case)",
+    "scout_mb4": "Llama4-Scout-like routed experts, one optimizer step of 4 microbatches (G=8, K=5120, N=8192, "
+                 "M=16384 tokens each, Zipf(1.1) group sizes in 32-token chunks, seeds 0-3): W quantized once "
+                 "(prequantized-weight cache), then fwd+bwd per microbatch",
 }
 
 
@@ -64,6 +67,11 @@ def workload_parts(name: str, dev) -> list:
 
     if name in ("scout", "imbalanced", "tiny"):
         return [synth.workload(name, seed=0, device=dev)]
+    if name == "scout_mb4":
+        mbs = [synth.workload("scout", seed=i, device=dev) for i in range(4)]
+        for w in mbs[1:]:
+            w["W"] = mbs[0]["W"]  # one weight tensor for the whole optimizer step
+        return mbs
     s = synth.workload("swiglu", seed=0, device=dev)
     G, M, D, H = s["G"], s["M"], s["D"], s["H"]
     h = synth.randn_bf16((M, H), 1.0, seed=50, device=dev)      # stands in for silu(x Wg^T) * (x Wu^T)
@@ -92,7 +100,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--no-baseline", action="store_true", help="skip the cuBLAS bf16 comparison leg")
-    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "tiny", "sweep"],
+    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "tiny", "scout_mb4", "sweep"],
                     help="scout (default, the reported line); the others are extra measurements")
     return ap.parse_args()
 
@@ -195,7 +203,7 @@ class ClockSampler:
 class Step:
     """Device buffers of one replica and the C-ABI calls of one pass of the path."""
 
-    def __init__(self, w: dict, device):
+    def __init__(self, w: dict, device, shared_w: "Step | None" = None):
         import mxfp8_precision_moe_gb300 as mx
 
         L = mx.load()
@@ -212,8 +220,12 @@ class Step:
         self.aq, self.as_ = u8(M, K), u8(sb(M, K, G, 1))
         self.aTq, self.aTs = u8(K, M), u8(sc(K, M, G))
         ce = lambda r, c: ((r + 127) // 128) * 128 * ((c + 127) // 128) * 4
-        self.wq, self.ws = u8(G, N, K), u8(G, ce(N, K))
-        self.wTq, self.wTs = u8(G, K, N), u8(G, ce(K, N))
+        if shared_w is None:
+            self.wq, self.ws = u8(G, N, K), u8(G, ce(N, K))
+            self.wTq, self.wTs = u8(G, K, N), u8(G, ce(K, N))
+        else:  # prequantized weights of another microbatch of the same optimizer step
+            self.W = shared_w.W
+            self.wq, self.ws, self.wTq, self.wTs = shared_w.wq, shared_w.ws, shared_w.wTq, shared_w.wTs
         self.dq, self.ds = u8(M, N), u8(sb(M, N, G, 1))
         self.dTq, self.dTs = u8(N, M), u8(sc(N, M, G))
         self.out, self.dA, self.dW = bf(M, N), bf(M, K), bf(G, N, K)
@@ -239,6 +251,9 @@ class Step:
         self.flops = 3 * 2.0 * M * N * K
         self.bytes = {"quant_A": M * K * (2 + 1 + 1 + 2 / 32), "quant_W": G * N * K * (2 + 1 + 1 + 2 / 32),
                       "quant_dOut": M * N * (2 + 1 + 1 + 2 / 32)}
+        if shared_w is not None:
+            self.calls = [c for c in self.calls if c[0] != "quant_W"]
+            del self.launches["quant_W"], self.bytes["quant_W"]
         self.gemm_flops = {"fwd": 2.0 * M * N * K, "dgrad": 2.0 * M * N * K, "wgrad": 2.0 * M * N * K}
 
     def run(self, stream, events=None):
@@ -258,8 +273,10 @@ class Step:
 class StepGroup:
     """Several grouped-GEMM problems run back to back as one step (the SwiGLU expert's three)."""
 
-    def __init__(self, parts: list, device):
-        self.parts = [Step(w, device) for w in parts]
+    def __init__(self, parts: list, device, share_w: bool = False):
+        self.parts = []
+        for w in parts:
+            self.parts.append(Step(w, device, self.parts[0] if (share_w and self.parts) else None))
         self.calls, self.gemm_flops, self.bytes, self.launches = [], {}, {}, {}
         for i, st in enumerate(self.parts):
             for name, fn, argv in st.calls:
@@ -354,7 +371,7 @@ def run_native(args, rank, world, local):
     pk = peaks()
     parts = workload_parts(args.workload, dev)
     w = parts[0]
-    step = Step(w, dev) if len(parts) == 1 else StepGroup(parts, dev)
+    step = Step(w, dev) if len(parts) == 1 else StepGroup(parts, dev, share_w=args.workload == "scout_mb4")
     single = isinstance(step, Step)
     stream = torch.cuda.current_stream(dev)
 
@@ -499,7 +516,7 @@ def run_native(args, rank, world, local):
         "config": {"workload": WORKLOAD_TEXT[args.workload], "G": step.G, "M": step.M, "N": step.N, "K": step.K,
                    "group_sizes": list(map(int, w["sizes"])), "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({L2_BYTES // 2**20} MiB): A, W, dOut = "
-                         f"{sum((p['A'].numel() + p['W'].numel() + p['dOut'].numel()) * 2 for p in parts) // 2**20} "
+                         f"{sum(t.numel() * 2 for t in {id(t): t for p in parts for t in (p['A'], p['W'], p['dOut'])}.values()) // 2**20} "
                          "MiB bf16 per step" if args.workload != "tiny" else "tiny: L2-resident (latency-bound case)",
                    "frac_fp8_peak_step": round(step.flops / ms_step / 1e9 / fp8_peak, 3)},
         "roofline": {"bound": "tensor", "kernel": "grouped_mm_fwd" + ("" if single else " (gate)"), "achieved": round(achieved, 1),

@@ -27,6 +27,7 @@ __all__ = [
     "mxfp8_quantize_2d", "mxfp8_quantize_3d_experts", "mxfp8_grouped_mm_fwd", "mxfp8_grouped_mm_dgrad",
     "mxfp8_grouped_mm_wgrad", "mxfp8_scale_bytes", "mxfp8_scale_bytes_colgroups", "mxfp8_check_offsets",
     "mxfp8_debug_wait_timeout", "new_status", "read_status", "to_mxfp8_then_scaled_grouped_mm", "load",
+    "quantize_expert_weights", "Mxfp8WeightCache",
 ]
 
 
@@ -192,13 +193,16 @@ class _ToMxfp8ThenScaledGroupedMM(torch.autograd.Function):
     GEMMs.  Quantization is treated as the identity for gradients."""
 
     @staticmethod
-    def forward(ctx, A, W, offs):
+    def forward(ctx, A, W, offs, w_mxfp8):
         need_dA = ctx.needs_input_grad[0]
         need_dW = ctx.needs_input_grad[1]
         a_dirs = ROW | (COL if need_dW else 0)
         aq, as_, aTq, aTs = mxfp8_quantize_2d(A.contiguous(), a_dirs, SCALES_BLOCKED, offs)
-        w_dirs = ROW | (COL if need_dA else 0)
-        wq, ws, wTq, wTs = mxfp8_quantize_3d_experts(W.contiguous(), w_dirs, SCALES_BLOCKED)
+        if w_mxfp8 is None:
+            w_dirs = ROW | (COL if need_dA else 0)
+            wq, ws, wTq, wTs = mxfp8_quantize_3d_experts(W.contiguous(), w_dirs, SCALES_BLOCKED)
+        else:
+            wq, ws, wTq, wTs = _check_quad(w_mxfp8, W, need_dA)
         out = mxfp8_grouped_mm_fwd(aq, as_, wq, ws, offs)
         ctx.save_for_backward(aTq, aTs, wTq, wTs, offs)
         ctx.shape = (A.shape[0], W.shape[0], W.shape[1], W.shape[2])
@@ -210,20 +214,61 @@ class _ToMxfp8ThenScaledGroupedMM(torch.autograd.Function):
         need_dA, need_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
         dirs = (ROW if need_dA else 0) | (COL if need_dW else 0)
         if dirs == 0:
-            return None, None, None
+            return None, None, None, None
         dq, ds, dTq, dTs = mxfp8_quantize_2d(dOut.contiguous().to(torch.bfloat16), dirs, SCALES_BLOCKED, offs)
         dA = mxfp8_grouped_mm_dgrad(dq, ds, wTq, wTs, offs) if need_dA else None
         dW = mxfp8_grouped_mm_wgrad(dTq, dTs, aTq, aTs, offs) if need_dW else None
-        return dA, dW, None
+        return dA, dW, None, None
 
 
-def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torch.Tensor) -> torch.Tensor:
+def _blocked_bytes(rows: int, cols: int) -> int:
+    return ((rows + 127) // 128) * 128 * ((cols // 32 + 3) // 4) * 4
+
+
+def _check_quad(quad, W: torch.Tensor, need_t: bool):
+    """Validate a prequantized (weight_fp8, weight_scale, weight_t_fp8, weight_t_scale)
+    quadruple against W[G, N, K]; the transposed pair may be None when no dgrad is needed."""
+    if len(quad) != 4:
+        raise ValueError("w_mxfp8 must be (weight_fp8, weight_scale, weight_t_fp8, weight_t_scale)")
+    wq, ws, wTq, wTs = quad
+    G, N, K = W.shape
+    want = [(wq, (G, N, K)), (ws, (G, _blocked_bytes(N, K)))]
+    if need_t or wTq is not None:
+        want += [(wTq, (G, K, N)), (wTs, (G, _blocked_bytes(K, N)))]
+    for t, shape in want:
+        if t is None or t.dtype != torch.uint8 or tuple(t.shape) != shape or t.device != W.device \
+                or not t.is_contiguous():
+            raise ValueError(f"w_mxfp8: expected a contiguous uint8 tensor of shape {shape} on {W.device}")
+    return wq, ws, wTq, wTs
+
+
+def quantize_expert_weights(W: torch.Tensor):
+    """One fused launch: W[G, N, K] -> (weight_fp8 [G, N, K], weight_scale, weight_t_fp8 [G, K, N],
+    weight_t_scale), scales in the blocked layout, one flat buffer per expert."""
+    return mxfp8_quantize_3d_experts(W.detach().contiguous(), ROW | COL, SCALES_BLOCKED)
+
+
+def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, *, w_mxfp8=None,
+                                    weight_cache=None) -> torch.Tensor:
     """Differentiable MXFP8 grouped GEMM: out[m] = A[m] @ W[g]^T for rows m of
     group g (offs = int32 cumulative end rows).  A [M, K] bf16, W [G, N, K] bf16,
     out [M, N] bf16.  Group sizes must be multiples of 32 when gradients of W
-    are needed (token-wise quantization for the wgrad)."""
+    are needed (token-wise quantization for the wgrad).
+
+    The expert weights are quantized on the fly unless they come prequantized:
+    ``w_mxfp8`` = (weight_fp8, weight_scale, weight_t_fp8, weight_t_scale) as
+    returned by ``quantize_expert_weights(W)``, or ``weight_cache`` = an
+    ``Mxfp8WeightCache`` that keeps that quadruple across microbatches until W
+    changes or the optimizer steps.  Gradients still flow to W."""
     if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise ValueError("to_mxfp8_then_scaled_grouped_mm expects bf16 A and W")
     if offs.dtype != torch.int32:
         raise ValueError("offs must be int32")
-    return _ToMxfp8ThenScaledGroupedMM.apply(A, W, offs)
+    if w_mxfp8 is not None and weight_cache is not None:
+        raise ValueError("pass w_mxfp8 or weight_cache, not both")
+    if weight_cache is not None:
+        w_mxfp8 = weight_cache.get(W)
+    return _ToMxfp8ThenScaledGroupedMM.apply(A, W, offs, w_mxfp8)
+
+
+from .weight_cache import Mxfp8WeightCache  # noqa: E402  (uses quantize_expert_weights above)
