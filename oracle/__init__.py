@@ -68,6 +68,10 @@ def lib():
         L.oracle_grouped_mm_rows.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P]
         L.oracle_grouped_mm_wgrad.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P]
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_bf16_from_f64.argtypes = [ctypes.c_double]
+        L.oracle_bf16_from_f64.restype = ctypes.c_uint16
+        L.oracle_bf16_from_f64_array.argtypes = [P, I64, P]
+        L.oracle_swiglu_bf16.argtypes = [P, P, I64, P]
         _lib = L
     return _lib
 
@@ -243,4 +247,44 @@ def grouped_mm_wgrad(dq, ds, aq, as_, ends) -> np.ndarray:
     G = e.size
     out = np.zeros((G, N, K), np.float64)
     lib().oracle_grouped_mm_wgrad(_p(dq), _p(ds), _p(aq), _p(as_), _p(e), G, M, N, K, _p(out))
+    return out
+
+
+# ---------------------------------------------------------------- SwiGLU stage of a routed expert
+def bf16_from_f64(x) -> np.ndarray:
+    """fp64 values -> bf16 bit patterns (uint16), round to nearest even, one rounding."""
+    x = np.ascontiguousarray(x, np.float64)
+    out = np.empty(x.shape, np.uint16)
+    lib().oracle_bf16_from_f64_array(_p(x), x.size, _p(out))
+    return out
+
+
+def swiglu_bf16(h1, h3) -> np.ndarray:
+    """h = bf16(bf16(silu(h1)) * h3) over bf16 bit patterns (uint16 in, uint16 out)."""
+    h1 = _u16(h1)
+    h3 = _u16(h3)
+    assert h1.shape == h3.shape
+    out = np.empty(h1.shape, np.uint16)
+    lib().oracle_swiglu_bf16(_p(h1), _p(h3), h1.size, _p(out))
+    return out
+
+
+def swiglu_gate_up(x_u16, wg_u16, wu_u16, ends) -> dict:
+    """The gate/up half of a SwiGLU routed expert, from bf16 inputs: x [M, D], Wg and Wu
+    [G, H, D].  x and the weights are quantized along D, both GEMMs run in fp64, and
+    h1, h3, h follow the bf16 rounding points of oracle_swiglu_bf16.  Returns the fp64
+    GEMM results (h1_f64, h3_f64), the bf16 patterns (h1, h3, h), and h quantized along
+    H (h_q, h_s compact [M, H/32]) and along the tokens (hT_q [H, M], hT_s compact)."""
+    xq, xs = quantize_rows(x_u16)
+    G = wg_u16.shape[0]
+    wg = [quantize_rows(wg_u16[g]) for g in range(G)]
+    wu = [quantize_rows(wu_u16[g]) for g in range(G)]
+    h1f = grouped_mm_rows(xq, xs, np.stack([q for q, _ in wg]), np.stack([s_ for _, s_ in wg]), ends)
+    h3f = grouped_mm_rows(xq, xs, np.stack([q for q, _ in wu]), np.stack([s_ for _, s_ in wu]), ends)
+    h1, h3 = bf16_from_f64(h1f), bf16_from_f64(h3f)
+    h = swiglu_bf16(h1, h3)
+    out = dict(h1_f64=h1f, h3_f64=h3f, h1=h1, h3=h3, h=h)
+    out["h_q"], out["h_s"] = quantize_rows(h)
+    if h.shape[0] % 32 == 0:
+        out["hT_q"], out["hT_s"] = quantize_cols(h)
     return out

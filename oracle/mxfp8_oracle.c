@@ -36,6 +36,8 @@
  * round-trip error bounds, transpose invariance, blocked-layout bijection and
  * hand-computed positions, brute-force tiny GEMMs, the identity-weight case.
  * NaN/Inf input blocks: parity unpinned (one hand-made block only).
+ * SwiGLU stage: bf16 rounding pinned against torch's fp32->bf16 cast, hand
+ * ties and a double-rounding case; silu against torch's fp64 silu.
  */
 #include <math.h>
 #include <stdint.h>
@@ -303,6 +305,57 @@ void oracle_grouped_mm_wgrad(const uint8_t* dq, const uint8_t* ds, const uint8_t
             for (int64_t k = 0; k < K; ++k)
                 out[(g * N + n) * K + k] =
                     oracle_dot(dq + n * M + lo, ds + n * Mb + lo / BLK, aq + k * M + lo, as + k * Mb + lo / BLK, hi - lo);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* SwiGLU stage of a routed expert (bf16 rounding points)              */
+/* ------------------------------------------------------------------ */
+/* "feat(moe): add MoK MXFP8 expert support" (gate / up / down routed-expert
+ * weights) and "MXFP8 (Micro-scaling FP8)", "Neutralizing quantization
+ * overhead" (quantization fused into the kernel that produces the activation).
+ * The pages give no formula for the expert's activation; the reading is the
+ * SwiGLU of an elementwise bf16 evaluation:
+ *   h1 = bf16(x Wg^T), h3 = bf16(x Wu^T), s = bf16(silu(h1)), h = bf16(s * h3),
+ * with silu(v) = v / (1 + e^-v).  Every bf16() is round-to-nearest-even of the
+ * exact value (computed here in fp64). */
+
+/* fp64 -> bf16 bit pattern, nearest with ties to the even pattern, directly
+ * from the fp64 value (never through fp32: that would round twice).  Magnitudes
+ * at or past the midpoint between the largest finite bf16 and 2^128 give inf;
+ * NaN gives the quiet NaN 0x7FC0 with the sign. */
+uint16_t oracle_bf16_from_f64(double x) {
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (isnan(x)) return (uint16_t)(sign | 0x7FC0u);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+    int E;
+    frexp(a, &E);                       /* a = m * 2^E, m in [0.5, 1) */
+    int qexp = E - 8;                   /* 8 significant bits: quantum 2^(E-8) */
+    if (qexp < -133) qexp = -133;       /* subnormal quantum 2^-133 */
+    double n = ldexp(a, -qexp);         /* exact: power-of-two scaling */
+    double lo = floor(n), frac = n - lo;
+    double r = lo;
+    if (frac > 0.5 || (frac == 0.5 && fmod(lo, 2.0) != 0.0)) r = lo + 1.0;
+    double v = ldexp(r, qexp);
+    if (v >= 0x1p128) return (uint16_t)(sign | 0x7F80u);
+    float f = (float)v;                 /* exact: v has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFFu));
+}
+
+void oracle_bf16_from_f64_array(const double* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_from_f64(x[i]);
+}
+
+/* h = bf16( bf16(silu(h1)) * h3 ) elementwise over bf16 bit patterns. */
+void oracle_swiglu_bf16(const uint16_t* h1, const uint16_t* h3, int64_t n, uint16_t* h) {
+    for (int64_t i = 0; i < n; ++i) {
+        double a = oracle_bf16_to_f64(h1[i]);
+        double s = oracle_bf16_to_f64(oracle_bf16_from_f64(a / (1.0 + exp(-a))));
+        h[i] = oracle_bf16_from_f64(s * oracle_bf16_to_f64(h3[i]));  /* 8 x 8 significant bits: exact in fp64 */
     }
 }
 
