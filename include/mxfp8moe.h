@@ -178,6 +178,37 @@ mxfp8_status_t mxfp8_grouped_mm_wgrad(const void* doutT_q, const void* doutT_s, 
                                       int64_t K, void* dw_bf16, int32_t* dev_status, mxfp8_stream_t stream);
 
 /* ----------------------------------------------------------------------------
+ * mxfp8_grouped_mm_swiglu_fwd -- the gate and up GEMMs of a SwiGLU routed expert
+ * with the SwiGLU and its MXFP8 quantization fused into their epilogue.
+ * [P3] "Neutralizing quantization overhead" (fuse the quantization of
+ * activations into the kernel that produces them); [P4] (gate/up/down routed
+ * expert weights).  For rows m of group g:
+ *   h1[m, n] = bf16( sum_d X[m,d] Wg[g][n,d] ),  h3[m, n] = bf16( sum_d X[m,d] Wu[g][n,d] )
+ *   h[m, n]  = bf16( bf16(silu(h1[m,n])) * h3[m,n] ),  silu(x) = x / (1 + e^-x) in fp32
+ * (the rounding points of an elementwise bf16 SwiGLU), then h is quantized:
+ *   h_q [M, H] + h_s: along H (the down GEMM's contraction), blocked row groups
+ *       (sized by mxfp8_scale_bytes(M, H, G, MXFP8_SCALES_BLOCKED));
+ *   hT_q [H, M] + hT_s: along the tokens (the down GEMM's wgrad operand), blocked
+ *       column groups (sized by mxfp8_scale_bytes_colgroups(H, M, G)).  Optional:
+ *       both NULL to skip; when given, M % 32 == 0 and every group size % 32 == 0
+ *       (device-checked: MXFP8_ERR_OFFSETS, nothing written).
+ *   These are the bytes mxfp8_quantize_2d(h, MXFP8_ROW | MXFP8_COL, BLOCKED, offs)
+ *   writes for h.
+ * Inputs: x_q [M, D] + x_s (blocked row groups, as for the forward GEMM);
+ *   wg_q, wu_q [G, H, D] + wg_s, wu_s (blocked per expert, as
+ *   mxfp8_quantize_3d_experts(MXFP8_ROW) writes them).  h1, h3: [M, H] bf16
+ *   outputs (kept for the SwiGLU backward).
+ * Shapes: H % 32 == 0, D % 32 == 0, 1 <= G <= MXFP8_MAX_GROUPS; every pointer
+ * 16-byte aligned; all buffers caller-owned device memory; M may be 0.
+ * Errors: MXFP8_ERR_NULL / _SHAPE / _ALIGN / _ARCH synchronously.
+ * ------------------------------------------------------------------------- */
+mxfp8_status_t mxfp8_grouped_mm_swiglu_fwd(const void* x_q, const void* x_s, const void* wg_q, const void* wg_s,
+                                           const void* wu_q, const void* wu_s, const int32_t* offs, int32_t G,
+                                           int64_t M, int64_t H, int64_t D, void* h1_bf16, void* h3_bf16, void* h_q,
+                                           void* h_s, void* hT_q, void* hT_s, int32_t* dev_status,
+                                           mxfp8_stream_t stream);
+
+/* ----------------------------------------------------------------------------
  * Sizes and checks.
  * mxfp8_scale_bytes: bytes to allocate for the scales of an operand with `rows`
  *   rows of K elements (K % 32 == 0) quantized along K, its rows split into G

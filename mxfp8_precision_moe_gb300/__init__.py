@@ -27,7 +27,7 @@ __all__ = [
     "mxfp8_quantize_2d", "mxfp8_quantize_3d_experts", "mxfp8_grouped_mm_fwd", "mxfp8_grouped_mm_dgrad",
     "mxfp8_grouped_mm_wgrad", "mxfp8_scale_bytes", "mxfp8_scale_bytes_colgroups", "mxfp8_check_offsets",
     "mxfp8_debug_wait_timeout", "new_status", "read_status", "to_mxfp8_then_scaled_grouped_mm", "load",
-    "quantize_expert_weights", "Mxfp8WeightCache",
+    "quantize_expert_weights", "Mxfp8WeightCache", "mxfp8_grouped_mm_swiglu_fwd", "mxfp8_swiglu_expert",
 ]
 
 
@@ -173,6 +173,34 @@ def mxfp8_grouped_mm_wgrad(doutT_q, doutT_s, aT_q, aT_s, offs, out=None, dev_sta
     return out
 
 
+def mxfp8_grouped_mm_swiglu_fwd(x_q, x_s, wg_q, wg_s, wu_q, wu_s, offs, token_wise: bool = True,
+                                dev_status=None):
+    """Gate and up GEMMs with the SwiGLU and its MXFP8 quantization in the epilogue.
+
+    x_q [M, D] (+ blocked row-group scales), wg_q / wu_q [G, H, D] (+ blocked
+    per-expert scales).  Returns (h1, h3, h_q, h_s, hT_q, hT_s): h1 = x Wg^T and
+    h3 = x Wu^T in bf16 [M, H]; h = bf16(bf16(silu(h1)) * h3) quantized along H
+    (h_q [M, H], blocked row groups) and, if token_wise, along the tokens
+    (hT_q [H, M], blocked token groups; group sizes must be multiples of 32)."""
+    _cuda(x_q, x_s, wg_q, wg_s, wu_q, wu_s, offs, dev_status)
+    M, D = x_q.shape
+    G, H, _ = wg_q.shape
+    if tuple(wu_q.shape) != (G, H, D):
+        raise ValueError("gate and up weights must have the same shape")
+    dev = x_q.device
+    h1 = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    h3 = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    h_q = _u8((M, H), dev)
+    h_s = _u8((mxfp8_scale_bytes(M, H, G, SCALES_BLOCKED),), dev)
+    hT_q = _u8((H, M), dev) if token_wise else None
+    hT_s = _u8((mxfp8_scale_bytes_colgroups(H, M, G),), dev) if token_wise else None
+    st = load().mxfp8_grouped_mm_swiglu_fwd(_p(x_q), _p(x_s), _p(wg_q), _p(wg_s), _p(wu_q), _p(wu_s), _p(offs), G, M,
+                                            H, D, _p(h1), _p(h3), _p(h_q), _p(h_s), _p(hT_q), _p(hT_s),
+                                            _p(dev_status), _stream(dev))
+    check(st, "mxfp8_grouped_mm_swiglu_fwd")
+    return h1, h3, h_q, h_s, hT_q, hT_s
+
+
 def mxfp8_check_offsets(offs: torch.Tensor, M: int, align: int, dev_status: torch.Tensor) -> None:
     _cuda(offs, dev_status)
     st = load().mxfp8_check_offsets(_p(offs), int(offs.numel()), M, align, _p(dev_status), _stream(offs.device))
@@ -272,3 +300,4 @@ def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torc
 
 
 from .weight_cache import Mxfp8WeightCache  # noqa: E402  (uses quantize_expert_weights above)
+from .swiglu import mxfp8_swiglu_expert  # noqa: E402

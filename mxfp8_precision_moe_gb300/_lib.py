@@ -50,6 +50,8 @@ def load():
         f = getattr(L, name)
         f.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, P, P]
         f.restype = S
+    L.mxfp8_grouped_mm_swiglu_fwd.argtypes = [P, P, P, P, P, P, P, I32, I64, I64, I64, P, P, P, P, P, P, P, P]
+    L.mxfp8_grouped_mm_swiglu_fwd.restype = S
     L.mxfp8_scale_bytes.argtypes = [I64, I64, I32, INT]
     L.mxfp8_scale_bytes.restype = ctypes.c_size_t
     L.mxfp8_scale_bytes_colgroups.argtypes = [I64, I64, I32]

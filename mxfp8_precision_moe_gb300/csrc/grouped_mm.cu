@@ -79,8 +79,19 @@ struct GemmParams {
     __nv_bfloat16* out;
     int64_t ldo;              // ROWGROUPED: output row pitch (elements)
     int mode;
+    int need32;               // group sizes must be multiples of 32 (token-wise blocks or TMA coordinates)
     int32_t* dev_status;
     uint64_t timeout_ns;
+    // SwiGLU gate/up variant only: B rows 0-127 of a tile come from the gate weights (sfb), rows
+    // 128-255 from the up weights (sfb2); out = h1, out2 = h3; h = silu(h1) * h3 quantized along
+    // its row into hq/hs (blocked, row groups) and along the tokens into hTq/hTs (blocked, token groups).
+    const uint8_t* sfb2;
+    __nv_bfloat16* out2;
+    uint8_t* hq;
+    uint8_t* hs;
+    int64_t hs_ct;            // column tiles of the row-wise h scales (= ceil(H / 128))
+    uint8_t* hTq;             // nullable (with hTs): no token-wise copy
+    uint8_t* hTs;
 };
 
 struct TileInfo {
@@ -94,6 +105,8 @@ struct TileInfo {
     __nv_bfloat16* out;       // first element of the tile
     int64_t ldo;
     int valid_rows, valid_cols;
+    int64_t prow0;            // ROWGROUPED: padded (per-group 128-aligned) row of the tile's first row
+    int64_t col0;             // first output column
 };
 
 __device__ __forceinline__ int band_split(int64_t l, int64_t mt, int64_t nt, int64_t& m, int64_t& n) {
@@ -105,11 +118,14 @@ __device__ __forceinline__ int band_split(int64_t l, int64_t mt, int64_t nt, int
     return 0;
 }
 
-template <int BN>
+// kSwi: a tile is 128 output columns wide and its 256 B rows are those 128 rows of the gate
+// weights followed by the same 128 rows of the up weights.
+template <int BN, bool kSwi = false>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, const int32_t* ends_s,
                                               const int32_t* pstart_s, int64_t ptotal) {
+    constexpr int TN = kSwi ? 128 : BN;  // output columns per tile
     TileInfo ti;
-    const int64_t ntb = (p.nb + BN - 1) / BN;  // tiles along B rows
+    const int64_t ntb = (p.nb + TN - 1) / TN;  // tiles along B rows
     if (p.mode == ROWGROUPED) {
         // group of tile t: last g whose tile range starts at or before t
         int lo = 0, hi = p.G;
@@ -125,20 +141,22 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, co
         band_split(t - (int64_t)(pstart_s[g] / BM) * ntb, mt, ntb, m, n);
         ti.g = g;
         ti.a_row = start + m * BM;
-        ti.b_row = (int64_t)g * p.nb + n * BN;
+        ti.b_row = (int64_t)g * p.nb + n * TN;
         ti.a_x0 = 0;
         ti.k_tiles = (int)((p.kc + BK - 1) / BK);
         ti.sfa_base = ((int64_t)(pstart_s[g] / BM + m) * p.sfa_ct) * 512;
         const int64_t last_chunk = (p.nb + 127) / 128 - 1;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int64_t ch = min64(n * (BN / 128) + j, last_chunk);
+            const int64_t ch = kSwi ? n : min64(n * (BN / 128) + j, last_chunk);
             ti.sfb_base[j] = (int64_t)g * p.sfb_estride + ch * p.sfb_ct * 512;
         }
-        ti.out = p.out + ti.a_row * p.ldo + n * BN;
+        ti.out = p.out + ti.a_row * p.ldo + n * TN;
         ti.ldo = p.ldo;
         ti.valid_rows = (int)min64(BM, size - m * BM);
-        ti.valid_cols = (int)min64(BN, p.nb - n * BN);
+        ti.valid_cols = (int)min64(TN, p.nb - n * TN);
+        ti.prow0 = (int64_t)pstart_s[g] + m * BM;
+        ti.col0 = n * TN;
     } else {
         const int64_t nta = (p.na + BM - 1) / BM;
         const int64_t per_g = nta * ntb;
@@ -164,6 +182,8 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, co
         ti.ldo = p.nb;
         ti.valid_rows = (int)min64(BM, p.na - m * BM);
         ti.valid_cols = (int)min64(BN, p.nb - n * BN);
+        ti.prow0 = 0;
+        ti.col0 = n * BN;
     }
     ti.sf_kstep = 512;
     return ti;
@@ -175,11 +195,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
-template <int BN>
+__device__ __forceinline__ void st_shared_u8(void* p, uint32_t v) {
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// The warp's 32 rows of 128 bytes (row = lane; words w[OFF .. OFF+31]) to global memory, every
+// store instruction writing 4 full 128-byte row segments: each lane parks its eight 16-byte
+// pieces in the warp's 32 x 128 B staging buffer (piece j of row r at slot j ^ (r & 7): no bank
+// conflicts), then lanes 8i..8i+7 store one row.  Rows >= vrows and pieces at or past
+// valid_bytes are skipped.
+template <int OFF, int NW>
+__device__ __forceinline__ void store_rows_128B(uint8_t* stg, const uint32_t (&w)[NW], uint8_t* gbase,
+                                                int64_t ld_bytes, int vrows, int valid_bytes, int lane) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) * 16),
+                     make_uint4(w[OFF + 4 * j], w[OFF + 4 * j + 1], w[OFF + 4 * j + 2], w[OFF + 4 * j + 3]));
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rl = (lane >> 3) + 4 * i, piece = lane & 7;
+        const uint4 val = ld_shared_v4(stg + rl * 128 + ((piece ^ (rl & 7)) * 16));
+        if (rl < vrows && piece * 16 < valid_bytes)
+            *reinterpret_cast<uint4*>(gbase + (int64_t)rl * ld_bytes + piece * 16) = val;
+    }
+    __syncwarp();
+}
+
+// Codes of a non-finite block (scale 0xFF): 0x7F with each element's sign, for a bf16 pair.
+__device__ __forceinline__ uint32_t nonfinite_codes2(uint32_t v) {
+    return 0x7F7Fu | ((v >> 8) & 0x80u) | ((v >> 16) & 0x8000u);
+}
+
+// One bf16 pair times f (a power of two, exact) -> two E4M3 codes (RNE, satfinite).
+__device__ __forceinline__ uint32_t quant_pair(uint32_t v, float f) { return cvt_e4m3x2(bf16lo(v) * f, bf16hi(v) * f); }
+
+template <int BN, bool kSwi>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_mm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                      const GemmParams p) {
+                      const __grid_constant__ CUtensorMap tmap_b2, const GemmParams p) {
     using C = Cfg<BN>;
+    static_assert(!kSwi || BN == 256, "the SwiGLU variant pairs 128 gate with 128 up rows");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int32_t ends_s[kMaxGroups];
     __shared__ int32_t pstart_s[kMaxGroups];
@@ -217,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int g = g0; g < g1; ++g) {
             const int32_t e = max(prev, min(max(p.offs[g], 0), Mc));
             ends_s[g] = e;
-            if (p.mode == KGROUPED && (e - prev) % 32 != 0) bad = 1;  // TMA token coordinates must stay 16B aligned
+            if (p.need32 && (e - prev) % 32 != 0) bad = 1;  // token blocks / 16-byte TMA token coordinates
             psum += ((e - prev + 127) / 128) * 128;
             prev = e;
         }
@@ -241,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             abort_s = 0;
             prefetch_tmap(&tmap_a);
             prefetch_tmap(&tmap_b);
+            if (kSwi) prefetch_tmap(&tmap_b2);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -269,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (bad_s) {
         if (threadIdx.x == 0) report(p.dev_status, MXFP8_ERR_OFFSETS);
     } else {
-        const int64_t ntb = (p.nb + BN - 1) / BN;
+        constexpr int TN = kSwi ? 128 : BN;  // output columns per tile (as in tile_info)
+        const int64_t ntb = (p.nb + TN - 1) / TN;
         const int64_t ntiles = p.mode == ROWGROUPED ? (ptotal / BM) * ntb
                                                     : (int64_t)p.G * ((p.na + BM - 1) / BM) * ntb;
 
@@ -280,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
@@ -293,11 +351,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&full[stage], C::kTx);
                     const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kt * BK);
                     tma_load_2d(sa, &tmap_a, kx, (int32_t)ti.a_row, &full[stage]);
-                    tma_load_2d(sb, &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
                     bulk_load(ssa, p.sfa + ti.sfa_base + kt * ti.sf_kstep, 512, &full[stage]);
+                    if constexpr (kSwi) {
+                        // rows 0-127: gate weights, rows 128-255: the same rows of the up weights
+                        tma_load_2d(sb, &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
+                        tma_load_2d(sb + 128 * BK, &tmap_b2, kx, (int32_t)ti.b_row, &full[stage]);
+                        bulk_load(ssb, p.sfb + ti.sfb_base[0] + kt * ti.sf_kstep, 512, &full[stage]);
+                        bulk_load(ssb + 512, p.sfb2 + ti.sfb_base[1] + kt * ti.sf_kstep, 512, &full[stage]);
+                    } else {
+                        tma_load_2d(sb, &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
 #pragma unroll
-                    for (int j = 0; j < BN / 128; ++j)
-                        bulk_load(ssb + j * 512, p.sfb + ti.sfb_base[j] + kt * ti.sf_kstep, 512, &full[stage]);
+                        for (int j = 0; j < BN / 128; ++j)
+                            bulk_load(ssb + j * 512, p.sfb + ti.sfb_base[j] + kt * ti.sf_kstep, 512, &full[stage]);
+                    }
                     issued_mask |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -317,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
                 if (ti.k_tiles == 0) continue;
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
@@ -362,6 +428,121 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile int no_abort = 0;
             mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
         } else if (warp >= 2) {
+          if constexpr (kSwi) {
+            // ------------------------------------------------ SwiGLU epilogue
+            // Per tile: h1 (gate, columns 0-127 of the accumulator) and h3 (up, 128-255) rounded to
+            // bf16 and stored; h = bf16(bf16(silu(h1)) * h3) with silu(x) = x / (1 + e^-x) in fp32
+            // (the bf16 rounding points of an elementwise bf16 SwiGLU); h quantized to MXFP8 along
+            // its row (blocks of 32 columns) and, optionally, along the tokens (the warp's 32 rows
+            // are one 32-token block of every column).
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
+            uint8_t* stg = smem + C::kOffStage + (warp - 2) * (32 * 128);
+            const int64_t H = p.nb;
+            const int64_t ct_T = ptotal / 128;  // column tiles of the token-grouped h^T scales
+            uint32_t acc_phase = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
+                if (!mbar_wait_bounded(&tfull[0], acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+                tc_fence_after();
+                uint32_t hg[64], hu[64];  // bf16 pairs (columns 2i, 2i+1) of h1 and h3
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+                for (int c = 0; c < 128; c += 32) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(taddr + c, v0);
+                    tmem_ld_32x32b_x32(taddr + 128 + c, v1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        hg[c / 2 + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+                        hu[c / 2 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[0]);
+                acc_phase ^= 1u;
+
+                const int vrows = ti.valid_rows - quarter * 32;  // rows of this warp inside the group
+                const int vcols = ti.valid_cols;
+                const int64_t row0 = ti.a_row + quarter * 32;    // first token of this warp
+                uint8_t* g1 = reinterpret_cast<uint8_t*>(p.out + row0 * H + ti.col0);
+                uint8_t* g3 = reinterpret_cast<uint8_t*>(p.out2 + row0 * H + ti.col0);
+                store_rows_128B<0>(stg, hg, g1, H * 2, vrows, vcols * 2, lane);
+                store_rows_128B<32>(stg, hg, g1 + 128, H * 2, vrows, (vcols - 64) * 2, lane);
+                store_rows_128B<0>(stg, hu, g3, H * 2, vrows, vcols * 2, lane);
+                store_rows_128B<32>(stg, hu, g3 + 128, H * 2, vrows, (vcols - 64) * 2, lane);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const float a = bf16lo(hg[i]), b = bf16hi(hg[i]);
+                    const uint32_t sl = pack_bf16x2(a / (1.0f + expf(-a)), b / (1.0f + expf(-b)));
+                    hg[i] = pack_bf16x2(bf16lo(sl) * bf16lo(hu[i]), bf16hi(sl) * bf16hi(hu[i]));
+                }
+                // row-wise: 4 blocks of 32 columns -> 128 codes and one 32-bit word of scale bytes
+                uint32_t codes[32];
+                uint32_t sword = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) m = vmax_u16x2(m, hg[16 * j + i] & 0x7FFF7FFFu);
+                    const uint32_t sc = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
+                    const float f = inv_scale_from_e8m0(sc);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t w0 = hg[16 * j + 2 * i], w1 = hg[16 * j + 2 * i + 1];
+                        codes[8 * j + i] = sc == 0xFFu ? nonfinite_codes2(w0) | (nonfinite_codes2(w1) << 16)
+                                                       : quant_pair(w0, f) | (quant_pair(w1, f) << 16);
+                    }
+                    if (r < ti.valid_rows && 32 * j < vcols) sword |= sc << (8 * j);
+                }
+                store_rows_128B<0>(stg, codes, p.hq + row0 * H + ti.col0, H, vrows, vcols, lane);
+                // the tile's row scales are exactly one 512-byte blocked tile (rows past the group: 0)
+                *reinterpret_cast<uint32_t*>(p.hs + ((ti.prow0 >> 7) * p.hs_ct + (ti.col0 >> 7)) * 512 + lane * 16 +
+                                             quarter * 4) = sword;
+                if (p.hTq != nullptr) {
+                    // group sizes are multiples of 32 here (device-checked), so a warp's block is
+                    // either all inside the group or all padding
+                    const int64_t cq = ti.prow0 / 32 + quarter;  // scale column of this 32-token block
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t my_s = 0;  // scale of column 32j + lane
+                        if (vrows > 0 && 32 * j < vcols) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const uint32_t w = hg[16 * j + i];
+                                const uint32_t slo = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, w & 0x7FFFu));
+                                const uint32_t shi =
+                                    e8m0_from_absbits(__reduce_max_sync(0xffffffffu, (w >> 16) & 0x7FFFu));
+                                uint32_t c2 = cvt_e4m3x2(bf16lo(w) * inv_scale_from_e8m0(slo),
+                                                         bf16hi(w) * inv_scale_from_e8m0(shi));
+                                if (slo == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu | ((w >> 8) & 0x80u);
+                                if (shi == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u | ((w >> 16) & 0x8000u);
+                                // transpose through shared memory: byte (column c, token lane) at c*32 + lane
+                                st_shared_u8(stg + (2 * i) * 32 + lane, c2 & 0xFFu);
+                                st_shared_u8(stg + (2 * i + 1) * 32 + lane, c2 >> 8);
+                                my_s = lane == 2 * i ? slo : (lane == 2 * i + 1 ? shi : my_s);
+                            }
+                            __syncwarp();
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int cc = 16 * h2 + (lane >> 1);  // column within the chunk
+                                const uint4 val = ld_shared_v4(stg + cc * 32 + (lane & 1) * 16);
+                                if (32 * j + cc < vcols)
+                                    *reinterpret_cast<uint4*>(p.hTq + (ti.col0 + 32 * j + cc) * p.M + row0 +
+                                                              (lane & 1) * 16) = val;
+                            }
+                            __syncwarp();
+                            if (32 * j + lane >= vcols) my_s = 0;
+                        }
+                        const int64_t cH = ti.col0 + 32 * j + lane;  // row of h^T (columns past H: padding 0)
+                        p.hTs[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] =
+                            (uint8_t)my_s;
+                    }
+                }
+            }
+          } else {
             // ------------------------------------------------ epilogue
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
@@ -369,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
                 const bool row_ok = r < ti.valid_rows;
                 __nv_bfloat16* orow = ti.out + (int64_t)r * ti.ldo;
                 __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo;  // first row of this warp
@@ -424,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
             }
+          }
         }
     }
     tc_fence_before();
@@ -808,17 +990,22 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+// b2 (SwiGLU variant only): the up weights, same shape as b; each B map then has 128-row boxes.
+template <int BN, bool kSwi = false>
 static mxfp8_status_t launch_gemm(const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
-                                  int64_t b_cols, GemmParams& p, int64_t tiles_bound, cudaStream_t st) {
+                                  int64_t b_cols, GemmParams& p, int64_t tiles_bound, cudaStream_t st,
+                                  const void* b2 = nullptr) {
     using C = Cfg<BN>;
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, BN)) return MXFP8_ERR_DRIVER;
+    CUtensorMap ma, mb, mb2;
+    const int b_box = kSwi ? 128 : BN;
+    if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, b_box)) return MXFP8_ERR_DRIVER;
+    if (kSwi ? !make_map(&mb2, b2, b_rows, b_cols, b_box) : false) return MXFP8_ERR_DRIVER;
+    if (!kSwi) mb2 = mb;
     static std::atomic<int> attr_set[host::kMaxDevices];
-    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_kernel<BN>), C::kSmem, attr_set))
+    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_kernel<BN, kSwi>), C::kSmem, attr_set))
         return MXFP8_ERR_LAUNCH;
     const int grid = (int)max64(1, min64(tiles_bound, host::num_sms()));
-    grouped_mm_kernel<BN><<<grid, kThreads, C::kSmem, st>>>(ma, mb, p);
+    grouped_mm_kernel<BN, kSwi><<<grid, kThreads, C::kSmem, st>>>(ma, mb, mb2, p);
     return host::last_launch_status();
 }
 
@@ -977,6 +1164,7 @@ extern "C" mxfp8_status_t mxfp8_grouped_mm_wgrad(const void* doutT_q, const void
     p.M = M;
     p.out = static_cast<__nv_bfloat16*>(dw_bf16);
     p.mode = KGROUPED;
+    p.need32 = 1;
     p.dev_status = dev_status;
     p.timeout_ns = default_timeout_ns();
     if (K >= 256 && kPairForKGrouped) {
@@ -991,4 +1179,51 @@ extern "C" mxfp8_status_t mxfp8_grouped_mm_wgrad(const void* doutT_q, const void
     }
     const int64_t bound = (int64_t)G * ((N + BM - 1) / BM) * ((K + 127) / 128);
     return launch_gemm<128>(doutT_q, N, M, aT_q, K, M, p, bound, st);
+}
+
+extern "C" mxfp8_status_t mxfp8_grouped_mm_swiglu_fwd(const void* x_q, const void* x_s, const void* wg_q,
+                                                      const void* wg_s, const void* wu_q, const void* wu_s,
+                                                      const int32_t* offs, int32_t G, int64_t M, int64_t H, int64_t D,
+                                                      void* h1_bf16, void* h3_bf16, void* h_q, void* h_s, void* hT_q,
+                                                      void* hT_s, int32_t* dev_status, mxfp8_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!x_q || !x_s || !wg_q || !wg_s || !wu_q || !wu_s || !offs || !h1_bf16 || !h3_bf16 || !h_q || !h_s)
+        return MXFP8_ERR_NULL;
+    if ((hT_q == nullptr) != (hT_s == nullptr)) return MXFP8_ERR_NULL;
+    if (G < 1 || G > MXFP8_MAX_GROUPS || M < 0 || H <= 0 || D <= 0 || M > INT32_MAX || (int64_t)G * H > INT32_MAX ||
+        D > INT32_MAX)
+        return MXFP8_ERR_SHAPE;
+    if (H % 32 || D % 32 || (hT_q && M % 32)) return MXFP8_ERR_ALIGN;
+    const void* ptrs[] = {x_q, x_s, wg_q, wg_s, wu_q, wu_s, h1_bf16, h3_bf16, h_q, h_s};
+    for (const void* q : ptrs)
+        if (!host::aligned16(q)) return MXFP8_ERR_ALIGN;
+    if (hT_q && (!host::aligned16(hT_q) || !host::aligned16(hT_s))) return MXFP8_ERR_ALIGN;
+    if (mxfp8_status_t a = host::check_arch(); a != MXFP8_OK) return a;
+    if (M == 0) return MXFP8_OK;
+    GemmParams p{};
+    p.sfa = static_cast<const uint8_t*>(x_s);
+    p.sfb = static_cast<const uint8_t*>(wg_s);
+    p.sfb2 = static_cast<const uint8_t*>(wu_s);
+    p.sfa_ct = (D + 127) / 128;
+    p.sfb_ct = (D + 127) / 128;
+    p.sfb_estride = ((H + 127) / 128) * 128 * p.sfb_ct * 4;
+    p.nb = H;
+    p.kc = D;
+    p.offs = offs;
+    p.G = G;
+    p.M = M;
+    p.out = static_cast<__nv_bfloat16*>(h1_bf16);
+    p.out2 = static_cast<__nv_bfloat16*>(h3_bf16);
+    p.ldo = H;
+    p.hq = static_cast<uint8_t*>(h_q);
+    p.hs = static_cast<uint8_t*>(h_s);
+    p.hs_ct = (H + 127) / 128;
+    p.hTq = static_cast<uint8_t*>(hT_q);
+    p.hTs = static_cast<uint8_t*>(hT_s);
+    p.mode = ROWGROUPED;
+    p.need32 = hT_q != nullptr;
+    p.dev_status = dev_status;
+    p.timeout_ns = default_timeout_ns();
+    const int64_t bound = ((M + BM - 1) / BM + G) * ((H + 127) / 128);
+    return launch_gemm<256, true>(x_q, M, D, wg_q, (int64_t)G * H, D, p, bound, st, wu_q);
 }

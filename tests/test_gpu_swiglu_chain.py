@@ -1,7 +1,8 @@
 """The SwiGLU routed expert as three chained MXFP8 grouped GEMMs (gate, up, down) with the
 elementwise SwiGLU in torch, forward and backward, against the same chain computed by the
 oracle (its own quantization, fp64 GEMMs, the glue in fp64 with bf16 rounding of every
-intermediate).  No GPU value feeds the oracle.
+intermediate); and the fused expert (mxfp8_swiglu_expert: gate/up GEMMs with the SwiGLU and
+its quantization in the epilogue) against the same oracle chain.  No GPU value feeds the oracle.
 
 Tolerance: the per-GEMM bound 1e-2|o| + 1e-3 rms(o) holds for every single GEMM
 (test_gpu_grouped_mm.py).  Chained, the bf16 intermediates of the GPU (torch CUDA glue) and of
@@ -16,7 +17,7 @@ import torch
 
 import oracle
 from mxfp8_precision_moe_gb300 import synth
-from tests._util import f64, require_gpu, sizes_to_ends, u16
+from tests._util import assert_gemm_close, f64, require_gpu, sizes_to_ends, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +32,9 @@ def mx():
 
 
 def bf16_round(a: np.ndarray) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16)
+    """bf16 round-to-nearest-even of fp64 values, one rounding (the oracle's pinned routine)."""
+    b = oracle.bf16_from_f64(np.ascontiguousarray(a, np.float64))
+    return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
 
 
 def o_fwd(A, W, sizes):
@@ -61,49 +64,114 @@ def chain_close(got, ref, what):
     assert ok.mean() >= 0.999, f"{what}: {int((~ok).sum())}/{ok.size} elements outside the chain bound"
 
 
-def test_swiglu_expert_chain_fwd_bwd(mx):
-    sizes = [384, 256]
-    G, M, D, H = 2, sum(sizes), 256, 512
+SIZES = [384, 256]
+G, D, H = 2, 256, 512
+M = sum(SIZES)
+
+
+def inputs():
     x = synth.randn_bf16((M, D), 1.0, seed=61)
     Wg = synth.randn_bf16((G, H, D), 0.05, seed=62)
     Wu = synth.randn_bf16((G, H, D), 0.05, seed=63)
     Wd = synth.randn_bf16((G, D, H), 0.05, seed=64)
     dY = synth.randn_bf16((M, D), 1e-2, seed=65)
-    offs = torch.tensor(sizes_to_ends(sizes).astype(np.int32), device="cuda")
+    return x, Wg, Wu, Wd, dY
 
-    # ---- GPU: three differentiable MXFP8 grouped GEMMs, SwiGLU glue in torch (bf16)
-    xg = x.cuda().requires_grad_(True)
-    Wgg, Wug, Wdg = (t.cuda().requires_grad_(True) for t in (Wg, Wu, Wd))
-    h1 = mx.to_mxfp8_then_scaled_grouped_mm(xg, Wgg, offs)
-    h3 = mx.to_mxfp8_then_scaled_grouped_mm(xg, Wug, offs)
-    h = torch.nn.functional.silu(h1) * h3
-    y = mx.to_mxfp8_then_scaled_grouped_mm(h, Wdg, offs)
-    y.backward(dY.cuda())
-    torch.cuda.synchronize()
 
-    # ---- oracle chain: fp64 GEMMs; the glue in fp64 with a bf16 rounding after each elementwise
-    # op, the same places the bf16 torch glue rounds (silu(h1) and the product; in the backward
-    # dh*silu(h1), dh*h3 and the silu derivative product)
+def oracle_chain(x, Wg, Wu, Wd, dY, sizes):
+    """The expert on the oracle: fp64 GEMMs of oracle-quantized operands, the SwiGLU glue in
+    fp64 with a bf16 rounding after each elementwise op (silu(h1), the product; in the
+    backward dh*silu(h1), dh*h3 and the silu-derivative product)."""
     o_h1 = bf16_round(o_fwd(x, Wg, sizes))
     o_h3 = bf16_round(o_fwd(x, Wu, sizes))
     h1d, h3d = o_h1.double().numpy(), o_h3.double().numpy()
     sig = 1.0 / (1.0 + np.exp(-h1d))
     silu = bf16_round(h1d * sig).double().numpy()
     o_h = bf16_round(silu * h3d)
-    o_y = o_fwd(o_h, Wd, sizes)
+    o = dict(y=o_fwd(o_h, Wd, sizes))
     # backward: dh = dY Wd (dgrad); dWd = dY^T h (wgrad); then the SwiGLU backward
     o_dh = bf16_round(o_dgrad(dY, Wd, sizes))
-    o_dWd = o_wgrad(dY, o_h, sizes)
+    o["dWd"] = o_wgrad(dY, o_h, sizes)
     dhd = o_dh.double().numpy()
     d_h3 = bf16_round(dhd * silu)                                          # d/dh3 of silu(h1) * h3
     d_silu = bf16_round(dhd * h3d).double().numpy()
     d_h1 = bf16_round(d_silu * sig * (1.0 + h1d * (1.0 - sig)))            # silu derivative
-    o_dx = o_dgrad(d_h1, Wg, sizes) + o_dgrad(d_h3, Wu, sizes)
-    o_dWg = o_wgrad(d_h1, x, sizes)
-    o_dWu = o_wgrad(d_h3, x, sizes)
+    o["dx"] = o_dgrad(d_h1, Wg, sizes) + o_dgrad(d_h3, Wu, sizes)
+    o["dWg"] = o_wgrad(d_h1, x, sizes)
+    o["dWu"] = o_wgrad(d_h3, x, sizes)
+    return o
 
-    chain_close(f64(y), o_y, "y")
-    chain_close(f64(Wdg.grad), o_dWd, "dW_down")
-    chain_close(f64(Wgg.grad), o_dWg, "dW_gate")
-    chain_close(f64(Wug.grad), o_dWu, "dW_up")
-    chain_close(f64(xg.grad), o_dx, "dx")
+
+def gpu_leaves(x, Wg, Wu, Wd):
+    return [t.cuda().requires_grad_(True) for t in (x, Wg, Wu, Wd)]
+
+
+def offs_dev():
+    return torch.tensor(sizes_to_ends(SIZES).astype(np.int32), device="cuda")
+
+
+def check_chain(o, y, xg, Wgg, Wug, Wdg):
+    chain_close(f64(y), o["y"], "y")
+    chain_close(f64(Wdg.grad), o["dWd"], "dW_down")
+    chain_close(f64(Wgg.grad), o["dWg"], "dW_gate")
+    chain_close(f64(Wug.grad), o["dWu"], "dW_up")
+    chain_close(f64(xg.grad), o["dx"], "dx")
+
+
+def test_swiglu_expert_chain_fwd_bwd(mx):
+    """Three differentiable MXFP8 grouped GEMMs with the SwiGLU glue in torch (bf16)."""
+    x, Wg, Wu, Wd, dY = inputs()
+    offs = offs_dev()
+    xg, Wgg, Wug, Wdg = gpu_leaves(x, Wg, Wu, Wd)
+    h1 = mx.to_mxfp8_then_scaled_grouped_mm(xg, Wgg, offs)
+    h3 = mx.to_mxfp8_then_scaled_grouped_mm(xg, Wug, offs)
+    h = torch.nn.functional.silu(h1) * h3
+    y = mx.to_mxfp8_then_scaled_grouped_mm(h, Wdg, offs)
+    y.backward(dY.cuda())
+    torch.cuda.synchronize()
+    check_chain(oracle_chain(x, Wg, Wu, Wd, dY, SIZES), y, xg, Wgg, Wug, Wdg)
+
+
+def test_fused_swiglu_expert_fwd_bwd(mx):
+    """The fused expert (gate/up GEMMs with SwiGLU + quantization in the epilogue, down GEMM
+    on the fused kernel's codes) against the same oracle chain, and against the unfused chain
+    on the GPU within the per-GEMM bound."""
+    x, Wg, Wu, Wd, dY = inputs()
+    offs = offs_dev()
+    xg, Wgg, Wug, Wdg = gpu_leaves(x, Wg, Wu, Wd)
+    y = mx.mxfp8_swiglu_expert(xg, Wgg, Wug, Wdg, offs)
+    y.backward(dY.cuda())
+    torch.cuda.synchronize()
+    check_chain(oracle_chain(x, Wg, Wu, Wd, dY, SIZES), y, xg, Wgg, Wug, Wdg)
+
+    ug = gpu_leaves(x, Wg, Wu, Wd)
+    h = torch.nn.functional.silu(mx.to_mxfp8_then_scaled_grouped_mm(ug[0], ug[1], offs)) * \
+        mx.to_mxfp8_then_scaled_grouped_mm(ug[0], ug[2], offs)
+    yu = mx.to_mxfp8_then_scaled_grouped_mm(h, ug[3], offs)
+    yu.backward(dY.cuda())
+    torch.cuda.synchronize()
+    for a, b, what in ((y, yu, "y"), (xg.grad, ug[0].grad, "dx"), (Wgg.grad, ug[1].grad, "dWg"),
+                       (Wug.grad, ug[2].grad, "dWu"), (Wdg.grad, ug[3].grad, "dWd")):
+        assert_gemm_close(f64(a), f64(b), what=f"fused vs unfused {what}")
+
+
+def test_fused_swiglu_expert_prequantized_weights(mx):
+    """Weights through an Mxfp8WeightCache give bit-identical results to on-the-fly quantization."""
+    x, Wg, Wu, Wd, dY = inputs()
+    offs = offs_dev()
+    outs = []
+    cache = mx.Mxfp8WeightCache()
+    leaves_w = gpu_leaves(x, Wg, Wu, Wd)[1:]
+    for kw in ({}, {"weight_cache": cache}, {"weight_cache": cache}):
+        xg = x.cuda().requires_grad_(True)
+        for w in leaves_w:
+            w.grad = None
+        y = mx.mxfp8_swiglu_expert(xg, *leaves_w, offs, **kw)
+        y.backward(dY.cuda())
+        torch.cuda.synchronize()
+        outs.append([y.detach().clone(), xg.grad.clone()] + [w.grad.clone() for w in leaves_w])
+    assert cache.misses == 3 and cache.hits == 3
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(outs[1], outs[2]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))

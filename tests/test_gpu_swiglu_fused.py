@@ -1,0 +1,212 @@
+"""The gate/up GEMMs with the SwiGLU and its MXFP8 quantization fused into the epilogue
+(mxfp8_grouped_mm_swiglu_fwd) against the oracle's gate/up stage ("MXFP8 (Micro-scaling
+FP8)", "Neutralizing quantization overhead": quantization fused into the kernel that
+produces the activation; "feat(moe): add MoK MXFP8 expert support": gate/up/down weights).
+
+Parity bars:
+- h1, h3 (bf16 GEMM outputs): the GEMM bound |gpu - o| <= 1e-2 |o| + 1e-3 rms(o).
+- Exact-arithmetic inputs (every fp32 accumulation exact, so h1 and h3 equal the oracle's):
+  h_q, h_s, hT_q, hT_s byte for byte, padding included.  The only freedom left is silu in fp32
+  versus fp64; elements whose fp64 silu lies within 2^-20 (relative) of a bf16 rounding
+  midpoint may round either way and are excluded.
+- Random inputs: h1/h3 may differ from the oracle's by a bf16 ulp where fp32 accumulation
+  crosses a rounding midpoint, and a one-ulp change of h moves its E4M3 code by at most one
+  step (or its block scale by one).  So every dequantized element must lie within one E4M3
+  step of the oracle's, every scale within one of the oracle's, and at least 99% of codes
+  and 99.9% of scales must be identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp8_precision_moe_gb300 import synth
+from tests._util import assert_gemm_close, f64, require_gpu, sizes_to_ends, u8, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mx():
+    require_gpu()
+    import mxfp8_precision_moe_gb300 as m
+
+    m.load()
+    return m
+
+
+def offs_of(sizes):
+    return torch.tensor(sizes_to_ends(sizes).astype(np.int32), device="cuda")
+
+
+def run_fused(mx, x, Wg, Wu, sizes, token_wise=True):
+    offs = offs_of(sizes)
+    status = mx.new_status()
+    xq, xs, _, _ = mx.mxfp8_quantize_2d(x.cuda(), mx.ROW, mx.SCALES_BLOCKED, offs)
+    gq, gs, _, _ = mx.mxfp8_quantize_3d_experts(Wg.cuda(), mx.ROW, mx.SCALES_BLOCKED)
+    uq, us, _, _ = mx.mxfp8_quantize_3d_experts(Wu.cuda(), mx.ROW, mx.SCALES_BLOCKED)
+    out = mx.mxfp8_grouped_mm_swiglu_fwd(xq, xs, gq, gs, uq, us, offs, token_wise, status)
+    torch.cuda.synchronize()
+    return out, status
+
+
+def decode_blocked(kind, R, Kb, ends):
+    """Blocked-layout position of every compact scale (r, kb), found by passing probe arrays
+    through the oracle's own layout function; also the mask of bytes that hold a scale."""
+    if kind == "rows":
+        place = lambda a: oracle.blocked_rowgroups(a, ends)
+    else:
+        place = lambda a: oracle.blocked_colgroups(a, ends)
+    r = np.arange(R)[:, None] + np.zeros((1, Kb), np.int64)
+    k = np.zeros((R, 1), np.int64) + np.arange(Kb)[None, :]
+    probes = [place(((v >> sh) & 0xFF).astype(np.uint8)) for v in (r, k) for sh in (0, 8, 16)]
+    valid = place(np.ones((R, Kb), np.uint8)).astype(bool)
+    pr = probes[0].astype(np.int64) | (probes[1].astype(np.int64) << 8) | (probes[2].astype(np.int64) << 16)
+    pk = probes[3].astype(np.int64) | (probes[4].astype(np.int64) << 8) | (probes[5].astype(np.int64) << 16)
+    pos = np.zeros((R, Kb), np.int64)
+    idx = np.nonzero(valid)[0]
+    pos[pr[idx], pk[idx]] = idx
+    return pos, valid
+
+
+def e4m3_step(v, s):
+    """One E4M3 quantum at magnitude |v| in a block with scale byte s (subnormal step 2^-9)."""
+    e = s.astype(np.int64) - 127
+    y = np.abs(v) * np.ldexp(1.0, -e)
+    ex = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+    return np.ldexp(1.0, (ex - 3 + e).astype(np.int64))
+
+
+def compare_quantized(q_gpu, s_gpu_blk, q_o, s_o, kind, ends, exact, exclude=None, what=""):
+    R, C = q_o.shape
+    pos, valid = decode_blocked(kind, R, C // 32, ends)
+    s_blk = s_gpu_blk[:valid.size]
+    assert np.all(s_blk[~valid] == 0), f"{what}: padding bytes not zero"
+    s_g = s_blk[pos]
+    if exact:
+        keep = np.ones(q_o.shape, bool) if exclude is None else ~exclude
+        blk_keep = keep.reshape(R, C // 32, 32).all(axis=2)
+        assert np.array_equal(s_g[blk_keep], s_o[blk_keep]), f"{what}: scales differ"
+        sel = keep & np.repeat(blk_keep, 32, axis=1)
+        assert np.array_equal(q_gpu[sel], q_o[sel]), f"{what}: {int((q_gpu != q_o)[sel].sum())} codes differ"
+        return
+    tab = oracle.e4m3_table()
+    sg_e, so_e = np.repeat(s_g, 32, axis=1), np.repeat(s_o, 32, axis=1)
+    dg = tab[q_gpu] * np.ldexp(1.0, sg_e.astype(np.int64) - 127)
+    do = tab[q_o] * np.ldexp(1.0, so_e.astype(np.int64) - 127)
+    step = e4m3_step(np.maximum(np.abs(dg), np.abs(do)), np.maximum(sg_e, so_e))
+    assert np.all(np.abs(s_g.astype(int) - s_o.astype(int)) <= 1), f"{what}: a scale differs by more than one"
+    assert np.all(np.abs(dg - do) <= step), f"{what}: {int((np.abs(dg - do) > step).sum())} elements beyond one step"
+    assert (q_gpu == q_o).mean() >= 0.99, f"{what}: code agreement {(q_gpu == q_o).mean():.4f}"
+    assert (s_g == s_o).mean() >= 0.999, f"{what}: scale agreement {(s_g == s_o).mean():.5f}"
+
+
+def near_silu_ties(h1_u16):
+    """Elements whose fp64 silu(h1) lies within 2^-20 (relative) of a bf16 rounding midpoint."""
+    a = (h1_u16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    v = np.abs(a / (1.0 + np.exp(-a)))
+    ex = np.floor(np.log2(np.maximum(v, 2.0 ** -126)))
+    q = np.ldexp(1.0, (ex - 7).astype(np.int64))       # bf16 quantum at v
+    frac = v / q - np.floor(v / q)
+    return (np.abs(frac - 0.5) * q <= v * 2.0 ** -20) & (v > 0)
+
+
+CASES = [
+    ([384, 0, 256, 96], 384, 256),   # 4 groups: an empty one, a 96-row tail tile
+    ([160, 96], 160, 128),           # ragged H: the second column tile has 32 valid columns
+    ([64], 128, 512),                # one group, 4 k-tiles
+]
+
+
+@pytest.mark.parametrize("sizes,H,D", CASES)
+def test_fused_gate_up_random_inputs(mx, sizes, H, D):
+    G, M = len(sizes), sum(sizes)
+    x = synth.randn_bf16((M, D), 1.0, seed=80 + H)
+    Wg = synth.randn_bf16((G, H, D), 0.08, seed=81 + H)
+    Wu = synth.randn_bf16((G, H, D), 0.08, seed=82 + H)
+    (h1, h3, hq, hs, hTq, hTs), status = run_fused(mx, x, Wg, Wu, sizes)
+    mx.read_status(status)
+    ends = sizes_to_ends(sizes)
+    o = oracle.swiglu_gate_up(u16(x), u16(Wg), u16(Wu), ends)
+    assert_gemm_close(f64(h1), o["h1_f64"], what="h1")
+    assert_gemm_close(f64(h3), o["h3_f64"], what="h3")
+    compare_quantized(u8(hq), u8(hs), o["h_q"], o["h_s"], "rows", ends, exact=False, what="h (row-wise)")
+    compare_quantized(u8(hTq), u8(hTs), o["hT_q"], o["hT_s"], "cols", ends, exact=False, what="h (token-wise)")
+
+
+def exact_inputs(M, D, G, H, seed):
+    """Values with few significant bits: every partial sum of the GEMMs is exact in fp32."""
+    g = torch.Generator().manual_seed(seed)
+    xv = torch.tensor([0.0, 0.5, -0.5, 1.0, -1.0, 2.0, -2.0])
+    wv = torch.tensor([0.0, 1 / 16, -1 / 16, 1 / 8, -1 / 8, 1 / 4, -1 / 4])
+    x = xv[torch.randint(0, 7, (M, D), generator=g)].to(torch.bfloat16)
+    Wg = wv[torch.randint(0, 7, (G, H, D), generator=g)].to(torch.bfloat16)
+    Wu = wv[torch.randint(0, 7, (G, H, D), generator=g)].to(torch.bfloat16)
+    return x, Wg, Wu
+
+
+def test_fused_gate_up_exact_inputs_bit_exact(mx):
+    sizes, H, D = [128, 64, 0, 192], 256, 256
+    G, M = len(sizes), sum(sizes)
+    x, Wg, Wu = exact_inputs(M, D, G, H, seed=90)
+    (h1, h3, hq, hs, hTq, hTs), status = run_fused(mx, x, Wg, Wu, sizes)
+    mx.read_status(status)
+    ends = sizes_to_ends(sizes)
+    o = oracle.swiglu_gate_up(u16(x), u16(Wg), u16(Wu), ends)
+    assert np.array_equal(u16(h1), o["h1"]) and np.array_equal(u16(h3), o["h3"])
+    ties = near_silu_ties(o["h1"])
+    compare_quantized(u8(hq), u8(hs), o["h_q"], o["h_s"], "rows", ends, exact=True, exclude=ties, what="h rows")
+    compare_quantized(u8(hTq), u8(hTs), o["hT_q"], o["hT_s"], "cols", ends, exact=True, exclude=ties.T,
+                      what="h tokens")
+    assert ties.mean() < 1e-3
+
+
+def test_token_wise_requires_groups_of_32(mx):
+    sizes, H, D = [48, 80], 128, 128
+    G, M = len(sizes), sum(sizes)
+    x = synth.randn_bf16((M, D), 1.0, seed=95)
+    Wg = synth.randn_bf16((G, H, D), 0.08, seed=96)
+    Wu = synth.randn_bf16((G, H, D), 0.08, seed=97)
+    _, status = run_fused(mx, x, Wg, Wu, sizes, token_wise=True)
+    with pytest.raises(mx.Mxfp8Error) as e:
+        mx.read_status(status)
+    assert e.value.status == 7  # MXFP8_ERR_OFFSETS
+    # row-wise only: any group sizes
+    (h1, h3, hq, hs, hTq, hTs), status = run_fused(mx, x, Wg, Wu, sizes, token_wise=False)
+    mx.read_status(status)
+    assert hTq is None and hTs is None
+    ends = sizes_to_ends(sizes)
+    o = oracle.swiglu_gate_up(u16(x), u16(Wg), u16(Wu), ends)
+    assert_gemm_close(f64(h1), o["h1_f64"], what="h1")
+    compare_quantized(u8(hq), u8(hs), o["h_q"], o["h_s"], "rows", ends, exact=False, what="h (row-wise)")
+
+
+def test_fused_equals_unfused_gpu_path(mx):
+    """Same GPU, two routes: the fused epilogue and (forward GEMM x2, torch bf16 SwiGLU,
+    ROW|COL quantize).  h1/h3 come from the same MMA sequence; torch's bf16 silu evaluates
+    the same fp32 expression, so the quantized bytes should agree almost everywhere."""
+    sizes, H, D = [256, 128, 96], 256, 256
+    G, M = len(sizes), sum(sizes)
+    x = synth.randn_bf16((M, D), 1.0, seed=98)
+    Wg = synth.randn_bf16((G, H, D), 0.08, seed=99)
+    Wu = synth.randn_bf16((G, H, D), 0.08, seed=100)
+    (h1, h3, hq, hs, hTq, hTs), status = run_fused(mx, x, Wg, Wu, sizes)
+    mx.read_status(status)
+    offs = offs_of(sizes)
+    xq, xs, _, _ = mx.mxfp8_quantize_2d(x.cuda(), mx.ROW, mx.SCALES_BLOCKED, offs)
+    gq, gs, _, _ = mx.mxfp8_quantize_3d_experts(Wg.cuda(), mx.ROW, mx.SCALES_BLOCKED)
+    uq, us, _, _ = mx.mxfp8_quantize_3d_experts(Wu.cuda(), mx.ROW, mx.SCALES_BLOCKED)
+    r1 = mx.mxfp8_grouped_mm_fwd(xq, xs, gq, gs, offs)
+    r3 = mx.mxfp8_grouped_mm_fwd(xq, xs, uq, us, offs)
+    assert torch.equal(r1.view(torch.int16), h1.view(torch.int16))
+    assert torch.equal(r3.view(torch.int16), h3.view(torch.int16))
+    h = torch.nn.functional.silu(r1) * r3
+    q, s, qT, sT = mx.mxfp8_quantize_2d(h, mx.ROW | mx.COL, mx.SCALES_BLOCKED, offs)
+    torch.cuda.synchronize()
+    assert (u8(q) == u8(hq)).mean() >= 0.999
+    assert (u8(qT) == u8(hTq)).mean() >= 0.999
+    ends = sizes_to_ends(sizes)
+    n_row = oracle.blocked_rowgroups_bytes(ends, H // 32)
+    n_col = oracle.blocked_colgroups_bytes(H, ends)
+    assert (u8(s)[:n_row] == u8(hs)[:n_row]).mean() >= 0.999
+    assert (u8(sT)[:n_col] == u8(hTs)[:n_col]).mean() >= 0.999
