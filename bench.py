@@ -52,8 +52,13 @@ WORKLOAD_TEXT = {
     "scout": WORKLOAD,
     "imbalanced": "Fine-grained imbalanced experts fwd+bwd: G=16, K=7168, N=2048, M=32768, group 1 = 13120 tokens, "
                   "groups 0/7/15 empty, 1% x100 activation outliers",
-    "swiglu": "SwiGLU routed expert fwd+bwd GEMMs: G=2, M=65600 (39360/26240), gate/up W[2,8192,5120], "
-              "down W[2,5120,8192]; 9 grouped GEMMs, synthetic stand-ins for the SwiGLU intermediates",
+    "swiglu": "SwiGLU routed expert fwd+bwd: G=2, M=65600 (39360/26240), D=5120, H=8192, gate/up W[2,8192,5120], "
+              "down W[2,5120,8192]; gate/up GEMMs with the SwiGLU and its MXFP8 quantization fused into the "
+              "epilogue, 9 GEMMs, SwiGLU backward in torch bf16",
+    "swiglu_unfused": "SwiGLU routed expert fwd+bwd as swiglu, with separate gate and up GEMMs, the SwiGLU in "
+                      "torch bf16 and a separate ROW|COL quantization of h",
+    "swiglu_standin": "SwiGLU routed expert GEMMs: G=2, M=65600 (39360/26240), gate/up W[2,8192,5120], "
+                      "down W[2,5120,8192]; 9 grouped GEMMs, seeded stand-ins for the SwiGLU intermediates",
     "tiny": "Tiny: G=2, A[256,256], offs [128,256], W[2,128,256] (latency-bound; parity case)",
     "scout_mb4": "Llama4-Scout-like routed experts, one optimizer step of 4 microbatches (G=8, K=5120, N=8192, "
                  "M=16384 tokens each, Zipf(1.1) group sizes in 32-token chunks, seeds 0-3): W quantized once "
@@ -67,11 +72,14 @@ def workload_parts(name: str, dev) -> list:
 
     if name in ("scout", "imbalanced", "tiny"):
         return [synth.workload(name, seed=0, device=dev)]
+    if name in ("swiglu", "swiglu_unfused"):
+        return [synth.workload("swiglu", seed=0, device=dev)]
     if name == "scout_mb4":
         mbs = [synth.workload("scout", seed=i, device=dev) for i in range(4)]
         for w in mbs[1:]:
             w["W"] = mbs[0]["W"]  # one weight tensor for the whole optimizer step
         return mbs
+    # swiglu_standin: the expert's 9 GEMMs as three plain problems with seeded intermediates
     s = synth.workload("swiglu", seed=0, device=dev)
     G, M, D, H = s["G"], s["M"], s["D"], s["H"]
     h = synth.randn_bf16((M, H), 1.0, seed=50, device=dev)      # stands in for silu(x Wg^T) * (x Wu^T)
@@ -81,6 +89,13 @@ def workload_parts(name: str, dev) -> list:
     return [dict(common, N=H, K=D, A=s["x"], W=s["Wg"], dOut=dh1),
             dict(common, N=H, K=D, A=s["x"], W=s["Wu"], dOut=dh3),
             dict(common, N=D, K=H, A=h, W=s["Wd"], dOut=s["dY"])]
+
+
+def step_inputs(step, parts) -> list:
+    """The bf16 input tensors one step reads."""
+    if hasattr(step, "x"):
+        return [step.x, step.dY, *step.W.values()]
+    return [t for p in parts for t in (p["A"], p["W"], p["dOut"])]
 
 
 def kernel_src_sha() -> str:
@@ -100,7 +115,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--no-baseline", action="store_true", help="skip the cuBLAS bf16 comparison leg")
-    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "tiny", "scout_mb4", "sweep"],
+    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "swiglu_unfused", "swiglu_standin", "tiny", "scout_mb4",
+                             "sweep"],
                     help="scout (default, the reported line); the others are extra measurements")
     return ap.parse_args()
 
@@ -306,6 +322,117 @@ class StepGroup:
             st.check_status()
 
 
+class SwiGLUStep:
+    """One fwd+bwd of the SwiGLU routed expert y = (silu(x Wg^T) * (x Wu^T)) Wd^T through the C ABI.
+
+    fused:   the gate/up GEMMs write h1, h3 and h already quantized both ways (one kernel);
+    unfused: two forward GEMMs, h = silu(h1) * h3 in torch bf16, a ROW|COL quantization of h.
+    Both then run the down GEMM, and the backward: dY quantized both ways, down dgrad and wgrad,
+    the SwiGLU backward in torch bf16 ops, dh1/dh3 quantized both ways, two dgrads (summed) and two
+    wgrads.  Entries whose name starts with "torch." are torch elementwise glue, not library kernels."""
+
+    def __init__(self, s: dict, device, fused: bool):
+        import mxfp8_precision_moe_gb300 as mx
+        from mxfp8_precision_moe_gb300.swiglu import swiglu_backward_bf16
+
+        L = mx.load()
+        self.mx, self.L = mx, L
+        G, M, D, H = s["G"], s["M"], s["D"], s["H"]
+        self.G, self.M, self.N, self.K = G, M, H, D
+        u8 = lambda *sh: torch.empty(sh, dtype=torch.uint8, device=device)
+        bf = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=device)
+        P = lambda t: ctypes.c_void_p(t.data_ptr())
+        sb, sc = mx.mxfp8_scale_bytes, mx.mxfp8_scale_bytes_colgroups
+        ce = lambda r, c: ((r + 127) // 128) * 128 * ((c + 127) // 128) * 4
+        self.x, self.dY, self.offs = s["x"].to(device), s["dY"].to(device), s["offs"].to(device)
+        self.W = {n: s[n].to(device) for n in ("Wg", "Wu", "Wd")}
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        st = P(self.status)
+        RC = 3
+        tok = lambda cols: (u8(M, cols), u8(sb(M, cols, G, 1)), u8(cols, M), u8(sc(cols, M, G)))
+        xq = tok(D)
+        wq = {}
+        for n, (r, c) in (("Wg", (H, D)), ("Wu", (H, D)), ("Wd", (D, H))):
+            wq[n] = (u8(G, r, c), u8(G, ce(r, c)), u8(G, c, r), u8(G, ce(c, r)))
+        h1, h3 = bf(M, H), bf(M, H)
+        hq = tok(H)
+        dYq = tok(D)
+        dh, dh1, dh3 = bf(M, H), bf(M, H), bf(M, H)
+        a1, a3 = tok(H), tok(H)
+        y, dx, dx2 = bf(M, D), bf(M, D), bf(M, D)
+        dWg, dWu, dWd = bf(G, H, D), bf(G, H, D), bf(G, D, H)
+        self.keep = [xq, wq, h1, h3, hq, dYq, dh, dh1, dh3, a1, a3, y, dx, dx2, dWg, dWu, dWd]
+        offs, x, dY = P(self.offs), P(self.x), P(self.dY)
+        q = lambda t4: tuple(P(t) for t in t4)
+
+        def glue(fn):
+            def call(*args):
+                fn()
+                return 0
+            return call
+
+        def swiglu_fwd_torch():
+            torch.mul(torch.nn.functional.silu(h1), h3, out=dh)  # dh holds h in the forward
+
+        def swiglu_bwd_torch():
+            g1, g3 = swiglu_backward_bf16(dh, h1, h3)
+            dh1.copy_(g1)
+            dh3.copy_(g3)
+
+        calls = [("quant_x", L.mxfp8_quantize_2d, (x, M, D, RC, 1, offs, G, *q(xq), st))]
+        for n, (r, c) in (("Wg", (H, D)), ("Wu", (H, D)), ("Wd", (D, H))):
+            calls.append((f"quant_{n}", L.mxfp8_quantize_3d_experts, (P(self.W[n]), G, r, c, RC, 1, *q(wq[n]), st)))
+        if fused:
+            calls.append(("gateup_swiglu", L.mxfp8_grouped_mm_swiglu_fwd,
+                          (*q(xq)[:2], *q(wq["Wg"])[:2], *q(wq["Wu"])[:2], offs, G, M, H, D, P(h1), P(h3),
+                           *q(hq), st)))
+        else:
+            calls += [("fwd_gate", L.mxfp8_grouped_mm_fwd, (*q(xq)[:2], *q(wq["Wg"])[:2], offs, G, M, H, D, P(h1), st)),
+                      ("fwd_up", L.mxfp8_grouped_mm_fwd, (*q(xq)[:2], *q(wq["Wu"])[:2], offs, G, M, H, D, P(h3), st)),
+                      ("torch.swiglu", glue(swiglu_fwd_torch), ()),
+                      ("quant_h", L.mxfp8_quantize_2d, (P(dh), M, H, RC, 1, offs, G, *q(hq), st))]
+        calls += [
+            ("fwd_down", L.mxfp8_grouped_mm_fwd, (*q(hq)[:2], *q(wq["Wd"])[:2], offs, G, M, D, H, P(y), st)),
+            ("quant_dY", L.mxfp8_quantize_2d, (dY, M, D, RC, 1, offs, G, *q(dYq), st)),
+            ("dgrad_down", L.mxfp8_grouped_mm_dgrad, (*q(dYq)[:2], *q(wq["Wd"])[2:], offs, G, M, D, H, P(dh), st)),
+            ("wgrad_down", L.mxfp8_grouped_mm_wgrad, (*q(dYq)[2:], *q(hq)[2:], offs, G, M, D, H, P(dWd), st)),
+            ("torch.swiglu_bwd", glue(swiglu_bwd_torch), ()),
+            ("quant_dh1", L.mxfp8_quantize_2d, (P(dh1), M, H, RC, 1, offs, G, *q(a1), st)),
+            ("quant_dh3", L.mxfp8_quantize_2d, (P(dh3), M, H, RC, 1, offs, G, *q(a3), st)),
+            ("dgrad_gate", L.mxfp8_grouped_mm_dgrad, (*q(a1)[:2], *q(wq["Wg"])[2:], offs, G, M, H, D, P(dx), st)),
+            ("dgrad_up", L.mxfp8_grouped_mm_dgrad, (*q(a3)[:2], *q(wq["Wu"])[2:], offs, G, M, H, D, P(dx2), st)),
+            ("torch.add", glue(lambda: dx.add_(dx2)), ()),
+            ("wgrad_gate", L.mxfp8_grouped_mm_wgrad, (*q(a1)[2:], *q(xq)[2:], offs, G, M, H, D, P(dWg), st)),
+            ("wgrad_up", L.mxfp8_grouped_mm_wgrad, (*q(a3)[2:], *q(xq)[2:], offs, G, M, H, D, P(dWu), st)),
+        ]
+        self.calls = calls
+        self.launches = {n: (0 if n.startswith("torch.") else 1) for n, _, _ in calls}
+        f1 = 2.0 * M * D * H
+        self.gemm_flops = {n: (2 * f1 if n == "gateup_swiglu" else f1) for n, _, _ in calls
+                           if n.startswith(("fwd_", "dgrad_", "wgrad_", "gateup"))}
+        self.flops = 9 * f1
+        qb = lambda e: e * (2 + 1 + 1 + 2 / 32)
+        self.bytes = {"quant_x": qb(M * D), "quant_Wg": qb(G * H * D), "quant_Wu": qb(G * H * D),
+                      "quant_Wd": qb(G * D * H), "quant_dY": qb(M * D), "quant_dh1": qb(M * H), "quant_dh3": qb(M * H)}
+        if not fused:
+            self.bytes["quant_h"] = qb(M * H)
+        self.roofline_key = "gateup_swiglu" if fused else "fwd_gate"
+        self.roofline_name = "grouped_mm_swiglu_fwd (gate+up, fused epilogue)" if fused else "grouped_mm_fwd (gate)"
+
+    def run(self, stream, events=None):
+        for name, fn, args in self.calls:
+            if events is not None:
+                events[name][0].record(stream)
+            rc = fn(*args, ctypes.c_void_p(stream.cuda_stream))
+            if rc != 0:
+                raise RuntimeError(f"{name}: {self.mx._lib.STATUS_NAMES.get(rc, rc)}")
+            if events is not None:
+                events[name][1].record(stream)
+
+    def check_status(self):
+        self.mx.read_status(self.status, "bench SwiGLU step")
+
+
 # ---------------------------------------------------------------- oracle sample (CPU baseline / reference arm)
 def _bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -371,7 +498,12 @@ def run_native(args, rank, world, local):
     pk = peaks()
     parts = workload_parts(args.workload, dev)
     w = parts[0]
-    step = Step(w, dev) if len(parts) == 1 else StepGroup(parts, dev, share_w=args.workload == "scout_mb4")
+    if args.workload in ("swiglu", "swiglu_unfused"):
+        step = SwiGLUStep(w, dev, fused=args.workload == "swiglu")
+    elif len(parts) == 1:
+        step = Step(w, dev)
+    else:
+        step = StepGroup(parts, dev, share_w=args.workload == "scout_mb4")
     single = isinstance(step, Step)
     stream = torch.cuda.current_stream(dev)
 
@@ -486,7 +618,7 @@ def run_native(args, rank, world, local):
         return None
     ms_step = ms / args.steps
     fp8_peak = pk["bf16_sus"] * FP8_OVER_BF16
-    fwd_key = "fwd" if single else "p0.fwd"
+    fwd_key = getattr(step, "roofline_key", "fwd" if single else "p0.fwd")
     fwd_ms = per[fwd_key]
     achieved = step.gemm_flops[fwd_key] / fwd_ms / 1e9
     traffic = FWD_TRAFFIC["bytes"] if (FWD_TRAFFIC["src_sha"] == kernel_src_sha() and args.workload == "scout") else None
@@ -516,10 +648,11 @@ def run_native(args, rank, world, local):
         "config": {"workload": WORKLOAD_TEXT[args.workload], "G": step.G, "M": step.M, "N": step.N, "K": step.K,
                    "group_sizes": list(map(int, w["sizes"])), "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({L2_BYTES // 2**20} MiB): A, W, dOut = "
-                         f"{sum(t.numel() * 2 for t in {id(t): t for p in parts for t in (p['A'], p['W'], p['dOut'])}.values()) // 2**20} "
+                         f"{sum(t.numel() * 2 for t in {id(t): t for t in step_inputs(step, parts)}.values()) // 2**20} "
                          "MiB bf16 per step" if args.workload != "tiny" else "tiny: L2-resident (latency-bound case)",
                    "frac_fp8_peak_step": round(step.flops / ms_step / 1e9 / fp8_peak, 3)},
-        "roofline": {"bound": "tensor", "kernel": "grouped_mm_fwd" + ("" if single else " (gate)"), "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": getattr(step, "roofline_name", "grouped_mm_fwd" + ("" if single else " (gate)")),
+                     "achieved": round(achieved, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 3),
                      "traffic": traffic,
                      "peak_note": f"{pk['src']} sustained bf16 {pk['bf16_sus']} TFLOP/s x {FP8_OVER_BF16} "
