@@ -628,10 +628,10 @@ def run_native(args, rank, world, local):
         if n in step.gemm_flops:
             tf = step.gemm_flops[n] / per[n] / 1e9
             d.update(tflops=round(tf, 1), frac_fp8_peak=round(tf / fp8_peak, 3))
-        else:
+        elif n in step.bytes:
             gbs = step.bytes[n] / per[n] / 1e6
             d.update(gbs=round(gbs, 1), frac_hbm=round(gbs / pk["hbm"], 3))
-        kernels[n] = d
+        kernels[n] = d  # entries named torch.* are torch elementwise glue: time only
     line = {
         "metric": METRIC,
         "value": round(world * step.flops / ms_step / 1e9, 2),
