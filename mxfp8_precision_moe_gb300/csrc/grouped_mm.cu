@@ -37,6 +37,10 @@ namespace mx {
 constexpr int BM = 128;  // tile rows = tensor-memory lanes
 constexpr int BK = 128;  // contraction bytes (= e4m3 elements) per stage: one 128-byte swizzle row
 constexpr int kThreads = 192;
+// SwiGLU variant: 16 epilogue warps (4 per tensor-memory lane quarter, one 32-column block each):
+// its per-element work (silu, two quantizations) needs the extra warps to keep pace with the MMAs.
+constexpr int kSwiEpiWarps = 16;
+constexpr int kThreadsSwi = 64 + 32 * kSwiEpiWarps;
 constexpr int kBand = 16;  // m-tiles per raster band (tiles of a band share B tiles in L2)
 
 enum GemmMode : int { ROWGROUPED = 0, KGROUPED = 1 };
@@ -199,29 +203,6 @@ __device__ __forceinline__ void st_shared_u8(void* p, uint32_t v) {
     asm volatile("st.shared.u8 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
-// The warp's 32 rows of 128 bytes (row = lane; words w[OFF .. OFF+31]) to global memory, every
-// store instruction writing 4 full 128-byte row segments: each lane parks its eight 16-byte
-// pieces in the warp's 32 x 128 B staging buffer (piece j of row r at slot j ^ (r & 7): no bank
-// conflicts), then lanes 8i..8i+7 store one row.  Rows >= vrows and pieces at or past
-// valid_bytes are skipped.
-template <int OFF, int NW>
-__device__ __forceinline__ void store_rows_128B(uint8_t* stg, const uint32_t (&w)[NW], uint8_t* gbase,
-                                                int64_t ld_bytes, int vrows, int valid_bytes, int lane) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) * 16),
-                     make_uint4(w[OFF + 4 * j], w[OFF + 4 * j + 1], w[OFF + 4 * j + 2], w[OFF + 4 * j + 3]));
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int rl = (lane >> 3) + 4 * i, piece = lane & 7;
-        const uint4 val = ld_shared_v4(stg + rl * 128 + ((piece ^ (rl & 7)) * 16));
-        if (rl < vrows && piece * 16 < valid_bytes)
-            *reinterpret_cast<uint4*>(gbase + (int64_t)rl * ld_bytes + piece * 16) = val;
-    }
-    __syncwarp();
-}
-
 // Codes of a non-finite block (scale 0xFF): 0x7F with each element's sign, for a bf16 pair.
 __device__ __forceinline__ uint32_t nonfinite_codes2(uint32_t v) {
     return 0x7F7Fu | ((v >> 8) & 0x80u) | ((v >> 16) & 0x8000u);
@@ -231,7 +212,7 @@ __device__ __forceinline__ uint32_t nonfinite_codes2(uint32_t v) {
 __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float f) { return cvt_e4m3x2(bf16lo(v) * f, bf16hi(v) * f); }
 
 template <int BN, bool kSwi>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
     grouped_mm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_b2, const GemmParams p) {
     using C = Cfg<BN>;
@@ -307,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int a = 0; a < C::kAcc; ++a) {
                 mbar_init(&tfull[a], 1);
-                mbar_init(&tempty[a], 4);
+                mbar_init(&tempty[a], kSwi ? kSwiEpiWarps : 4);
             }
             mbar_init(drain, 1);
             fence_barrier_init();
@@ -430,14 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp >= 2) {
           if constexpr (kSwi) {
             // ------------------------------------------------ SwiGLU epilogue
-            // Per tile: h1 (gate, columns 0-127 of the accumulator) and h3 (up, 128-255) rounded to
-            // bf16 and stored; h = bf16(bf16(silu(h1)) * h3) with silu(x) = x / (1 + e^-x) in fp32
-            // (the bf16 rounding points of an elementwise bf16 SwiGLU); h quantized to MXFP8 along
-            // its row (blocks of 32 columns) and, optionally, along the tokens (the warp's 32 rows
-            // are one 32-token block of every column).
+            // Per tile: h1 (gate, accumulator columns 0-127) and h3 (up, 128-255) rounded to bf16 and
+            // stored; h = bf16(bf16(silu(h1)) * h3) with silu(x) = x / (1 + e^-x) in fp32 (the bf16
+            // rounding points of an elementwise bf16 SwiGLU); h quantized to MXFP8 along its row and,
+            // optionally, along the tokens.  Warp (quarter q, block j) owns rows 32q..32q+31 and the
+            // 32 columns 32j..32j+31: one row block of 32 per thread, one token block of 32 per column.
             const int quarter = warp & 3;
+            const int jb = (warp - 2) >> 2;     // 32-column block of this warp
             const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
-            uint8_t* stg = smem + C::kOffStage + (warp - 2) * (32 * 128);
+            uint8_t* stg = smem + C::kOffStage + (warp - 2) * 1024;
             const int64_t H = p.nb;
             const int64_t ct_T = ptotal / 128;  // column tiles of the token-grouped h^T scales
             uint32_t acc_phase = 0;
@@ -445,101 +427,101 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
                 if (!mbar_wait_bounded(&tfull[0], acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
-                uint32_t hg[64], hu[64];  // bf16 pairs (columns 2i, 2i+1) of h1 and h3
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-#pragma unroll
-                for (int c = 0; c < 128; c += 32) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld_32x32b_x32(taddr + c, v0);
-                    tmem_ld_32x32b_x32(taddr + 128 + c, v1);
+                uint32_t hg[16], hu[16];  // bf16 pairs (columns 2i, 2i+1 of the block) of h1 and h3
+                {
+                    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + 32 * jb;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        hg[c / 2 + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-                        hu[c / 2 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
-                    }
+                    for (int i = 0; i < 16; ++i) hg[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                    tmem_ld_32x32b_x32(taddr + 128, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) hu[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[0]);
                 acc_phase ^= 1u;
 
-                const int vrows = ti.valid_rows - quarter * 32;  // rows of this warp inside the group
                 const int vcols = ti.valid_cols;
-                const int64_t row0 = ti.a_row + quarter * 32;    // first token of this warp
-                uint8_t* g1 = reinterpret_cast<uint8_t*>(p.out + row0 * H + ti.col0);
-                uint8_t* g3 = reinterpret_cast<uint8_t*>(p.out2 + row0 * H + ti.col0);
-                store_rows_128B<0>(stg, hg, g1, H * 2, vrows, vcols * 2, lane);
-                store_rows_128B<32>(stg, hg, g1 + 128, H * 2, vrows, (vcols - 64) * 2, lane);
-                store_rows_128B<0>(stg, hu, g3, H * 2, vrows, vcols * 2, lane);
-                store_rows_128B<32>(stg, hu, g3 + 128, H * 2, vrows, (vcols - 64) * 2, lane);
+                const bool bvalid = 32 * jb < vcols;            // this column block lies inside H
+                const bool rvalid = r < ti.valid_rows;          // this row lies inside the group
+                const int64_t row = ti.a_row + r;
+                const int64_t c0 = ti.col0 + 32 * jb;           // first column of the block
+                if (bvalid && rvalid) {
+                    uint4* g1 = reinterpret_cast<uint4*>(p.out + row * H + c0);
+                    uint4* g3 = reinterpret_cast<uint4*>(p.out2 + row * H + c0);
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
+                    for (int i = 0; i < 4; ++i) {
+                        g1[i] = make_uint4(hg[4 * i], hg[4 * i + 1], hg[4 * i + 2], hg[4 * i + 3]);
+                        g3[i] = make_uint4(hu[4 * i], hu[4 * i + 1], hu[4 * i + 2], hu[4 * i + 3]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
                     const float a = bf16lo(hg[i]), b = bf16hi(hg[i]);
                     const uint32_t sl = pack_bf16x2(a / (1.0f + expf(-a)), b / (1.0f + expf(-b)));
                     hg[i] = pack_bf16x2(bf16lo(sl) * bf16lo(hu[i]), bf16hi(sl) * bf16hi(hu[i]));
                 }
-                // row-wise: 4 blocks of 32 columns -> 128 codes and one 32-bit word of scale bytes
-                uint32_t codes[32];
-                uint32_t sword = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                // row-wise: this thread's 32 elements are one block -> 32 codes and one scale byte
+                {
                     uint32_t m = 0;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) m = vmax_u16x2(m, hg[16 * j + i] & 0x7FFF7FFFu);
+                    for (int i = 0; i < 16; ++i) m = vmax_u16x2(m, hg[i] & 0x7FFF7FFFu);
                     const uint32_t sc = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
                     const float f = inv_scale_from_e8m0(sc);
+                    uint32_t codes[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t w0 = hg[16 * j + 2 * i], w1 = hg[16 * j + 2 * i + 1];
-                        codes[8 * j + i] = sc == 0xFFu ? nonfinite_codes2(w0) | (nonfinite_codes2(w1) << 16)
-                                                       : quant_pair(w0, f) | (quant_pair(w1, f) << 16);
+                    for (int i = 0; i < 8; ++i)
+                        codes[i] = sc == 0xFFu ? nonfinite_codes2(hg[2 * i]) | (nonfinite_codes2(hg[2 * i + 1]) << 16)
+                                               : quant_pair(hg[2 * i], f) | (quant_pair(hg[2 * i + 1], f) << 16);
+                    if (bvalid && rvalid) {
+                        uint4* gq = reinterpret_cast<uint4*>(p.hq + row * H + c0);
+                        gq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+                        gq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
                     }
-                    if (r < ti.valid_rows && 32 * j < vcols) sword |= sc << (8 * j);
+                    // the tile's row scales are one 512-byte blocked tile: row r -> (r%32)*16 + (r/32)*4,
+                    // block jb -> byte jb; rows past the group and blocks past H are padding (0)
+                    p.hs[((ti.prow0 >> 7) * p.hs_ct + (ti.col0 >> 7)) * 512 + lane * 16 + quarter * 4 + jb] =
+                        (uint8_t)((bvalid && rvalid) ? sc : 0u);
                 }
-                store_rows_128B<0>(stg, codes, p.hq + row0 * H + ti.col0, H, vrows, vcols, lane);
-                // the tile's row scales are exactly one 512-byte blocked tile (rows past the group: 0)
-                *reinterpret_cast<uint32_t*>(p.hs + ((ti.prow0 >> 7) * p.hs_ct + (ti.col0 >> 7)) * 512 + lane * 16 +
-                                             quarter * 4) = sword;
                 if (p.hTq != nullptr) {
-                    // group sizes are multiples of 32 here (device-checked), so a warp's block is
+                    // group sizes are multiples of 32 here (device-checked), so the warp's 32 rows are
                     // either all inside the group or all padding
                     const int64_t cq = ti.prow0 / 32 + quarter;  // scale column of this 32-token block
+                    uint32_t my_s = 0;                          // scale of column c0 + lane
+                    if (ti.valid_rows > quarter * 32 && bvalid) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t my_s = 0;  // scale of column 32j + lane
-                        if (vrows > 0 && 32 * j < vcols) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const uint32_t w = hg[16 * j + i];
-                                const uint32_t slo = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, w & 0x7FFFu));
-                                const uint32_t shi =
-                                    e8m0_from_absbits(__reduce_max_sync(0xffffffffu, (w >> 16) & 0x7FFFu));
-                                uint32_t c2 = cvt_e4m3x2(bf16lo(w) * inv_scale_from_e8m0(slo),
-                                                         bf16hi(w) * inv_scale_from_e8m0(shi));
-                                if (slo == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu | ((w >> 8) & 0x80u);
-                                if (shi == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u | ((w >> 16) & 0x8000u);
-                                // transpose through shared memory: byte (column c, token lane) at c*32 + lane
-                                st_shared_u8(stg + (2 * i) * 32 + lane, c2 & 0xFFu);
-                                st_shared_u8(stg + (2 * i + 1) * 32 + lane, c2 >> 8);
-                                my_s = lane == 2 * i ? slo : (lane == 2 * i + 1 ? shi : my_s);
-                            }
-                            __syncwarp();
-#pragma unroll
-                            for (int h2 = 0; h2 < 2; ++h2) {
-                                const int cc = 16 * h2 + (lane >> 1);  // column within the chunk
-                                const uint4 val = ld_shared_v4(stg + cc * 32 + (lane & 1) * 16);
-                                if (32 * j + cc < vcols)
-                                    *reinterpret_cast<uint4*>(p.hTq + (ti.col0 + 32 * j + cc) * p.M + row0 +
-                                                              (lane & 1) * 16) = val;
-                            }
-                            __syncwarp();
-                            if (32 * j + lane >= vcols) my_s = 0;
+                        for (int i = 0; i < 16; ++i) {
+                            const uint32_t w = hg[i];
+                            const uint32_t slo = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, w & 0x7FFFu));
+                            const uint32_t shi = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, (w >> 16) & 0x7FFFu));
+                            uint32_t c2 = cvt_e4m3x2(bf16lo(w) * inv_scale_from_e8m0(slo),
+                                                     bf16hi(w) * inv_scale_from_e8m0(shi));
+                            if (slo == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu | ((w >> 8) & 0x80u);
+                            if (shi == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u | ((w >> 16) & 0x8000u);
+                            // transpose through shared memory: byte (column c, token lane) at c*32 + lane
+                            st_shared_u8(stg + (2 * i) * 32 + lane, c2 & 0xFFu);
+                            st_shared_u8(stg + (2 * i + 1) * 32 + lane, c2 >> 8);
+                            my_s = lane == 2 * i ? slo : (lane == 2 * i + 1 ? shi : my_s);
                         }
-                        const int64_t cH = ti.col0 + 32 * j + lane;  // row of h^T (columns past H: padding 0)
-                        p.hTs[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] =
-                            (uint8_t)my_s;
+                        __syncwarp();
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int cc = 16 * h2 + (lane >> 1);  // column within the block
+                            const uint4 val = ld_shared_v4(stg + cc * 32 + (lane & 1) * 16);
+                            if (32 * jb + cc < vcols)
+                                *reinterpret_cast<uint4*>(p.hTq + (c0 + cc) * p.M + ti.a_row + quarter * 32 +
+                                                          (lane & 1) * 16) = val;
+                        }
+                        __syncwarp();
+                        if (32 * jb + lane >= vcols) my_s = 0;
                     }
+                    const int64_t cH = c0 + lane;  // row of h^T (columns past H: padding 0)
+                    p.hTs[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] =
+                        (uint8_t)my_s;
                 }
             }
           } else {
@@ -1005,7 +987,7 @@ static mxfp8_status_t launch_gemm(const void* a, int64_t a_rows, int64_t a_cols,
     if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_kernel<BN, kSwi>), C::kSmem, attr_set))
         return MXFP8_ERR_LAUNCH;
     const int grid = (int)max64(1, min64(tiles_bound, host::num_sms()));
-    grouped_mm_kernel<BN, kSwi><<<grid, kThreads, C::kSmem, st>>>(ma, mb, mb2, p);
+    grouped_mm_kernel<BN, kSwi><<<grid, kSwi ? kThreadsSwi : kThreads, C::kSmem, st>>>(ma, mb, mb2, p);
     return host::last_launch_status();
 }
 
