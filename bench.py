@@ -60,6 +60,8 @@ WORKLOAD_TEXT = {
     "swiglu_standin": "SwiGLU routed expert GEMMs: G=2, M=65600 (39360/26240), gate/up W[2,8192,5120], "
                       "down W[2,5120,8192]; 9 grouped GEMMs, seeded stand-ins for the SwiGLU intermediates",
     "tiny": "Tiny: G=2, A[256,256], offs [128,256], W[2,128,256] (latency-bound; parity case)",
+    "scout_w32": WORKLOAD + "; expert weights quantized with one scale per 32x32 block (one quantization for "
+                            "the forward and the dgrad)",
     "scout_mb4": "Llama4-Scout-like routed experts, one optimizer step of 4 microbatches (G=8, K=5120, N=8192, "
                  "M=16384 tokens each, Zipf(1.1) group sizes in 32-token chunks, seeds 0-3): W quantized once "
                  "(prequantized-weight cache), then fwd+bwd per microbatch",
@@ -72,6 +74,8 @@ def workload_parts(name: str, dev) -> list:
 
     if name in ("scout", "imbalanced", "tiny"):
         return [synth.workload(name, seed=0, device=dev)]
+    if name == "scout_w32":
+        return [synth.workload("scout", seed=0, device=dev)]
     if name in ("swiglu", "swiglu_unfused"):
         return [synth.workload("swiglu", seed=0, device=dev)]
     if name == "scout_mb4":
@@ -115,7 +119,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--no-baseline", action="store_true", help="skip the cuBLAS bf16 comparison leg")
-    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "swiglu_unfused", "swiglu_standin", "tiny", "scout_mb4",
+    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "swiglu_unfused", "swiglu_standin", "tiny", "scout_mb4", "scout_w32",
                              "sweep"],
                     help="scout (default, the reported line); the others are extra measurements")
     return ap.parse_args()
@@ -219,7 +223,7 @@ class ClockSampler:
 class Step:
     """Device buffers of one replica and the C-ABI calls of one pass of the path."""
 
-    def __init__(self, w: dict, device, shared_w: "Step | None" = None):
+    def __init__(self, w: dict, device, shared_w: "Step | None" = None, w_block32: bool = False):
         import mxfp8_precision_moe_gb300 as mx
 
         L = mx.load()
@@ -251,7 +255,8 @@ class Step:
         self.calls = [
             ("quant_A", L.mxfp8_quantize_2d, (P(self.A), M, K, RC, 1, P(self.offs), G, P(self.aq), P(self.as_),
                                               P(self.aTq), P(self.aTs), st)),
-            ("quant_W", L.mxfp8_quantize_3d_experts, (P(self.W), G, N, K, RC, 1, P(self.wq), P(self.ws),
+            ("quant_W", L.mxfp8_quantize_3d_experts, (P(self.W), G, N, K, RC | (4 if w_block32 else 0), 1,
+                                                      P(self.wq), P(self.ws),
                                                       P(self.wTq), P(self.wTs), st)),
             ("fwd", L.mxfp8_grouped_mm_fwd, (P(self.aq), P(self.as_), P(self.wq), P(self.ws), P(self.offs), G, M,
                                              N, K, P(self.out), st)),
@@ -501,7 +506,7 @@ def run_native(args, rank, world, local):
     if args.workload in ("swiglu", "swiglu_unfused"):
         step = SwiGLUStep(w, dev, fused=args.workload == "swiglu")
     elif len(parts) == 1:
-        step = Step(w, dev)
+        step = Step(w, dev, w_block32=args.workload == "scout_w32")
     else:
         step = StepGroup(parts, dev, share_w=args.workload == "scout_mb4")
     single = isinstance(step, Step)
@@ -746,8 +751,8 @@ def run_sweep(args) -> dict:
     qT, sT = torch.empty((G, K, N), dtype=torch.uint8, device=dev), torch.empty((G, ce(K, N)), dtype=torch.uint8, device=dev)
     E = G * N * K
     for label, dirs, out in (("3d plain", 1, (q, s3, None, None)), ("3d transposed", 2, (None, None, qT, sT)),
-                             ("3d both", 3, (q, s3, qT, sT))):
-        nb = E * (2 + 2 + 2 / 32) if dirs == 3 else E * (2 + 1 + 1 / 32)
+                             ("3d both", 3, (q, s3, qT, sT)), ("3d 32x32 both", 7, (q, s3, qT, sT))):
+        nb = E * (2 + 2 + 2 / 32) if dirs & 3 == 3 else E * (2 + 1 + 1 / 32)
         time_call(L.mxfp8_quantize_3d_experts, (sp(w), G, N, K, dirs, 1, *[sp(t) for t in out], None), nb, label,
                   [G, N, K])
     best = max(r["frac_hbm"] for r in rows)

@@ -138,6 +138,13 @@ mxfp8_status_t mxfp8_quantize_2d(const void* x_bf16, int64_t M, int64_t K, unsig
  *   dirs & MXFP8_COL ("transposed", along N, for dgrad):
  *        qT [G, K, N] (N contiguous), sT per expert [K, N/32] compact or blocked.
  *   Both bits: one read of w.  N % 32 == 0, K % 32 == 0.
+ *   dirs | MXFP8_BLOCK32X32 (with ROW and/or COL): [32, 32] square blocks
+ *        ([P3] "Low-precision Flash Attention", item 3: one scale per 32x32
+ *        block makes the quantization transpose invariant, so one quantization
+ *        serves the forward and the dgrad).  One scale per 32x32 block of each
+ *        expert; qT holds exactly the codes of q, transposed.  s and sT repeat the
+ *        block's scale on each of its 32 rows (columns), in the compact or blocked
+ *        layout above, so the grouped GEMMs take them unchanged.
  *   Per-expert scale strides: compact N*K/32 (s) and K*N/32 (sT); blocked
  *   ceil(N/128)*128*ceil(K/128)*4 (s) and ceil(K/128)*128*ceil(N/128)*4 (sT).
  * ------------------------------------------------------------------------- */

@@ -221,13 +221,13 @@ class _ToMxfp8ThenScaledGroupedMM(torch.autograd.Function):
     GEMMs.  Quantization is treated as the identity for gradients."""
 
     @staticmethod
-    def forward(ctx, A, W, offs, w_mxfp8):
+    def forward(ctx, A, W, offs, w_mxfp8, w_block32x32):
         need_dA = ctx.needs_input_grad[0]
         need_dW = ctx.needs_input_grad[1]
         a_dirs = ROW | (COL if need_dW else 0)
         aq, as_, aTq, aTs = mxfp8_quantize_2d(A.contiguous(), a_dirs, SCALES_BLOCKED, offs)
         if w_mxfp8 is None:
-            w_dirs = ROW | (COL if need_dA else 0)
+            w_dirs = ROW | (COL if need_dA else 0) | (BLOCK32X32 if w_block32x32 else 0)
             wq, ws, wTq, wTs = mxfp8_quantize_3d_experts(W.contiguous(), w_dirs, SCALES_BLOCKED)
         else:
             wq, ws, wTq, wTs = _check_quad(w_mxfp8, W, need_dA)
@@ -242,11 +242,11 @@ class _ToMxfp8ThenScaledGroupedMM(torch.autograd.Function):
         need_dA, need_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
         dirs = (ROW if need_dA else 0) | (COL if need_dW else 0)
         if dirs == 0:
-            return None, None, None, None
+            return None, None, None, None, None
         dq, ds, dTq, dTs = mxfp8_quantize_2d(dOut.contiguous().to(torch.bfloat16), dirs, SCALES_BLOCKED, offs)
         dA = mxfp8_grouped_mm_dgrad(dq, ds, wTq, wTs, offs) if need_dA else None
         dW = mxfp8_grouped_mm_wgrad(dTq, dTs, aTq, aTs, offs) if need_dW else None
-        return dA, dW, None, None
+        return dA, dW, None, None, None
 
 
 def _blocked_bytes(rows: int, cols: int) -> int:
@@ -270,14 +270,17 @@ def _check_quad(quad, W: torch.Tensor, need_t: bool):
     return wq, ws, wTq, wTs
 
 
-def quantize_expert_weights(W: torch.Tensor):
+def quantize_expert_weights(W: torch.Tensor, block32x32: bool = False):
     """One fused launch: W[G, N, K] -> (weight_fp8 [G, N, K], weight_scale, weight_t_fp8 [G, K, N],
-    weight_t_scale), scales in the blocked layout, one flat buffer per expert."""
-    return mxfp8_quantize_3d_experts(W.detach().contiguous(), ROW | COL, SCALES_BLOCKED)
+    weight_t_scale), scales in the blocked layout, one flat buffer per expert.  With block32x32,
+    one scale per 32x32 block: weight_t_fp8 is exactly weight_fp8 transposed (one quantization
+    serves the forward and the dgrad)."""
+    dirs = ROW | COL | (BLOCK32X32 if block32x32 else 0)
+    return mxfp8_quantize_3d_experts(W.detach().contiguous(), dirs, SCALES_BLOCKED)
 
 
 def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, *, w_mxfp8=None,
-                                    weight_cache=None) -> torch.Tensor:
+                                    weight_cache=None, weight_block32x32: bool = False) -> torch.Tensor:
     """Differentiable MXFP8 grouped GEMM: out[m] = A[m] @ W[g]^T for rows m of
     group g (offs = int32 cumulative end rows).  A [M, K] bf16, W [G, N, K] bf16,
     out [M, N] bf16.  Group sizes must be multiples of 32 when gradients of W
@@ -287,7 +290,9 @@ def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torc
     ``w_mxfp8`` = (weight_fp8, weight_scale, weight_t_fp8, weight_t_scale) as
     returned by ``quantize_expert_weights(W)``, or ``weight_cache`` = an
     ``Mxfp8WeightCache`` that keeps that quadruple across microbatches until W
-    changes or the optimizer steps.  Gradients still flow to W."""
+    changes or the optimizer steps.  Gradients still flow to W.  weight_block32x32:
+    quantize W on the fly with one scale per 32x32 block, so the forward and the
+    dgrad use the same quantization of W (transposed for the dgrad)."""
     if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise ValueError("to_mxfp8_then_scaled_grouped_mm expects bf16 A and W")
     if offs.dtype != torch.int32:
@@ -296,7 +301,10 @@ def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torc
         raise ValueError("pass w_mxfp8 or weight_cache, not both")
     if weight_cache is not None:
         w_mxfp8 = weight_cache.get(W)
-    return _ToMxfp8ThenScaledGroupedMM.apply(A, W, offs, w_mxfp8)
+    if weight_block32x32 and w_mxfp8 is not None:
+        raise ValueError("weight_block32x32 applies to on-the-fly quantization; prequantize with "
+                         "quantize_expert_weights(W, block32x32=True) instead")
+    return _ToMxfp8ThenScaledGroupedMM.apply(A, W, offs, w_mxfp8, weight_block32x32)
 
 
 from .weight_cache import Mxfp8WeightCache  # noqa: E402  (uses quantize_expert_weights above)

@@ -153,6 +153,11 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
     constexpr bool kRow = (DIRS & MXFP8_ROW) != 0;
     constexpr bool kCol = (DIRS & MXFP8_COL) != 0;
     constexpr bool kB32 = (DIRS & MXFP8_BLOCK32X32) != 0;
+    // 32x32 blocks alone: row-major codes + compact [R/32][C/32] scales.  32x32 blocks with ROW and/or
+    // COL: the plain and/or transposed codes of the same 32x32 quantization, the block scale written
+    // for every row (column) of the block in the row (column) layouts.
+    constexpr bool kB32Only = DIRS == MXFP8_BLOCK32X32;
+    constexpr bool kRowOut = kRow || kB32Only;
     extern __shared__ uint8_t qsmem_raw[];
     __shared__ int32_t ends_s[kMaxGroups];
     __shared__ int32_t pstart_s[kMaxGroups];
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
     //   row layout:    (batch, group, 32-row chunk) of the group's padding rows, every column tile;
     //   column layout: (batch, group, 128-row slice) of the group's padding block-columns, and
     //                  (batch) the padding rows C .. ceil(C/128)*128, every column tile.
-    if (p.blocked && !kB32) {
+    if (p.blocked && (kRow || kCol)) {
         const int G_eff = grouped ? p.G : 1;
         const int64_t rslices = (C + 127) / 128;
         const int64_t units_row = kRow ? (int64_t)p.batch * G_eff * 4 : 0;
@@ -303,7 +308,22 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
 #pragma unroll
             for (int k = 0; k < 4; ++k) mg[rr][k] = v[rr][k] & 0x7FFF7FFFu;
 
-        if constexpr (kRow || kB32) {
+        uint32_t sblk = 0;  // the 32x32 block's scale
+        if constexpr (kB32) {
+            // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1), 4 down (li)
+            uint32_t m = 0;
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) m = vmax_u16x2(m, mg[rr][k]);
+            m = shfl_xor_max16x2(m, 1);
+            m = shfl_xor_max16x2(m, 2);
+            m = shfl_xor_max16x2(m, 8);
+            m = shfl_xor_max16x2(m, 16);
+            sblk = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
+        }
+
+        if constexpr (kRowOut) {
             // two rows per word: pp[k] = (amax of row 2k, amax of row 2k+1) over this lane's 8 columns
             uint32_t pp[4];
 #pragma unroll
@@ -315,15 +335,8 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
             }
             uint32_t s8[8];
             if constexpr (kB32) {
-                // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1), 4 down (li)
-                uint32_t m = vmax_u16x2(vmax_u16x2(pp[0], pp[1]), vmax_u16x2(pp[2], pp[3]));
-                m = shfl_xor_max16x2(m, 1);
-                m = shfl_xor_max16x2(m, 2);
-                m = shfl_xor_max16x2(m, 8);
-                m = shfl_xor_max16x2(m, 16);
-                const uint32_t s = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) s8[rr] = s;
+                for (int rr = 0; rr < 8; ++rr) s8[rr] = sblk;
             } else {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -354,7 +367,7 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
                 uint8_t* sb = p.s_row + b * p.s_row_bstride;
                 const int64_t cb = c8 / kBlk;
                 const int q4 = lj & 3;
-                if constexpr (kB32) {
+                if constexpr (kB32Only) {
                     if (li == 0 && q4 == 0) sb[(row0 / kBlk) * Cb + cb] = (uint8_t)s8[0];
                 } else {
                     // this lane's two rows 2*q4, 2*q4+1 (register selects, no local-memory indexing)
@@ -388,20 +401,25 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
         }
 
         if constexpr (kCol) {
-            // column amax over 32 rows: 8 here (packed pairs of columns), then lanes li = 0..3
-            uint32_t cm[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mg[0][k], mg[1][k]), vmax_u16x2(mg[2][k], mg[3][k])),
-                                        vmax_u16x2(vmax_u16x2(mg[4][k], mg[5][k]), vmax_u16x2(mg[6][k], mg[7][k])));
-                m = shfl_xor_max16x2(m, 8);
-                cm[k] = shfl_xor_max16x2(m, 16);
-            }
             uint32_t sc[8];
+            if constexpr (kB32) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                sc[2 * k] = e8m0_from_absbits(cm[k] & 0xFFFFu);
-                sc[2 * k + 1] = e8m0_from_absbits(cm[k] >> 16);
+                for (int cc = 0; cc < 8; ++cc) sc[cc] = sblk;
+            } else {
+                // column amax over 32 rows: 8 here (packed pairs of columns), then lanes li = 0..3
+                uint32_t cm[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mg[0][k], mg[1][k]), vmax_u16x2(mg[2][k], mg[3][k])),
+                                            vmax_u16x2(vmax_u16x2(mg[4][k], mg[5][k]), vmax_u16x2(mg[6][k], mg[7][k])));
+                    m = shfl_xor_max16x2(m, 8);
+                    cm[k] = shfl_xor_max16x2(m, 16);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    sc[2 * k] = e8m0_from_absbits(cm[k] & 0xFFFFu);
+                    sc[2 * k + 1] = e8m0_from_absbits(cm[k] >> 16);
+                }
             }
             bool nonfinite = false;
 #pragma unroll
@@ -505,6 +523,10 @@ static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t
         case MXFP8_COL: return launch_dirs<MXFP8_COL>(m, p, grid, st);
         case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL>(m, p, grid, st);
         case MXFP8_BLOCK32X32: return launch_dirs<MXFP8_BLOCK32X32>(m, p, grid, st);
+        case MXFP8_BLOCK32X32 | MXFP8_ROW: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW>(m, p, grid, st);
+        case MXFP8_BLOCK32X32 | MXFP8_COL: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_COL>(m, p, grid, st);
+        case MXFP8_BLOCK32X32 | MXFP8_ROW | MXFP8_COL:
+            return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW | MXFP8_COL>(m, p, grid, st);
         default: return MXFP8_ERR_LAYOUT;
     }
 }
@@ -556,7 +578,7 @@ extern "C" mxfp8_status_t mxfp8_quantize_3d_experts(const void* w_bf16, int32_t 
     if (N % 32 || K % 32) return MXFP8_ERR_ALIGN;
     if (scale_layout != MXFP8_SCALES_COMPACT && scale_layout != MXFP8_SCALES_BLOCKED) return MXFP8_ERR_LAYOUT;
     const bool row = dirs & MXFP8_ROW, col = dirs & MXFP8_COL;
-    if (dirs == 0 || (dirs & ~3u)) return MXFP8_ERR_LAYOUT;
+    if ((dirs & ~7u) || !(row || col)) return MXFP8_ERR_LAYOUT;  // BLOCK32X32 only together with ROW and/or COL
     if (!w_bf16) return MXFP8_ERR_NULL;
     if (row && (!q || !s)) return MXFP8_ERR_NULL;
     if (col && (!qT || !sT)) return MXFP8_ERR_NULL;

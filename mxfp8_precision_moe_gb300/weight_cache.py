@@ -34,12 +34,14 @@ class Mxfp8WeightCache:
     optimizer steps.
 
     ``quantize(W) -> quad`` defaults to one fused plain + transposed quantization of
-    ``W[G, N, K]`` into blocked scales (``quantize_expert_weights``).  ``hits`` and
-    ``misses`` count lookups."""
+    ``W[G, N, K]`` into blocked scales (``quantize_expert_weights``; with ``block32x32``,
+    one scale per 32x32 block).  ``hits`` and ``misses`` count lookups."""
 
-    def __init__(self, quantize: Optional[Callable[[torch.Tensor], Quad]] = None):
+    def __init__(self, quantize: Optional[Callable[[torch.Tensor], Quad]] = None, block32x32: bool = False):
         if quantize is None:
-            from . import quantize_expert_weights as quantize
+            from . import quantize_expert_weights
+
+            quantize = lambda W: quantize_expert_weights(W, block32x32=block32x32)  # noqa: E731
         self._quantize = quantize
         self._entries: dict[int, tuple] = {}  # id(W) -> (weakref(W), stamp, quad)
         self.hits = 0
