@@ -72,6 +72,15 @@ def lib():
         L.oracle_bf16_from_f64.restype = ctypes.c_uint16
         L.oracle_bf16_from_f64_array.argtypes = [P, I64, P]
         L.oracle_swiglu_bf16.argtypes = [P, P, I64, P]
+        L.oracle_philox4x32_10.argtypes = [P, P, P]
+        L.oracle_sr_word.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
+        L.oracle_sr_word.restype = ctypes.c_uint32
+        L.oracle_e4m3_encode_sr.argtypes = [ctypes.c_double, ctypes.c_uint32]
+        L.oracle_e4m3_encode_sr.restype = ctypes.c_uint8
+        L.oracle_rht_signs.argtypes = [ctypes.c_uint64, P]
+        L.oracle_rht32.argtypes = [P, P, P]
+        L.oracle_quantize_rows_opts.argtypes = [P, I64, I64, ctypes.c_uint, ctypes.c_uint64, P, P]
+        L.oracle_quantize_cols_opts.argtypes = [P, I64, I64, ctypes.c_uint, ctypes.c_uint64, P, P]
         _lib = L
     return _lib
 
@@ -288,3 +297,60 @@ def swiglu_gate_up(x_u16, wg_u16, wu_u16, ends) -> dict:
     if h.shape[0] % 32 == 0:
         out["hT_q"], out["hT_s"] = quantize_cols(h)
     return out
+
+
+# ---------------------------------------------------------------- stability variants
+OPT_SR, OPT_RHT = 1, 2
+
+
+def philox4x32_10(ctr, key) -> list:
+    c = np.ascontiguousarray(ctr, np.uint32)
+    k = np.ascontiguousarray(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    lib().oracle_philox4x32_10(_p(c), _p(k), _p(out))
+    return [int(v) for v in out]
+
+
+def sr_word(seed: int, n: int, direction: int) -> int:
+    return int(lib().oracle_sr_word(seed, n, direction))
+
+
+def e4m3_encode_sr(y: float, r: int) -> int:
+    return int(lib().oracle_e4m3_encode_sr(float(y), int(r)))
+
+
+def rht_signs(seed: int) -> np.ndarray:
+    d = np.zeros(32, np.int8)
+    lib().oracle_rht_signs(seed, _p(d))
+    return d
+
+
+def rht32(x, d) -> np.ndarray:
+    """c * H * (D x) of one block of 32 fp32 values, in fp32 (butterfly order h = 1..16)."""
+    x = np.ascontiguousarray(x, np.float32)
+    d = np.ascontiguousarray(d, np.int8)
+    assert x.size == 32 and d.size == 32
+    y = np.zeros(32, np.float32)
+    lib().oracle_rht32(_p(x), _p(d), _p(y))
+    return y
+
+
+def quantize_rows_opts(x_u16, opts: int, seed: int):
+    """Row-wise quantization with options (OPT_SR: stochastic rounding; OPT_RHT: Hadamard transform
+    of every block of 32 first): q [R, C], compact s [R, C/32]."""
+    x = _u16(x_u16)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    s_ = np.empty((R, C // 32), np.uint8)
+    lib().oracle_quantize_rows_opts(_p(x), R, C, opts, seed, _p(q), _p(s_))
+    return q, s_
+
+
+def quantize_cols_opts(x_u16, opts: int, seed: int):
+    """Column-wise quantization with options, transposed: qT [C, R], compact sT [C, R/32]."""
+    x = _u16(x_u16)
+    R, C = x.shape
+    qT = np.empty((C, R), np.uint8)
+    sT = np.empty((C, R // 32), np.uint8)
+    lib().oracle_quantize_cols_opts(_p(x), R, C, opts, seed, _p(qT), _p(sT))
+    return qT, sT

@@ -38,6 +38,10 @@
  * NaN/Inf input blocks: parity unpinned (one hand-made block only).
  * SwiGLU stage: bf16 rounding pinned against torch's fp32->bf16 cast, hand
  * ties and a double-rounding case; silu against torch's fp64 silu.
+ * Stability variants: Philox4x32-10 against its published known-answer
+ * vectors; stochastic rounding by hand cases, exactness on the grid and its
+ * mean; the Hadamard butterflies against scipy's Hadamard matrix on inputs
+ * where fp32 is exact, and orthogonality.
  */
 #include <math.h>
 #include <stdint.h>
@@ -124,9 +128,19 @@ uint8_t oracle_e8m0_from_amax(double amax) {
 /* Block quantization                                                  */
 /* ------------------------------------------------------------------ */
 
+static uint8_t quantize_block_f64_rw(const double* v, int64_t n, uint8_t* q, int64_t qstride, const uint32_t* rw);
+
 /* Quantize n values (already widened to fp64) sharing one scale.
  * Writes n codes to q (stride qstride) and returns the scale byte. */
 static uint8_t quantize_block_f64(const double* v, int64_t n, uint8_t* q, int64_t qstride) {
+    return quantize_block_f64_rw(v, n, q, qstride, NULL);
+}
+
+uint8_t oracle_e4m3_encode_sr(double y, uint32_t r);
+
+/* As above; with rw != NULL each element is rounded stochastically with its
+ * random word rw[i] (oracle_e4m3_encode_sr) instead of to nearest even. */
+static uint8_t quantize_block_f64_rw(const double* v, int64_t n, uint8_t* q, int64_t qstride, const uint32_t* rw) {
     double amax = 0.0;
     int nonfinite = 0;
     for (int64_t i = 0; i < n; ++i) {
@@ -141,7 +155,8 @@ static uint8_t quantize_block_f64(const double* v, int64_t n, uint8_t* q, int64_
     }
     uint8_t s = oracle_e8m0_from_amax(amax);
     int e = (int)s - 127;
-    for (int64_t i = 0; i < n; ++i) q[i * qstride] = oracle_e4m3_encode(ldexp(v[i], -e));
+    for (int64_t i = 0; i < n; ++i)
+        q[i * qstride] = rw ? oracle_e4m3_encode_sr(ldexp(v[i], -e), rw[i]) : oracle_e4m3_encode(ldexp(v[i], -e));
     return s;
 }
 
@@ -306,6 +321,137 @@ void oracle_grouped_mm_wgrad(const uint8_t* dq, const uint8_t* ds, const uint8_t
                 out[(g * N + n) * K + k] =
                     oracle_dot(dq + n * M + lo, ds + n * Mb + lo / BLK, aq + k * M + lo, as + k * Mb + lo / BLK, hi - lo);
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* Stability variants: stochastic rounding, random Hadamard transform  */
+/* ------------------------------------------------------------------ */
+/* "MXFP8 (Micro-scaling FP8)", "Numerical stability": random Hadamard
+ * transforms spread outliers before quantization, and stochastic rounding
+ * removes the bias of deterministic rounding.  The pages define neither; the
+ * readings below are written identically (but independently) on the GPU. */
+
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011): ten rounds of two 32x32->64-bit products with
+ * the multipliers 0xD2511F53 and 0xCD9E8D57, the key bumped by 0x9E3779B9 and
+ * 0xBB67AE85 between rounds.  Pinned by the published known-answer vectors. */
+void oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0, p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0, n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1, n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The random word of element n (row-major index r*C + c of the input) for the
+ * copy `dir` (0 = row-wise, 1 = column-wise): word n % 4 of Philox4x32-10 with
+ * counter (n / 4 low 32 bits, n / 4 high bits, dir, 0) and key (seed low 32
+ * bits, seed high 32 bits). */
+uint32_t oracle_sr_word(uint64_t seed, uint64_t n, uint32_t dir) {
+    uint32_t ctr[4] = {(uint32_t)(n >> 2), (uint32_t)(n >> 34), dir, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    oracle_philox4x32_10(ctr, key, o);
+    return o[n & 3];
+}
+
+/* Stochastic rounding of y to E4M3 (satfinite).  For |y| between the
+ * consecutive finite magnitudes lo <= |y| < hi, let F = floor((|y| - lo) /
+ * (hi - lo) * 2^20), the position inside the step in units of 2^-20 (the 20
+ * fp32 mantissa bits E4M3 drops).  The magnitude rounds up to hi iff
+ * F + (r >> 12) >= 2^20, so with r uniform it rounds up with probability
+ * F / 2^20.  |y| >= 448 gives 448; the sign is applied afterwards; NaN -> 0x7F. */
+uint8_t oracle_e4m3_encode_sr(double y, uint32_t r) {
+    int neg = signbit(y) ? 1 : 0;
+    if (isnan(y)) return (uint8_t)(0x7F | (neg << 7));
+    double a = fabs(y);
+    int code;
+    if (a >= E4M3_MAX) {
+        code = 0x7E;
+    } else {
+        int lo = 0;
+        for (int c = 0; c <= 0x7E; ++c)
+            if (oracle_e4m3_to_f64((uint8_t)c) <= a) lo = c;
+        double vlo = oracle_e4m3_to_f64((uint8_t)lo), vhi = oracle_e4m3_to_f64((uint8_t)(lo + 1));
+        double F = floor((a - vlo) / (vhi - vlo) * 1048576.0);
+        code = (F + (double)(r >> 12) >= 1048576.0) ? lo + 1 : lo;
+    }
+    return (uint8_t)(code | (neg << 7));
+}
+
+/* The 32 signs D of the Hadamard transform: bit i of word 0 of Philox4x32-10
+ * with counter (0, 0, 2, 0) and the seed as key; a set bit means -1. */
+void oracle_rht_signs(uint64_t seed, int8_t* d) {
+    uint32_t ctr[4] = {0u, 0u, 2u, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    oracle_philox4x32_10(ctr, key, o);
+    for (int i = 0; i < BLK; ++i) d[i] = ((o[0] >> i) & 1u) ? -1 : 1;
+}
+
+/* y = c * H * (D x) for one block of 32, in fp32: the signs flip, then the
+ * Sylvester-ordered Hadamard matrix (H[i][j] = (-1)^popcount(i & j)) is applied
+ * as butterflies (a, b) -> (a + b, a - b) over the pairs (i, i + h) for
+ * h = 1, 2, 4, 8, 16 in that order, each sum rounded to fp32; finally every
+ * element is multiplied by c = fp32(1/sqrt(32)).  H D / sqrt(32) is orthogonal,
+ * so two operands transformed alike along a GEMM's K keep their product. */
+void oracle_rht32(const float* x, const int8_t* d, float* y) {
+    float t[BLK];
+    for (int i = 0; i < BLK; ++i) t[i] = d[i] < 0 ? -x[i] : x[i];
+    for (int h = 1; h < BLK; h <<= 1)
+        for (int i = 0; i < BLK; ++i)
+            if ((i & h) == 0) {
+                float a = t[i], b = t[i + h];
+                t[i] = a + b;
+                t[i + h] = a - b;
+            }
+    const float c = (float)(1.0 / sqrt(32.0));
+    for (int i = 0; i < BLK; ++i) y[i] = t[i] * c;
+}
+
+/* One block of 32 bf16 values (element i at x[i * xstride], input index
+ * n0 + i * nstride) quantized with options: bit 0 = stochastic rounding
+ * (copy `dir`), bit 1 = Hadamard transform first. */
+static uint8_t quantize_block_opts(const uint16_t* x, int64_t xstride, uint64_t n0, uint64_t nstride, unsigned opts,
+                                   uint64_t seed, uint32_t dir, uint8_t* q, int64_t qstride) {
+    double v[BLK];
+    uint32_t rw[BLK];
+    if (opts & 2u) {
+        float xf[BLK], yf[BLK];
+        int8_t d[BLK];
+        oracle_rht_signs(seed, d);
+        for (int i = 0; i < BLK; ++i) xf[i] = (float)oracle_bf16_to_f64(x[i * xstride]);
+        oracle_rht32(xf, d, yf);
+        for (int i = 0; i < BLK; ++i) v[i] = (double)yf[i];
+    } else {
+        for (int i = 0; i < BLK; ++i) v[i] = oracle_bf16_to_f64(x[i * xstride]);
+    }
+    if (opts & 1u)
+        for (int i = 0; i < BLK; ++i) rw[i] = oracle_sr_word(seed, n0 + (uint64_t)i * nstride, dir);
+    return quantize_block_f64_rw(v, BLK, q, qstride, (opts & 1u) ? rw : NULL);
+}
+
+/* Row-wise quantization of x[R, C] with options (see quantize_block_opts). */
+void oracle_quantize_rows_opts(const uint16_t* x, int64_t R, int64_t C, unsigned opts, uint64_t seed, uint8_t* q,
+                               uint8_t* s) {
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t b = 0; b < C / BLK; ++b)
+            s[r * (C / BLK) + b] = quantize_block_opts(x + r * C + b * BLK, 1, (uint64_t)(r * C + b * BLK), 1, opts,
+                                                       seed, 0u, q + r * C + b * BLK, 1);
+}
+
+/* Column-wise quantization of x[R, C] with options, stored transposed. */
+void oracle_quantize_cols_opts(const uint16_t* x, int64_t R, int64_t C, unsigned opts, uint64_t seed, uint8_t* qT,
+                               uint8_t* sT) {
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t b = 0; b < R / BLK; ++b)
+            sT[c * (R / BLK) + b] = quantize_block_opts(x + b * BLK * C + c, C, (uint64_t)(b * BLK * C + c), (uint64_t)C,
+                                                        opts, seed, 1u, qT + c * R + b * BLK, 1);
 }
 
 /* ------------------------------------------------------------------ */

@@ -1,0 +1,139 @@
+"""Pins of the oracle's stability variants ("MXFP8 (Micro-scaling FP8)", "Numerical
+stability": random Hadamard transforms and stochastic rounding), no GPU:
+- Philox4x32-10 against the published known-answer vectors (tests/golden);
+- stochastic rounding against hand-worked cases, against an independent fp32 bit-pattern
+  algorithm (add the top 20 random bits to the 20 mantissa bits E4M3 drops, truncate) on the
+  normal E4M3 range, and for unbiasedness;
+- the Hadamard transform against scipy's Hadamard matrix on inputs where fp32 is exact, its
+  norm preservation, and the transpose relation between the row and column quantizations."""
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+
+
+def kat_rows():
+    for line in open(GOLDEN):
+        if line.strip() and not line.startswith("#"):
+            yield [int(w, 16) for w in line.split()]
+
+
+@pytest.mark.parametrize("row", list(kat_rows()))
+def test_philox_known_answers(row):
+    assert oracle.philox4x32_10(row[0:4], row[4:6]) == row[6:10]
+
+
+def test_sr_word_is_word_n_mod_4_of_counter_n_div_4():
+    seed = 0x0123456789ABCDEF
+    for n in (0, 1, 2, 3, 4, 7, 12345, 2 ** 34 + 5):
+        for d in (0, 1):
+            w = oracle.philox4x32_10([(n >> 2) & 0xFFFFFFFF, (n >> 34) & 0xFFFFFFFF, d, 0],
+                                     [seed & 0xFFFFFFFF, seed >> 32])
+            assert oracle.sr_word(seed, n, d) == w[n & 3]
+
+
+E = oracle.e4m3_table()
+
+
+@pytest.mark.parametrize("y,r,code", [
+    (1.0625, 0x80000000, 0x39),      # midway 1.0 / 1.125: F = 2^19, r>>12 = 2^19 -> up
+    (1.0625, 0x7FFFFFFF, 0x38),      # r>>12 = 2^19 - 1 -> down
+    (-1.0625, 0x80000000, 0xB9),     # the sign is applied afterwards
+    (1.5 * 2 ** -9, 0x80000000, 0x02),   # subnormal step, midway -> up
+    (1.5 * 2 ** -9, 0x7FFFFFFF, 0x01),
+    (447.0, 2 ** 27, 0x7E),          # 447 = 416 + 31/32 step: up iff r>>12 >= 2^15
+    (447.0, 2 ** 27 - 1, 0x7D),
+    (460.0, 0, 0x7E),                # beyond the largest finite magnitude: 448
+    (1e9, 0xFFFFFFFF, 0x7E),
+    (0.0, 0xFFFFFFFF, 0x00),
+    (-0.0, 0xFFFFFFFF, 0x80),
+])
+def test_sr_hand_cases(y, r, code):
+    assert oracle.e4m3_encode_sr(y, r) == code
+
+
+def test_sr_keeps_representable_values():
+    for c in range(0x7F):
+        for r in (0, 0x12345678, 0xFFFFFFFF):
+            assert oracle.e4m3_encode_sr(E[c], r) == c
+
+
+def test_sr_matches_fp32_bit_algorithm_on_normal_range():
+    rng = np.random.default_rng(1)
+    y = np.float32(2.0) ** rng.uniform(-6, np.log2(448), 4000).astype(np.float32)
+    y = y * rng.choice([-1, 1], y.size).astype(np.float32)
+    r = rng.integers(0, 2 ** 32, y.size, dtype=np.uint64).astype(np.uint32)
+    bits = np.abs(y).view(np.uint32).astype(np.uint64)
+    t = ((bits + (r.astype(np.uint64) >> 12)) & ~np.uint64(0xFFFFF)).astype(np.uint32)
+    want = np.minimum(t.view(np.float32).astype(np.float64), 448.0) * np.sign(y)
+    got = np.array([E[oracle.e4m3_encode_sr(float(a), int(b)) & 0x7F] * (-1 if oracle.e4m3_encode_sr(float(a), int(b)) & 0x80 else 1)
+                    for a, b in zip(y, r)])
+    assert np.array_equal(got, want)
+
+
+def test_sr_is_unbiased():
+    rng = np.random.default_rng(2)
+    for y in (1.0 + 5 / 64, 3.3, 0.013, 300.0, 2.5 * 2 ** -9):
+        r = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64)
+        vals = np.array([E[oracle.e4m3_encode_sr(y, int(w))] for w in r])
+        step = vals.max() - vals.min()
+        assert set(np.unique(vals)) <= {vals.min(), vals.max()} and step > 0
+        # mean within 5 standard errors of y (Bernoulli between two grid points)
+        p = (y - vals.min()) / step
+        se = step * np.sqrt(p * (1 - p) / r.size)
+        assert abs(vals.mean() - y) <= 5 * se + 1e-12
+
+
+def test_rht_signs():
+    d0, d1 = oracle.rht_signs(0), oracle.rht_signs(1)
+    assert set(np.unique(d0)) <= {-1, 1} and d0.size == 32
+    assert not np.array_equal(d0, d1)
+    assert np.array_equal(d0, oracle.rht_signs(0))
+
+
+def test_rht_matches_hadamard_matrix_exactly_on_integers():
+    rng = np.random.default_rng(3)
+    H = scipy.linalg.hadamard(32).astype(np.int64)
+    c = np.float32(1.0 / np.sqrt(32.0))
+    for seed in (0, 7, 2 ** 40 + 3):
+        d = oracle.rht_signs(seed)
+        x = rng.integers(-1000, 1000, 32).astype(np.float32)
+        exact = H @ (d.astype(np.int64) * x.astype(np.int64))     # integers, exact in fp32
+        want = exact.astype(np.float32) * c
+        assert np.array_equal(oracle.rht32(x, d), want)
+
+
+def test_rht_preserves_the_norm():
+    rng = np.random.default_rng(4)
+    d = oracle.rht_signs(11)
+    for _ in range(20):
+        x = (rng.standard_normal(32) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        y = oracle.rht32(x, d)
+        assert abs(np.linalg.norm(y.astype(np.float64)) / np.linalg.norm(x.astype(np.float64)) - 1) < 1e-5
+
+
+def bf16(a):
+    import torch
+    from tests._util import u16
+    return u16(torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16))
+
+
+def test_options_reduce_and_transpose():
+    rng = np.random.default_rng(5)
+    x = bf16(rng.standard_normal((64, 96)) * 3)
+    q, s = oracle.quantize_rows(x)
+    assert all(np.array_equal(a, b) for a, b in zip(oracle.quantize_rows_opts(x, 0, 9), (q, s)))
+    # the Hadamard transform alone is deterministic, so the column quantization of x is the
+    # row quantization of x^T
+    qT, sT = oracle.quantize_cols_opts(x, oracle.OPT_RHT, 9)
+    qr, sr = oracle.quantize_rows_opts(np.ascontiguousarray(x.T), oracle.OPT_RHT, 9)
+    assert np.array_equal(qT, qr) and np.array_equal(sT, sr)
+    # stochastic rounding moves no code by more than one step and keeps the scales
+    q2, s2 = oracle.quantize_rows_opts(x, oracle.OPT_SR, 9)
+    assert np.array_equal(s2, s)
+    assert np.all(np.abs(E[q2 & 0x7F] - E[q & 0x7F]) <= np.maximum(E[q & 0x7F] / 8, 2.0 ** -9) + 1e-12)
