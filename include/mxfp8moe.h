@@ -102,6 +102,13 @@ enum {
 
 enum { MXFP8_SCALES_COMPACT = 0, MXFP8_SCALES_BLOCKED = 1 };
 
+/* Options of mxfp8_quantize_2d_opts (bit mask). */
+enum {
+    MXFP8_OPT_STOCHASTIC = 1,     /* stochastic rounding of every code (both copies) */
+    MXFP8_OPT_HADAMARD_ROW = 2,   /* random Hadamard transform of each 32-block of the row-wise copy */
+    MXFP8_OPT_HADAMARD_COL = 4    /* random Hadamard transform of each 32-block of the column-wise copy */
+};
+
 /* Largest number of groups / experts a call accepts. */
 #define MXFP8_MAX_GROUPS 1024
 
@@ -127,6 +134,39 @@ enum { MXFP8_SCALES_COMPACT = 0, MXFP8_SCALES_BLOCKED = 1 };
 mxfp8_status_t mxfp8_quantize_2d(const void* x_bf16, int64_t M, int64_t K, unsigned dirs, int scale_layout,
                                  const int32_t* offs, int32_t G, void* q_row, void* s_row, void* q_col,
                                  void* s_col, int32_t* dev_status, mxfp8_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * mxfp8_quantize_2d_opts -- mxfp8_quantize_2d with the stability variants of
+ * [P3] "Numerical stability" (random Hadamard transforms spread outliers before
+ * quantization; stochastic rounding removes the bias of deterministic rounding).
+ * The pages define neither; this library's readings:
+ *   random words: element (r, c) of x (index n = r*K + c) of the row-wise copy
+ *     (dir 0) or the column-wise copy (dir 1) takes word n % 4 of Philox4x32-10
+ *     (Salmon et al., SC 2011) with counter (n / 4 mod 2^32, n / 2^34, dir, 0)
+ *     and key (seed mod 2^32, seed / 2^32).
+ *   MXFP8_OPT_STOCHASTIC: the scale rule is unchanged; each scaled element y is
+ *     rounded between the neighbouring finite E4M3 magnitudes lo <= |y| < hi:
+ *     up iff F + (word >> 12) >= 2^20, F = floor((|y| - lo) / (hi - lo) * 2^20);
+ *     |y| >= 448 gives 448.  So y rounds up with probability F / 2^20.
+ *   MXFP8_OPT_HADAMARD_ROW / _COL: every 32-block along the copy's axis becomes
+ *     y = c * H * (D x) in fp32 before quantization: D = diag(signs), sign i
+ *     negative iff bit i of word 0 of Philox4x32-10(counter (0, 0, 2, 0), key as
+ *     above) is set; H the Sylvester-ordered 32x32 Hadamard matrix applied as
+ *     butterflies (a, b) -> (a + b, a - b) over the pairs (i, i + h) for
+ *     h = 1, 2, 4, 8, 16 in that order, each rounded to fp32; c = fp32(1/sqrt(32)).
+ *     H D / sqrt(32) is orthogonal: two operands transformed with the same seed
+ *     along a GEMM's contraction keep their product (e.g. dOut and A along the
+ *     tokens for the wgrad).  Scales then come from the fp32 amax by the same
+ *     rule; a block with a non-finite value gets codes 0x7F of unspecified sign.
+ *   dirs: MXFP8_ROW, MXFP8_COL or both (no BLOCK32X32); each HADAMARD bit needs
+ *     its copy.  opts = 0 is exactly mxfp8_quantize_2d.  Other arguments,
+ *     layouts and errors as for mxfp8_quantize_2d; unknown option bits:
+ *     MXFP8_ERR_LAYOUT.
+ * ------------------------------------------------------------------------- */
+mxfp8_status_t mxfp8_quantize_2d_opts(const void* x_bf16, int64_t M, int64_t K, unsigned dirs, int scale_layout,
+                                      const int32_t* offs, int32_t G, unsigned opts, uint64_t seed, void* q_row,
+                                      void* s_row, void* q_col, void* s_col, int32_t* dev_status,
+                                      mxfp8_stream_t stream);
 
 /* ----------------------------------------------------------------------------
  * mxfp8_quantize_3d_experts -- quantize expert weights w[G, N, K] (bf16).

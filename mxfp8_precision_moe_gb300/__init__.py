@@ -20,10 +20,12 @@ import ctypes
 
 import torch
 
-from ._lib import (BLOCK32X32, COL, MAX_GROUPS, ROW, SCALES_BLOCKED, SCALES_COMPACT, Mxfp8Error, check, load)
+from ._lib import (BLOCK32X32, COL, MAX_GROUPS, OPT_HADAMARD_COL, OPT_HADAMARD_ROW, OPT_STOCHASTIC, ROW,
+                   SCALES_BLOCKED, SCALES_COMPACT, Mxfp8Error, check, load)
 
 __all__ = [
     "ROW", "COL", "BLOCK32X32", "SCALES_COMPACT", "SCALES_BLOCKED", "MAX_GROUPS", "Mxfp8Error",
+    "OPT_STOCHASTIC", "OPT_HADAMARD_ROW", "OPT_HADAMARD_COL",
     "mxfp8_quantize_2d", "mxfp8_quantize_3d_experts", "mxfp8_grouped_mm_fwd", "mxfp8_grouped_mm_dgrad",
     "mxfp8_grouped_mm_wgrad", "mxfp8_scale_bytes", "mxfp8_scale_bytes_colgroups", "mxfp8_check_offsets",
     "mxfp8_debug_wait_timeout", "new_status", "read_status", "to_mxfp8_then_scaled_grouped_mm", "load",
@@ -73,11 +75,14 @@ def mxfp8_scale_bytes_colgroups(R: int, M: int, G: int) -> int:
 
 # ---------------------------------------------------------------- quantization
 def mxfp8_quantize_2d(x: torch.Tensor, dirs: int = ROW, scale_layout: int = SCALES_BLOCKED,
-                      offs: torch.Tensor | None = None, dev_status: torch.Tensor | None = None):
+                      offs: torch.Tensor | None = None, dev_status: torch.Tensor | None = None, opts: int = 0,
+                      seed: int = 0):
     """Quantize x[M, K] (bf16).  Returns (q_row, s_row, q_col, s_col), None for
     directions not requested.  q_row [M, K]; q_col [K, M].  Compact scales are
     2D ([M, K/32], [K, M/32], or [M/32, K/32] for 32x32 blocks); blocked scales
-    are flat byte buffers (upper-bound size, zero padded)."""
+    are flat byte buffers (upper-bound size, zero padded).  opts (OPT_STOCHASTIC,
+    OPT_HADAMARD_ROW, OPT_HADAMARD_COL) and seed select the stability variants
+    of mxfp8_quantize_2d_opts."""
     if x.dtype != torch.bfloat16 or x.dim() != 2:
         raise ValueError("mxfp8_quantize_2d: x must be a 2D bf16 tensor")
     _cuda(x, offs, dev_status)
@@ -101,6 +106,12 @@ def mxfp8_quantize_2d(x: torch.Tensor, dirs: int = ROW, scale_layout: int = SCAL
             s_col = _u8((mxfp8_scale_bytes_colgroups(K, M, G),), dev)
     if offs is not None and offs.dtype != torch.int32:
         raise ValueError("offs must be int32")
+    if opts:
+        st = load().mxfp8_quantize_2d_opts(_p(x), M, K, dirs, scale_layout, _p(offs), G if offs is not None else 0,
+                                           opts, seed & (2 ** 64 - 1), _p(q_row), _p(s_row), _p(q_col), _p(s_col),
+                                           _p(dev_status), _stream(dev))
+        check(st, "mxfp8_quantize_2d_opts")
+        return q_row, s_row, q_col, s_col
     st = load().mxfp8_quantize_2d(_p(x), M, K, dirs, scale_layout, _p(offs), G if offs is not None else 0,
                                   _p(q_row), _p(s_row), _p(q_col), _p(s_col), _p(dev_status), _stream(dev))
     check(st, "mxfp8_quantize_2d")
@@ -221,11 +232,13 @@ class _ToMxfp8ThenScaledGroupedMM(torch.autograd.Function):
     GEMMs.  Quantization is treated as the identity for gradients."""
 
     @staticmethod
-    def forward(ctx, A, W, offs, w_mxfp8, w_block32x32):
+    def forward(ctx, A, W, offs, w_mxfp8, w_block32x32, stability):
         need_dA = ctx.needs_input_grad[0]
         need_dW = ctx.needs_input_grad[1]
+        sr, rht, seed = stability
         a_dirs = ROW | (COL if need_dW else 0)
-        aq, as_, aTq, aTs = mxfp8_quantize_2d(A.contiguous(), a_dirs, SCALES_BLOCKED, offs)
+        a_opts = OPT_HADAMARD_COL if (rht and need_dW) else 0
+        aq, as_, aTq, aTs = mxfp8_quantize_2d(A.contiguous(), a_dirs, SCALES_BLOCKED, offs, opts=a_opts, seed=seed)
         if w_mxfp8 is None:
             w_dirs = ROW | (COL if need_dA else 0) | (BLOCK32X32 if w_block32x32 else 0)
             wq, ws, wTq, wTs = mxfp8_quantize_3d_experts(W.contiguous(), w_dirs, SCALES_BLOCKED)
@@ -234,6 +247,7 @@ class _ToMxfp8ThenScaledGroupedMM(torch.autograd.Function):
         out = mxfp8_grouped_mm_fwd(aq, as_, wq, ws, offs)
         ctx.save_for_backward(aTq, aTs, wTq, wTs, offs)
         ctx.shape = (A.shape[0], W.shape[0], W.shape[1], W.shape[2])
+        ctx.stability = stability
         return out
 
     @staticmethod
@@ -242,11 +256,14 @@ class _ToMxfp8ThenScaledGroupedMM(torch.autograd.Function):
         need_dA, need_dW = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
         dirs = (ROW if need_dA else 0) | (COL if need_dW else 0)
         if dirs == 0:
-            return None, None, None, None, None
-        dq, ds, dTq, dTs = mxfp8_quantize_2d(dOut.contiguous().to(torch.bfloat16), dirs, SCALES_BLOCKED, offs)
+            return None, None, None, None, None, None
+        sr, rht, seed = ctx.stability
+        d_opts = (OPT_STOCHASTIC if sr else 0) | (OPT_HADAMARD_COL if (rht and need_dW) else 0)
+        dq, ds, dTq, dTs = mxfp8_quantize_2d(dOut.contiguous().to(torch.bfloat16), dirs, SCALES_BLOCKED, offs,
+                                             opts=d_opts, seed=seed)
         dA = mxfp8_grouped_mm_dgrad(dq, ds, wTq, wTs, offs) if need_dA else None
         dW = mxfp8_grouped_mm_wgrad(dTq, dTs, aTq, aTs, offs) if need_dW else None
-        return dA, dW, None, None, None
+        return dA, dW, None, None, None, None
 
 
 def _blocked_bytes(rows: int, cols: int) -> int:
@@ -280,7 +297,9 @@ def quantize_expert_weights(W: torch.Tensor, block32x32: bool = False):
 
 
 def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, *, w_mxfp8=None,
-                                    weight_cache=None, weight_block32x32: bool = False) -> torch.Tensor:
+                                    weight_cache=None, weight_block32x32: bool = False,
+                                    stochastic_rounding: bool = False, hadamard_wgrad: bool = False,
+                                    seed: int | None = None) -> torch.Tensor:
     """Differentiable MXFP8 grouped GEMM: out[m] = A[m] @ W[g]^T for rows m of
     group g (offs = int32 cumulative end rows).  A [M, K] bf16, W [G, N, K] bf16,
     out [M, N] bf16.  Group sizes must be multiples of 32 when gradients of W
@@ -292,7 +311,14 @@ def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torc
     ``Mxfp8WeightCache`` that keeps that quadruple across microbatches until W
     changes or the optimizer steps.  Gradients still flow to W.  weight_block32x32:
     quantize W on the fly with one scale per 32x32 block, so the forward and the
-    dgrad use the same quantization of W (transposed for the dgrad)."""
+    dgrad use the same quantization of W (transposed for the dgrad).
+
+    Stability variants ("MXFP8 (Micro-scaling FP8)", "Numerical stability"):
+    stochastic_rounding rounds the output gradient's codes stochastically (both of
+    its copies); hadamard_wgrad applies the same random Hadamard transform along the
+    tokens to both wgrad operands (A's and the output gradient's column-wise copies),
+    which leaves their product unchanged.  seed keys both (Philox4x32-10); None draws
+    one from torch's default CPU generator per forward call."""
     if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise ValueError("to_mxfp8_then_scaled_grouped_mm expects bf16 A and W")
     if offs.dtype != torch.int32:
@@ -304,7 +330,10 @@ def to_mxfp8_then_scaled_grouped_mm(A: torch.Tensor, W: torch.Tensor, offs: torc
     if weight_block32x32 and w_mxfp8 is not None:
         raise ValueError("weight_block32x32 applies to on-the-fly quantization; prequantize with "
                          "quantize_expert_weights(W, block32x32=True) instead")
-    return _ToMxfp8ThenScaledGroupedMM.apply(A, W, offs, w_mxfp8, weight_block32x32)
+    if (stochastic_rounding or hadamard_wgrad) and seed is None:
+        seed = int(torch.randint(0, 2 ** 62, (1,)).item())
+    stability = (bool(stochastic_rounding), bool(hadamard_wgrad), int(seed or 0))
+    return _ToMxfp8ThenScaledGroupedMM.apply(A, W, offs, w_mxfp8, weight_block32x32, stability)
 
 
 from .weight_cache import Mxfp8WeightCache  # noqa: E402  (uses quantize_expert_weights above)

@@ -18,6 +18,7 @@ STATUS_NAMES = {
     9: "MXFP8_ERR_DRIVER",
 }
 ROW, COL, BLOCK32X32 = 1, 2, 4
+OPT_STOCHASTIC, OPT_HADAMARD_ROW, OPT_HADAMARD_COL = 1, 2, 4
 SCALES_COMPACT, SCALES_BLOCKED = 0, 1
 MAX_GROUPS = 1024
 
@@ -44,6 +45,8 @@ def load():
     S = ctypes.c_int
     L.mxfp8_quantize_2d.argtypes = [P, I64, I64, U32, INT, P, I32, P, P, P, P, P, P]
     L.mxfp8_quantize_2d.restype = S
+    L.mxfp8_quantize_2d_opts.argtypes = [P, I64, I64, U32, INT, P, I32, U32, ctypes.c_uint64, P, P, P, P, P, P]
+    L.mxfp8_quantize_2d_opts.restype = S
     L.mxfp8_quantize_3d_experts.argtypes = [P, I32, I64, I64, U32, INT, P, P, P, P, P, P]
     L.mxfp8_quantize_3d_experts.restype = S
     for name in ("mxfp8_grouped_mm_fwd", "mxfp8_grouped_mm_dgrad", "mxfp8_grouped_mm_wgrad"):

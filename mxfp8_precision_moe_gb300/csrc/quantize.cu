@@ -45,6 +45,8 @@ struct QParams {
     int32_t G;
     int32_t* dev_status;
     int64_t tiles_r, tiles_c, ntiles;
+    unsigned opts;       // MXFP8_OPT_* (the stability-variant kernels only)
+    uint64_t seed;
 };
 
 // Warp 0 builds, for G groups over R rows, the clamped monotone end rows and
@@ -102,6 +104,59 @@ __device__ __forceinline__ int find_group(const int32_t* ends_s, int G, int64_t 
     return lo;
 }
 
+// ---- stability variants ("MXFP8 (Micro-scaling FP8)", "Numerical stability": random Hadamard
+// transforms before quantization, stochastic rounding)
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// The random words of the 4 elements n0..n0+3 (n0 % 4 == 0; element index r * C + c of the input)
+// for copy `dir` (0 row-wise, 1 column-wise): counter (n0 / 4, n0 / 2^34, dir, 0), key = seed.
+__device__ __forceinline__ uint4 sr_words4(uint64_t n0, uint32_t dir, uint64_t seed) {
+    return philox4x32_10(make_uint4((uint32_t)(n0 >> 2), (uint32_t)(n0 >> 34), dir, 0u), (uint32_t)seed,
+                         (uint32_t)(seed >> 32));
+}
+
+// E4M3 code of z rounded stochastically with the random word r.  Between consecutive finite
+// magnitudes lo <= |z| < hi the magnitude rounds up iff F + (r >> 12) >= 2^20, with F the part
+// of |z| above lo in units of 2^-20 of the step (truncated); |z| >= 448 gives 448.  On the normal
+// E4M3 range that is an integer add into the 20 fp32 mantissa bits E4M3 drops; below 2^-6 the step
+// is 2^-9.  The sign is applied last.
+__device__ __forceinline__ uint32_t e4m3_sr(float z, uint32_t r) {
+    const uint32_t bits = __float_as_uint(z), a = bits & 0x7FFFFFFFu;
+    float m;
+    if (a >= 0x43E00000u) {                 // 448 and beyond
+        m = 448.0f;
+    } else if (a >= 0x3C800000u) {          // 2^-6 <= |z| < 448
+        m = __uint_as_float((a + (r >> 12)) & ~0xFFFFFu);
+    } else {
+        const float n = __uint_as_float(a) * 512.0f;  // units of the subnormal step 2^-9 (exact)
+        const float lo = floorf(n);
+        const uint32_t F = (uint32_t)((n - lo) * 1048576.0f);
+        m = (lo + ((F + (r >> 12)) >= 0x100000u ? 1.0f : 0.0f)) * 0.001953125f;
+    }
+    return (cvt_e4m3x2(m, 0.0f) & 0xFFu) | ((bits >> 24) & 0x80u);  // m lies on the E4M3 grid: exact
+}
+
+// E8M0 scale byte from the magnitude bits of an fp32 amax (same rule as for bf16: max(E - 8, 0)).
+__device__ __forceinline__ uint32_t e8m0_from_f32bits(uint32_t a) {
+    const uint32_t E = a >> 23;
+    if (E == 0xFFu) return 0xFFu;
+    return E > 8u ? E - 8u : 0u;
+}
+
+constexpr float kRhtScale = 0x1.6a09e6p-3f;  // fp32(1 / sqrt(32))
+
 __device__ __forceinline__ uint32_t shfl_xor_max16x2(uint32_t v, int m) {
     return vmax_u16x2(v, __shfl_xor_sync(0xffffffffu, v, m));
 }
@@ -148,8 +203,11 @@ constexpr int kQTileBytes = 128 * 128 * 2;     // one 128 x 128 bf16 tile
 constexpr int kQThreads = 288;                 // 8 consumer warps + 1 TMA producer warp
 constexpr int kQSmem = kQStages * kQTileBytes + 128;
 
-template <unsigned DIRS>
-__global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
+// kExt: the stability variants of ROW / COL / ROW|COL (runtime options p.opts, seed p.seed); fp32
+// working values, one CTA per SM.
+template <unsigned DIRS, bool kExt = false>
+__global__ void __launch_bounds__(kQThreads, kExt ? 1 : 2)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
     constexpr bool kRow = (DIRS & MXFP8_ROW) != 0;
     constexpr bool kCol = (DIRS & MXFP8_COL) != 0;
     constexpr bool kB32 = (DIRS & MXFP8_BLOCK32X32) != 0;
@@ -301,176 +359,365 @@ __global__ void __launch_bounds__(kQThreads, 2) quant_tile_kernel(const __grid_c
             wg1 = find_group(ends_s, p.G, min64(row0 + 31, R - 1));
         }
 
-        // magnitude bits of every element (bf16 pairs), shared by both directions
-        uint32_t mg[8][4];
+        // Row-wise scales s8[rr] of this lane's 8 rows: the 4 lanes of a 32-column block each write
+        // two of the rows (2*q4, 2*q4 + 1).  Called with cval true.
+        auto store_row_scales = [&](const uint32_t (&s8)[8]) {
+            uint8_t* sb = p.s_row + b * p.s_row_bstride;
+            const int64_t cb = c8 / kBlk;
+            const int q4 = lj & 3;
+            // this lane's two rows (register selects, no local-memory indexing)
+            const uint32_t my_s[2] = {q4 == 0 ? s8[0] : q4 == 1 ? s8[2] : q4 == 2 ? s8[4] : s8[6],
+                                      q4 == 0 ? s8[1] : q4 == 1 ? s8[3] : q4 == 2 ? s8[5] : s8[7]};
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr)
+            for (int h = 0; h < 2; ++h) {
+                const int rr = 2 * q4 + h;
+                const int64_t row = row0 + 8 * li + rr;
+                if (row >= R) continue;
+                const uint8_t sv = (uint8_t)my_s[h];
+                if (!p.blocked) {
+                    sb[row * Cb + cb] = sv;
+                    continue;
+                }
+                int64_t pr = row;
+                if (grouped) {
+                    int g = wg0;
+                    if (wg0 != wg1) g = find_group(ends_s, p.G, row);
+                    if (g >= p.G) continue;
+                    pr = pstart_s[g] + (row - (g ? ends_s[g - 1] : 0));
+                }
+                const int64_t off = blocked_off(pr, cb, ct_row);
+                sb[off] = sv;
+                // last block-column of a row whose K/32 is not a multiple of 4: zero the rest of the word
+                if (cb == Cb - 1)
+                    for (int64_t z = (Cb & 3); z != 0 && z < 4; ++z) sb[off + z - (Cb & 3) + 1] = 0;
+            }
+        };
+        // Column-wise scales sc[cc] of this lane's 8 columns: each of the 4 lanes li writes two of
+        // them.  Called with cval true.
+        auto store_col_scales = [&](const uint32_t (&sc)[8]) {
+            uint8_t* sb = p.s_col + b * p.s_col_bstride;
+            const int64_t rb = row0 / kBlk;
+            int64_t pc = rb;
+            bool ok = true;
+            if (p.blocked && grouped) {
+                ok = wg0 < p.G;
+                if (ok) pc = pstart_s[wg0] / kBlk + (row0 - (wg0 ? ends_s[wg0 - 1] : 0)) / kBlk;
+            }
+            const uint32_t my_s[2] = {li == 0 ? sc[0] : li == 1 ? sc[2] : li == 2 ? sc[4] : sc[6],
+                                      li == 0 ? sc[1] : li == 1 ? sc[3] : li == 2 ? sc[5] : sc[7]};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mg[rr][k] = v[rr][k] & 0x7FFF7FFFu;
+            for (int h = 0; h < 2; ++h) {
+                const int64_t c = c8 + 2 * li + h;
+                if (!p.blocked) sb[c * (R / kBlk) + rb] = (uint8_t)my_s[h];
+                else if (ok) sb[blocked_off(c, pc, ct_col)] = (uint8_t)my_s[h];
+            }
+        };
 
-        uint32_t sblk = 0;  // the 32x32 block's scale
-        if constexpr (kB32) {
-            // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1), 4 down (li)
-            uint32_t m = 0;
+        if constexpr (kExt) {
+            // Stability variants: fp32 values; optionally a Hadamard transform of every block of 32
+            // along the copy's axis, y = c * H * (D x) (signs D, butterflies h = 1, 2, 4 inside the
+            // lane, h = 8, 16 across lanes, in that order); codes by round-to-nearest-even or by
+            // stochastic rounding with per-element Philox words.
+            const bool sr = p.opts & MXFP8_OPT_STOCHASTIC;
+            const uint32_t dsign = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)p.seed,
+                                                 (uint32_t)(p.seed >> 32)).x;
+            auto code2 = [&](float z0, float z1, uint32_t r0, uint32_t r1) -> uint32_t {
+                return sr ? e4m3_sr(z0, r0) | (e4m3_sr(z1, r1) << 8) : cvt_e4m3x2(z0, z1);
+            };
+            if constexpr (kRow) {
+                float y[8][8];
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) { y[rr][2 * k] = bf16lo(v[rr][k]); y[rr][2 * k + 1] = bf16hi(v[rr][k]); }
+                if (p.opts & MXFP8_OPT_HADAMARD_ROW) {
+                    // block position of (rr, c): 8 * (lj & 3) + c
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            if ((dsign >> (8 * (lj & 3) + c)) & 1u) y[rr][c] = -y[rr][c];
+#pragma unroll
+                    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                if ((c & h) == 0) {
+                                    const float a = y[rr][c], bb = y[rr][c + h];
+                                    y[rr][c] = a + bb;
+                                    y[rr][c + h] = a - bb;
+                                }
+#pragma unroll
+                    for (int m = 1; m <= 2; m <<= 1) {
+                        const bool upper = lane & m;
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const float o = __shfl_xor_sync(0xffffffffu, y[rr][c], m);
+                                y[rr][c] = upper ? o - y[rr][c] : y[rr][c] + o;
+                            }
+                    }
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) y[rr][c] *= kRhtScale;
+                }
+                uint32_t s8[8];
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) m = max(m, __float_as_uint(y[rr][c]) & 0x7FFFFFFFu);
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    s8[rr] = e8m0_from_f32bits(m);
+                }
+                uint8_t* qb = p.q_row + b * R * C;
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int64_t row = row0 + 8 * li + rr;
+                    const float f = inv_scale_from_e8m0(s8[rr]);
+                    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                    if (sr && row < R) {
+                        w0 = sr_words4((uint64_t)(row * C + c8), 0u, p.seed);
+                        w1 = sr_words4((uint64_t)(row * C + c8 + 4), 0u, p.seed);
+                    }
+                    uint2 q;
+                    q.x = code2(y[rr][0] * f, y[rr][1] * f, w0.x, w0.y) | (code2(y[rr][2] * f, y[rr][3] * f, w0.z, w0.w) << 16);
+                    q.y = code2(y[rr][4] * f, y[rr][5] * f, w1.x, w1.y) | (code2(y[rr][6] * f, y[rr][7] * f, w1.z, w1.w) << 16);
+                    if (s8[rr] == 0xFFu) {
+                        uint32_t sg[2] = {0u, 0u};
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) sg[c >> 2] |= ((__float_as_uint(y[rr][c]) >> 24) & 0x80u) << (8 * (c & 3));
+                        q.x = 0x7F7F7F7Fu | sg[0];
+                        q.y = 0x7F7F7F7Fu | sg[1];
+                    }
+                    if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
+                }
+                if (cval) store_row_scales(s8);
+            }
+            if constexpr (kCol) {
+                float y[8][8];
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) { y[rr][2 * k] = bf16lo(v[rr][k]); y[rr][2 * k + 1] = bf16hi(v[rr][k]); }
+                if (p.opts & MXFP8_OPT_HADAMARD_COL) {
+                    // block position of (rr, c): 8 * li + rr
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            if ((dsign >> (8 * li + rr)) & 1u) y[rr][c] = -y[rr][c];
+#pragma unroll
+                    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr)
+                            if ((rr & h) == 0)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    const float a = y[rr][c], bb = y[rr + h][c];
+                                    y[rr][c] = a + bb;
+                                    y[rr + h][c] = a - bb;
+                                }
+#pragma unroll
+                    for (int m = 8; m <= 16; m <<= 1) {
+                        const bool upper = lane & m;
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const float o = __shfl_xor_sync(0xffffffffu, y[rr][c], m);
+                                y[rr][c] = upper ? o - y[rr][c] : y[rr][c] + o;
+                            }
+                    }
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) y[rr][c] *= kRhtScale;
+                }
+                uint32_t sc[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) m = max(m, __float_as_uint(y[rr][c]) & 0x7FFFFFFFu);
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    sc[c] = e8m0_from_f32bits(m);
+                }
+                // random words of the lane's elements for the column copy, [row][column]
+                uint32_t rw[8][8];
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                    const int64_t row = row0 + 8 * li + rr;
+                    if (sr && row < R) {
+                        w0 = sr_words4((uint64_t)(row * C + c8), 1u, p.seed);
+                        w1 = sr_words4((uint64_t)(row * C + c8 + 4), 1u, p.seed);
+                    }
+                    rw[rr][0] = w0.x; rw[rr][1] = w0.y; rw[rr][2] = w0.z; rw[rr][3] = w0.w;
+                    rw[rr][4] = w1.x; rw[rr][5] = w1.y; rw[rr][6] = w1.z; rw[rr][7] = w1.w;
+                }
+                uint8_t* qb = p.q_col + b * R * C;
+                if (cval) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float f = inv_scale_from_e8m0(sc[c]);
+                        uint2 q;
+                        q.x = code2(y[0][c] * f, y[1][c] * f, rw[0][c], rw[1][c]) |
+                              (code2(y[2][c] * f, y[3][c] * f, rw[2][c], rw[3][c]) << 16);
+                        q.y = code2(y[4][c] * f, y[5][c] * f, rw[4][c], rw[5][c]) |
+                              (code2(y[6][c] * f, y[7][c] * f, rw[6][c], rw[7][c]) << 16);
+                        if (sc[c] == 0xFFu) {
+                            uint32_t sg[2] = {0u, 0u};
+#pragma unroll
+                            for (int rr = 0; rr < 8; ++rr)
+                                sg[rr >> 2] |= ((__float_as_uint(y[rr][c]) >> 24) & 0x80u) << (8 * (rr & 3));
+                            q.x = 0x7F7F7F7Fu | sg[0];
+                            q.y = 0x7F7F7F7Fu | sg[1];
+                        }
+                        *reinterpret_cast<uint2*>(qb + (c8 + c) * R + row0 + 8 * li) = q;
+                    }
+                    store_col_scales(sc);
+                }
+            }
+            continue;
+        }
+
+        if constexpr (!kExt) {  // the plain MX quantization
+            // magnitude bits of every element (bf16 pairs), shared by both directions
+            uint32_t mg[8][4];
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) m = vmax_u16x2(m, mg[rr][k]);
-            m = shfl_xor_max16x2(m, 1);
-            m = shfl_xor_max16x2(m, 2);
-            m = shfl_xor_max16x2(m, 8);
-            m = shfl_xor_max16x2(m, 16);
-            sblk = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
-        }
+                for (int k = 0; k < 4; ++k) mg[rr][k] = v[rr][k] & 0x7FFF7FFFu;
 
-        if constexpr (kRowOut) {
-            // two rows per word: pp[k] = (amax of row 2k, amax of row 2k+1) over this lane's 8 columns
-            uint32_t pp[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t a = vmax_u16x2(vmax_u16x2(mg[2 * k][0], mg[2 * k][1]), vmax_u16x2(mg[2 * k][2], mg[2 * k][3]));
-                const uint32_t c = vmax_u16x2(vmax_u16x2(mg[2 * k + 1][0], mg[2 * k + 1][1]),
-                                              vmax_u16x2(mg[2 * k + 1][2], mg[2 * k + 1][3]));
-                pp[k] = vmax_u16x2(__byte_perm(a, c, 0x5410), __byte_perm(a, c, 0x7632));
-            }
-            uint32_t s8[8];
+            uint32_t sblk = 0;  // the 32x32 block's scale
             if constexpr (kB32) {
+                // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1), 4 down (li)
+                uint32_t m = 0;
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) s8[rr] = sblk;
-            } else {
+                for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) m = vmax_u16x2(m, mg[rr][k]);
+                m = shfl_xor_max16x2(m, 1);
+                m = shfl_xor_max16x2(m, 2);
+                m = shfl_xor_max16x2(m, 8);
+                m = shfl_xor_max16x2(m, 16);
+                sblk = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
+            }
+
+            if constexpr (kRowOut) {
+                // two rows per word: pp[k] = (amax of row 2k, amax of row 2k+1) over this lane's 8 columns
+                uint32_t pp[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    uint32_t m = shfl_xor_max16x2(pp[k], 1);
-                    m = shfl_xor_max16x2(m, 2);
-                    s8[2 * k] = e8m0_from_absbits(m & 0xFFFFu);
-                    s8[2 * k + 1] = e8m0_from_absbits(m >> 16);
+                    const uint32_t a = vmax_u16x2(vmax_u16x2(mg[2 * k][0], mg[2 * k][1]), vmax_u16x2(mg[2 * k][2], mg[2 * k][3]));
+                    const uint32_t c = vmax_u16x2(vmax_u16x2(mg[2 * k + 1][0], mg[2 * k + 1][1]),
+                                                  vmax_u16x2(mg[2 * k + 1][2], mg[2 * k + 1][3]));
+                    pp[k] = vmax_u16x2(__byte_perm(a, c, 0x5410), __byte_perm(a, c, 0x7632));
                 }
-            }
-            bool nonfinite = false;
+                uint32_t s8[8];
+                if constexpr (kB32) {
 #pragma unroll
-            for (int rr = 0; rr < 8; ++rr) nonfinite |= s8[rr] == 0xFFu;
-            const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
-            uint8_t* qb = p.q_row + b * R * C;
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                const int64_t row = row0 + 8 * li + rr;
-                uint2 q = quant8(v[rr], inv_scale_from_e8m0(s8[rr]));
-                if (any_nonfinite && s8[rr] == 0xFFu) {
-                    const uint2 sg = signs8(v[rr]);
-                    q.x = 0x7F7F7F7Fu | sg.x;
-                    q.y = 0x7F7F7F7Fu | sg.y;
-                }
-                if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
-            }
-            // scales: the 4 lanes of a 32-column block each write two of the 8 rows
-            if (cval) {
-                uint8_t* sb = p.s_row + b * p.s_row_bstride;
-                const int64_t cb = c8 / kBlk;
-                const int q4 = lj & 3;
-                if constexpr (kB32Only) {
-                    if (li == 0 && q4 == 0) sb[(row0 / kBlk) * Cb + cb] = (uint8_t)s8[0];
+                    for (int rr = 0; rr < 8; ++rr) s8[rr] = sblk;
                 } else {
-                    // this lane's two rows 2*q4, 2*q4+1 (register selects, no local-memory indexing)
-                    const uint32_t my_s[2] = {q4 == 0 ? s8[0] : q4 == 1 ? s8[2] : q4 == 2 ? s8[4] : s8[6],
-                                              q4 == 0 ? s8[1] : q4 == 1 ? s8[3] : q4 == 2 ? s8[5] : s8[7]};
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int rr = 2 * q4 + h;
-                        const int64_t row = row0 + 8 * li + rr;
-                        if (row >= R) continue;
-                        const uint8_t sv = (uint8_t)my_s[h];
-                        if (!p.blocked) {
-                            sb[row * Cb + cb] = sv;
-                            continue;
-                        }
-                        int64_t pr = row;
-                        if (grouped) {
-                            int g = wg0;
-                            if (wg0 != wg1) g = find_group(ends_s, p.G, row);
-                            if (g >= p.G) continue;
-                            pr = pstart_s[g] + (row - (g ? ends_s[g - 1] : 0));
-                        }
-                        const int64_t off = blocked_off(pr, cb, ct_row);
-                        sb[off] = sv;
-                        // last block-column of a row whose K/32 is not a multiple of 4: zero the rest of the word
-                        if (cb == Cb - 1)
-                            for (int64_t z = (Cb & 3); z != 0 && z < 4; ++z) sb[off + z - (Cb & 3) + 1] = 0;
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t m = shfl_xor_max16x2(pp[k], 1);
+                        m = shfl_xor_max16x2(m, 2);
+                        s8[2 * k] = e8m0_from_absbits(m & 0xFFFFu);
+                        s8[2 * k + 1] = e8m0_from_absbits(m >> 16);
+                    }
+                }
+                bool nonfinite = false;
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) nonfinite |= s8[rr] == 0xFFu;
+                const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
+                uint8_t* qb = p.q_row + b * R * C;
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int64_t row = row0 + 8 * li + rr;
+                    uint2 q = quant8(v[rr], inv_scale_from_e8m0(s8[rr]));
+                    if (any_nonfinite && s8[rr] == 0xFFu) {
+                        const uint2 sg = signs8(v[rr]);
+                        q.x = 0x7F7F7F7Fu | sg.x;
+                        q.y = 0x7F7F7F7Fu | sg.y;
+                    }
+                    if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
+                }
+                // scales: the 4 lanes of a 32-column block each write two of the 8 rows
+                if (cval) {
+                    uint8_t* sb = p.s_row + b * p.s_row_bstride;
+                    const int64_t cb = c8 / kBlk;
+                    const int q4 = lj & 3;
+                    if constexpr (kB32Only) {
+                        if (li == 0 && q4 == 0) sb[(row0 / kBlk) * Cb + cb] = (uint8_t)s8[0];
+                    } else {
+                        store_row_scales(s8);
                     }
                 }
             }
-        }
 
-        if constexpr (kCol) {
-            uint32_t sc[8];
-            if constexpr (kB32) {
+            if constexpr (kCol) {
+                uint32_t sc[8];
+                if constexpr (kB32) {
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) sc[cc] = sblk;
-            } else {
-                // column amax over 32 rows: 8 here (packed pairs of columns), then lanes li = 0..3
-                uint32_t cm[4];
+                    for (int cc = 0; cc < 8; ++cc) sc[cc] = sblk;
+                } else {
+                    // column amax over 32 rows: 8 here (packed pairs of columns), then lanes li = 0..3
+                    uint32_t cm[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mg[0][k], mg[1][k]), vmax_u16x2(mg[2][k], mg[3][k])),
-                                            vmax_u16x2(vmax_u16x2(mg[4][k], mg[5][k]), vmax_u16x2(mg[6][k], mg[7][k])));
-                    m = shfl_xor_max16x2(m, 8);
-                    cm[k] = shfl_xor_max16x2(m, 16);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    sc[2 * k] = e8m0_from_absbits(cm[k] & 0xFFFFu);
-                    sc[2 * k + 1] = e8m0_from_absbits(cm[k] >> 16);
-                }
-            }
-            bool nonfinite = false;
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) nonfinite |= sc[cc] == 0xFFu;
-            const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
-            uint8_t* qb = p.q_col + b * R * C;
-            if (cval) {
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const float f = inv_scale_from_e8m0(sc[cc]);
-                    const int k = cc >> 1;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int rr = 0; rr < 8; rr += 2) {
-                        const float a = (cc & 1) ? bf16hi(v[rr][k]) : bf16lo(v[rr][k]);
-                        const float c = (cc & 1) ? bf16hi(v[rr + 1][k]) : bf16lo(v[rr + 1][k]);
-                        const float2 y = mul2(a, c, f);
-                        w[rr >> 1] = cvt_e4m3x2(y.x, y.y);
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mg[0][k], mg[1][k]), vmax_u16x2(mg[2][k], mg[3][k])),
+                                                vmax_u16x2(vmax_u16x2(mg[4][k], mg[5][k]), vmax_u16x2(mg[6][k], mg[7][k])));
+                        m = shfl_xor_max16x2(m, 8);
+                        cm[k] = shfl_xor_max16x2(m, 16);
                     }
-                    uint2 q;
-                    q.x = w[0] | (w[1] << 16);
-                    q.y = w[2] | (w[3] << 16);
-                    if (any_nonfinite && sc[cc] == 0xFFu) {
-                        uint32_t sg[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        sc[2 * k] = e8m0_from_absbits(cm[k] & 0xFFFFu);
+                        sc[2 * k + 1] = e8m0_from_absbits(cm[k] >> 16);
+                    }
+                }
+                bool nonfinite = false;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) nonfinite |= sc[cc] == 0xFFu;
+                const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
+                uint8_t* qb = p.q_col + b * R * C;
+                if (cval) {
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const float f = inv_scale_from_e8m0(sc[cc]);
+                        const int k = cc >> 1;
+                        uint32_t w[4];
 #pragma unroll
                         for (int rr = 0; rr < 8; rr += 2) {
-                            const uint32_t a = (cc & 1) ? (v[rr][k] >> 31) : ((v[rr][k] >> 15) & 1u);
-                            const uint32_t c = (cc & 1) ? (v[rr + 1][k] >> 31) : ((v[rr + 1][k] >> 15) & 1u);
-                            sg[rr >> 1] = (a << 7) | (c << 15);
+                            const float a = (cc & 1) ? bf16hi(v[rr][k]) : bf16lo(v[rr][k]);
+                            const float c = (cc & 1) ? bf16hi(v[rr + 1][k]) : bf16lo(v[rr + 1][k]);
+                            const float2 y = mul2(a, c, f);
+                            w[rr >> 1] = cvt_e4m3x2(y.x, y.y);
                         }
-                        q.x = 0x7F7F7F7Fu | sg[0] | (sg[1] << 16);
-                        q.y = 0x7F7F7F7Fu | sg[2] | (sg[3] << 16);
-                    }
-                    *reinterpret_cast<uint2*>(qb + (c8 + cc) * R + row0 + 8 * li) = q;
-                }
-                // scales: each of the 4 lanes li writes two of this lane-column's 8 columns
-                uint8_t* sb = p.s_col + b * p.s_col_bstride;
-                const int64_t rb = row0 / kBlk;
-                int64_t pc = rb;
-                bool ok = true;
-                if (p.blocked && grouped) {
-                    ok = wg0 < p.G;
-                    if (ok) pc = pstart_s[wg0] / kBlk + (row0 - (wg0 ? ends_s[wg0 - 1] : 0)) / kBlk;
-                }
-                const uint32_t my_s[2] = {li == 0 ? sc[0] : li == 1 ? sc[2] : li == 2 ? sc[4] : sc[6],
-                                          li == 0 ? sc[1] : li == 1 ? sc[3] : li == 2 ? sc[5] : sc[7]};
+                        uint2 q;
+                        q.x = w[0] | (w[1] << 16);
+                        q.y = w[2] | (w[3] << 16);
+                        if (any_nonfinite && sc[cc] == 0xFFu) {
+                            uint32_t sg[4];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int64_t c = c8 + 2 * li + h;
-                    if (!p.blocked) sb[c * (R / kBlk) + rb] = (uint8_t)my_s[h];
-                    else if (ok) sb[blocked_off(c, pc, ct_col)] = (uint8_t)my_s[h];
+                            for (int rr = 0; rr < 8; rr += 2) {
+                                const uint32_t a = (cc & 1) ? (v[rr][k] >> 31) : ((v[rr][k] >> 15) & 1u);
+                                const uint32_t c = (cc & 1) ? (v[rr + 1][k] >> 31) : ((v[rr + 1][k] >> 15) & 1u);
+                                sg[rr >> 1] = (a << 7) | (c << 15);
+                            }
+                            q.x = 0x7F7F7F7Fu | sg[0] | (sg[1] << 16);
+                            q.y = 0x7F7F7F7Fu | sg[2] | (sg[3] << 16);
+                        }
+                        *reinterpret_cast<uint2*>(qb + (c8 + cc) * R + row0 + 8 * li) = q;
+                    }
+                    store_col_scales(sc);
                 }
             }
         }
@@ -504,12 +751,12 @@ static bool make_x_map(CUtensorMap* m, const QParams& p) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <unsigned DIRS>
+template <unsigned DIRS, bool kExt = false>
 static mxfp8_status_t launch_dirs(const CUtensorMap& m, const QParams& p, int64_t grid, cudaStream_t st) {
     static std::atomic<int> attr_set[host::kMaxDevices];
-    if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS>), kQSmem, attr_set))
+    if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS, kExt>), kQSmem, attr_set))
         return MXFP8_ERR_LAUNCH;
-    quant_tile_kernel<DIRS><<<(unsigned)grid, kQThreads, kQSmem, st>>>(m, p);
+    quant_tile_kernel<DIRS, kExt><<<(unsigned)grid, kQThreads, kQSmem, st>>>(m, p);
     return host::last_launch_status();
 }
 
@@ -531,21 +778,32 @@ static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t
     }
 }
 
-}  // namespace mx
+// The stability variants (one CTA per SM: fp32 working values need the registers).
+static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStream_t st) {
+    if (p.ntiles == 0) return MXFP8_OK;
+    CUtensorMap m;
+    if (!make_x_map(&m, p)) return MXFP8_ERR_DRIVER;
+    const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms());
+    switch (dirs) {
+        case MXFP8_ROW: return launch_dirs<MXFP8_ROW, true>(m, p, grid, st);
+        case MXFP8_COL: return launch_dirs<MXFP8_COL, true>(m, p, grid, st);
+        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, true>(m, p, grid, st);
+        default: return MXFP8_ERR_LAYOUT;
+    }
+}
 
-using namespace mx;
-
-extern "C" mxfp8_status_t mxfp8_quantize_2d(const void* x_bf16, int64_t M, int64_t K, unsigned dirs,
-                                            int scale_layout, const int32_t* offs, int32_t G, void* q_row,
-                                            void* s_row, void* q_col, void* s_col, int32_t* dev_status,
-                                            mxfp8_stream_t stream) {
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+static mxfp8_status_t quantize_2d(const void* x_bf16, int64_t M, int64_t K, unsigned dirs, int scale_layout,
+                                  const int32_t* offs, int32_t G, unsigned opts, uint64_t seed, void* q_row,
+                                  void* s_row, void* q_col, void* s_col, int32_t* dev_status, cudaStream_t st) {
     if (M < 0 || K <= 0 || G < 0 || G > MXFP8_MAX_GROUPS || M > INT32_MAX) return MXFP8_ERR_SHAPE;
     if (K % 32) return MXFP8_ERR_ALIGN;
     if (scale_layout != MXFP8_SCALES_COMPACT && scale_layout != MXFP8_SCALES_BLOCKED) return MXFP8_ERR_LAYOUT;
     const bool row = dirs & MXFP8_ROW, col = dirs & MXFP8_COL, b32 = dirs & MXFP8_BLOCK32X32;
     if (dirs == 0 || (dirs & ~7u) || (b32 && (row || col))) return MXFP8_ERR_LAYOUT;
     if (b32 && scale_layout != MXFP8_SCALES_COMPACT) return MXFP8_ERR_LAYOUT;
+    if ((opts & ~7u) || (opts && b32) || ((opts & MXFP8_OPT_HADAMARD_ROW) && !row) ||
+        ((opts & MXFP8_OPT_HADAMARD_COL) && !col))
+        return MXFP8_ERR_LAYOUT;
     if (!x_bf16) return MXFP8_ERR_NULL;
     if ((row || b32) && (!q_row || !s_row)) return MXFP8_ERR_NULL;
     if (col && (!q_col || !s_col)) return MXFP8_ERR_NULL;
@@ -565,9 +823,30 @@ extern "C" mxfp8_status_t mxfp8_quantize_2d(const void* x_bf16, int64_t M, int64
     p.offs = offs; p.G = offs ? G : 0;
     p.dev_status = dev_status;
     p.tiles_r = (M + 127) / 128; p.tiles_c = (K + 127) / 128; p.ntiles = p.tiles_r * p.tiles_c;
+    p.opts = opts;
+    p.seed = seed;
     if (p.ntiles >= INT32_MAX) return MXFP8_ERR_SHAPE;
-    if (mxfp8_status_t s = launch_tiles(dirs, p, st); s != MXFP8_OK) return s;
-    return MXFP8_OK;
+    return opts ? launch_tiles_ext(dirs, p, st) : launch_tiles(dirs, p, st);
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" mxfp8_status_t mxfp8_quantize_2d(const void* x_bf16, int64_t M, int64_t K, unsigned dirs,
+                                            int scale_layout, const int32_t* offs, int32_t G, void* q_row,
+                                            void* s_row, void* q_col, void* s_col, int32_t* dev_status,
+                                            mxfp8_stream_t stream) {
+    return mx::quantize_2d(x_bf16, M, K, dirs, scale_layout, offs, G, 0u, 0u, q_row, s_row, q_col, s_col, dev_status,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" mxfp8_status_t mxfp8_quantize_2d_opts(const void* x_bf16, int64_t M, int64_t K, unsigned dirs,
+                                                 int scale_layout, const int32_t* offs, int32_t G, unsigned opts,
+                                                 uint64_t seed, void* q_row, void* s_row, void* q_col, void* s_col,
+                                                 int32_t* dev_status, mxfp8_stream_t stream) {
+    return mx::quantize_2d(x_bf16, M, K, dirs, scale_layout, offs, G, opts, seed, q_row, s_row, q_col, s_col,
+                           dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" mxfp8_status_t mxfp8_quantize_3d_experts(const void* w_bf16, int32_t G, int64_t N, int64_t K, unsigned dirs,

@@ -1,0 +1,136 @@
+"""Stability variants of the quantization ("MXFP8 (Micro-scaling FP8)", "Numerical stability":
+random Hadamard transforms spread outliers before quantization; stochastic rounding removes the
+bias of deterministic rounding) against the oracle, byte for byte.
+
+Both sides draw the same Philox4x32-10 words (counter from the element index and the copy, key
+from the seed) and evaluate the Hadamard butterflies in fp32 in the same order, so codes and
+scales must agree exactly, padding of the blocked layouts included.  The composite op's GEMMs
+with these options are compared with the oracle's fp64 GEMMs of the oracle's operands within
+the GEMM bound."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp8_precision_moe_gb300 import synth
+from tests._util import assert_gemm_close, f64, require_gpu, sizes_to_ends, u8, u16
+
+pytestmark = pytest.mark.gpu
+
+SEED = 0x1234_5678_9ABC_DEF0
+
+
+@pytest.fixture(scope="module")
+def mx():
+    require_gpu()
+    import mxfp8_precision_moe_gb300 as m
+
+    m.load()
+    return m
+
+
+def mixed_input(M, K, seed):
+    """Rows of very different magnitude, tiny elements (the subnormal E4M3 range after scaling)
+    and a few outliers."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((M, K), generator=g) * torch.pow(10.0, torch.rand((M, 1), generator=g) * 6 - 3)
+    x[torch.rand((M, K), generator=g) < 0.05] *= 1e-3
+    x[torch.rand((M, K), generator=g) < 0.01] *= 50.0
+    return x.to(torch.bfloat16)
+
+
+def oracle_opts(x, opts_gpu, seed):
+    row_opts = (oracle.OPT_SR if opts_gpu & 1 else 0) | (oracle.OPT_RHT if opts_gpu & 2 else 0)
+    col_opts = (oracle.OPT_SR if opts_gpu & 1 else 0) | (oracle.OPT_RHT if opts_gpu & 4 else 0)
+    return oracle.quantize_rows_opts(u16(x), row_opts, seed), oracle.quantize_cols_opts(u16(x), col_opts, seed)
+
+
+OPTS = [1, 2, 4, 2 | 4, 1 | 2, 1 | 4, 1 | 2 | 4]
+
+
+@pytest.mark.parametrize("opts", OPTS)
+def test_compact_both_directions(mx, opts):
+    M, K = 256, 384
+    x = mixed_input(M, K, seed=opts)
+    q, s, qT, sT = [u8(t) for t in mx.mxfp8_quantize_2d(x.cuda(), mx.ROW | mx.COL, mx.SCALES_COMPACT,
+                                                        opts=opts, seed=SEED)]
+    (qo, so), (qTo, sTo) = oracle_opts(x, opts, SEED)
+    assert np.array_equal(s, so) and np.array_equal(sT, sTo)
+    assert np.array_equal(q, qo), f"{int((q != qo).sum())} row codes differ"
+    assert np.array_equal(qT, qTo), f"{int((qT != qTo).sum())} column codes differ"
+
+
+@pytest.mark.parametrize("dirs,opts", [(1, 1), (1, 3), (2, 1), (2, 5)])
+def test_single_direction_equals_fused(mx, dirs, opts):
+    x = mixed_input(128, 256, seed=40 + opts).cuda()
+    a = mx.mxfp8_quantize_2d(x, mx.ROW | mx.COL, mx.SCALES_COMPACT, opts=opts, seed=SEED)
+    b = mx.mxfp8_quantize_2d(x, dirs, mx.SCALES_COMPACT, opts=opts, seed=SEED)
+    torch.cuda.synchronize()
+    i = 0 if dirs == 1 else 2
+    assert torch.equal(a[i], b[i]) and torch.equal(a[i + 1], b[i + 1])
+
+
+@pytest.mark.parametrize("opts", [1, 4, 1 | 2 | 4])
+def test_blocked_grouped(mx, opts):
+    sizes = [96, 0, 160, 32]
+    M, K = sum(sizes), 416   # K/32 = 13: a partial last scale tile
+    x = mixed_input(M, K, seed=50 + opts)
+    offs = torch.tensor(sizes_to_ends(sizes).astype(np.int32), device="cuda")
+    q, s, qT, sT = [u8(t) for t in mx.mxfp8_quantize_2d(x.cuda(), mx.ROW | mx.COL, mx.SCALES_BLOCKED, offs,
+                                                        opts=opts, seed=SEED)]
+    (qo, so), (qTo, sTo) = oracle_opts(x, opts, SEED)
+    ends = sizes_to_ends(sizes)
+    n_row = oracle.blocked_rowgroups_bytes(ends, K // 32)
+    n_col = oracle.blocked_colgroups_bytes(K, ends)
+    assert np.array_equal(q, qo) and np.array_equal(qT, qTo)
+    assert np.array_equal(s[:n_row], oracle.blocked_rowgroups(so, ends))
+    assert np.array_equal(sT[:n_col], oracle.blocked_colgroups(sTo, ends))
+
+
+def test_seed_changes_only_what_it_keys(mx):
+    x = mixed_input(64, 128, seed=60).cuda()
+    a = mx.mxfp8_quantize_2d(x, mx.ROW, mx.SCALES_COMPACT, opts=1, seed=1)
+    b = mx.mxfp8_quantize_2d(x, mx.ROW, mx.SCALES_COMPACT, opts=1, seed=2)
+    c = mx.mxfp8_quantize_2d(x, mx.ROW, mx.SCALES_COMPACT, opts=1, seed=1)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], c[0]) and not torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_option_errors(mx):
+    x = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    for dirs, opts in ((mx.ROW, mx.OPT_HADAMARD_COL), (mx.COL, mx.OPT_HADAMARD_ROW), (mx.ROW, 8),
+                       (mx.BLOCK32X32, mx.OPT_STOCHASTIC)):
+        with pytest.raises(mx.Mxfp8Error, match="LAYOUT"):
+            mx.mxfp8_quantize_2d(x, dirs, mx.SCALES_COMPACT, opts=opts, seed=1)
+
+
+def test_composite_with_stability_options(mx):
+    sizes = [128, 64, 0, 96]
+    G, N, K = len(sizes), 128, 256
+    M = sum(sizes)
+    A = mixed_input(M, K, seed=70)
+    W = synth.randn_bf16((G, N, K), 0.02, seed=71)
+    dO = synth.randn_bf16((M, N), 1e-2, seed=72)
+    offs = torch.tensor(sizes_to_ends(sizes).astype(np.int32), device="cuda")
+    Ag, Wg = A.cuda().requires_grad_(True), W.cuda().requires_grad_(True)
+    out = mx.to_mxfp8_then_scaled_grouped_mm(Ag, Wg, offs, stochastic_rounding=True, hadamard_wgrad=True, seed=SEED)
+    out.backward(dO.cuda())
+    torch.cuda.synchronize()
+    ends = sizes_to_ends(sizes)
+    # dgrad: dOut rounded stochastically along N
+    dq, ds = oracle.quantize_rows_opts(u16(dO), oracle.OPT_SR, SEED)
+    wTq, wTs = zip(*[oracle.quantize_cols(u16(W[g])) for g in range(G)])
+    assert_gemm_close(f64(Ag.grad), oracle.grouped_mm_rows(dq, ds, np.stack(wTq), np.stack(wTs), ends), what="dA")
+    # wgrad: both operands Hadamard-transformed along the tokens with the same seed, dOut also SR
+    dTq, dTs = oracle.quantize_cols_opts(u16(dO), oracle.OPT_SR | oracle.OPT_RHT, SEED)
+    aTq, aTs = oracle.quantize_cols_opts(u16(A), oracle.OPT_RHT, SEED)
+    ref_dw = oracle.grouped_mm_wgrad(dTq, dTs, aTq, aTs, ends)
+    assert_gemm_close(f64(Wg.grad), ref_dw, what="dW")
+    # the transform is orthogonal: the same wgrad without it, from the unquantized bf16 inputs,
+    # agrees to MXFP8 accuracy (relative Frobenius error well below E4M3's 2^-4)
+    exact = np.zeros_like(ref_dw)
+    lo = 0
+    for g, hi in enumerate(ends):
+        exact[g] = f64(dO)[lo:hi].T @ f64(A)[lo:hi]
+        lo = int(hi)
+    assert np.linalg.norm(f64(Wg.grad) - exact) / np.linalg.norm(exact) < 0.05
