@@ -126,11 +126,16 @@ def test_composite_with_stability_options(mx):
     aTq, aTs = oracle.quantize_cols_opts(u16(A), oracle.OPT_RHT, SEED)
     ref_dw = oracle.grouped_mm_wgrad(dTq, dTs, aTq, aTs, ends)
     assert_gemm_close(f64(Wg.grad), ref_dw, what="dW")
-    # the transform is orthogonal: the same wgrad without it, from the unquantized bf16 inputs,
-    # agrees to MXFP8 accuracy (relative Frobenius error well below E4M3's 2^-4)
+    # the transform is orthogonal, so the wgrad still approximates dOut^T A: against the fp64
+    # product of the unquantized inputs it is about as accurate as the plain MXFP8 wgrad (a sign
+    # vector that differed between the two operands would leave an error near 100%)
     exact = np.zeros_like(ref_dw)
     lo = 0
     for g, hi in enumerate(ends):
         exact[g] = f64(dO)[lo:hi].T @ f64(A)[lo:hi]
         lo = int(hi)
-    assert np.linalg.norm(f64(Wg.grad) - exact) / np.linalg.norm(exact) < 0.05
+    Ap, Wp = A.cuda().requires_grad_(True), W.cuda().requires_grad_(True)
+    mx.to_mxfp8_then_scaled_grouped_mm(Ap, Wp, offs).backward(dO.cuda())
+    torch.cuda.synchronize()
+    rel = lambda got: np.linalg.norm(f64(got) - exact) / np.linalg.norm(exact)
+    assert rel(Wg.grad) < max(2.0 * rel(Wp.grad), 0.02), (rel(Wg.grad), rel(Wp.grad))
