@@ -62,6 +62,8 @@ WORKLOAD_TEXT = {
     "tiny": "Tiny: G=2, A[256,256], offs [128,256], W[2,128,256] (latency-bound; parity case)",
     "scout_w32": WORKLOAD + "; expert weights quantized with one scale per 32x32 block (one quantization for "
                             "the forward and the dgrad)",
+    "scout_stab": WORKLOAD + "; stability variants: random Hadamard transform of both wgrad operands along the "
+                             "tokens, stochastic rounding of the output gradient",
     "scout_mb4": "Llama4-Scout-like routed experts, one optimizer step of 4 microbatches (G=8, K=5120, N=8192, "
                  "M=16384 tokens each, Zipf(1.1) group sizes in 32-token chunks, seeds 0-3): W quantized once "
                  "(prequantized-weight cache), then fwd+bwd per microbatch",
@@ -74,7 +76,7 @@ def workload_parts(name: str, dev) -> list:
 
     if name in ("scout", "imbalanced", "tiny"):
         return [synth.workload(name, seed=0, device=dev)]
-    if name == "scout_w32":
+    if name in ("scout_w32", "scout_stab"):
         return [synth.workload("scout", seed=0, device=dev)]
     if name in ("swiglu", "swiglu_unfused"):
         return [synth.workload("swiglu", seed=0, device=dev)]
@@ -119,7 +121,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--no-baseline", action="store_true", help="skip the cuBLAS bf16 comparison leg")
-    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "swiglu_unfused", "swiglu_standin", "tiny", "scout_mb4", "scout_w32",
+    ap.add_argument("--workload", default="scout", choices=["scout", "imbalanced", "swiglu", "swiglu_unfused", "swiglu_standin", "tiny", "scout_mb4", "scout_w32", "scout_stab",
                              "sweep"],
                     help="scout (default, the reported line); the others are extra measurements")
     return ap.parse_args()
@@ -223,7 +225,8 @@ class ClockSampler:
 class Step:
     """Device buffers of one replica and the C-ABI calls of one pass of the path."""
 
-    def __init__(self, w: dict, device, shared_w: "Step | None" = None, w_block32: bool = False):
+    def __init__(self, w: dict, device, shared_w: "Step | None" = None, w_block32: bool = False,
+                 stability: bool = False):
         import mxfp8_precision_moe_gb300 as mx
 
         L = mx.load()
@@ -267,6 +270,18 @@ class Step:
             ("wgrad", L.mxfp8_grouped_mm_wgrad, (P(self.dTq), P(self.dTs), P(self.aTq), P(self.aTs), P(self.offs), G,
                                                  M, N, K, P(self.dW), st)),
         ]
+        if stability:
+            # the stability variants: Hadamard transform of both wgrad operands along the tokens (A's and
+            # dOut's column-wise copies, one seed), stochastic rounding of both dOut copies
+            seed = 0x5EED
+            calls = dict((c[0], c) for c in self.calls)
+            calls["quant_A"] = ("quant_A", L.mxfp8_quantize_2d_opts,
+                                (P(self.A), M, K, RC, 1, P(self.offs), G, 4, seed, P(self.aq), P(self.as_),
+                                 P(self.aTq), P(self.aTs), st))
+            calls["quant_dOut"] = ("quant_dOut", L.mxfp8_quantize_2d_opts,
+                                   (P(self.D), M, N, RC, 1, P(self.offs), G, 1 | 4, seed, P(self.dq), P(self.ds),
+                                    P(self.dTq), P(self.dTs), st))
+            self.calls = [calls[c[0]] for c in self.calls]
         # kernels each call launches (one each: the quantize kernels also write the blocked padding)
         self.launches = {"quant_A": 1, "quant_W": 1, "fwd": 1, "quant_dOut": 1, "dgrad": 1, "wgrad": 1}
         self.flops = 3 * 2.0 * M * N * K
@@ -506,7 +521,7 @@ def run_native(args, rank, world, local):
     if args.workload in ("swiglu", "swiglu_unfused"):
         step = SwiGLUStep(w, dev, fused=args.workload == "swiglu")
     elif len(parts) == 1:
-        step = Step(w, dev, w_block32=args.workload == "scout_w32")
+        step = Step(w, dev, w_block32=args.workload == "scout_w32", stability=args.workload == "scout_stab")
     else:
         step = StepGroup(parts, dev, share_w=args.workload == "scout_mb4")
     single = isinstance(step, Step)
@@ -710,6 +725,9 @@ def run_sweep(args) -> dict:
     stream = torch.cuda.current_stream(dev)
     sp = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
     rows = []
+    sampler = ClockSampler(dev.index)
+    time.sleep(0.3)
+    wall0 = time.time()
 
     def time_call(fn, argv, nbytes, label, shape):
         for _ in range(3):
@@ -744,6 +762,17 @@ def run_sweep(args) -> dict:
                 time_call(L.mxfp8_quantize_2d, (sp(x), M, K, dirs, lay, None, 0, *[sp(t) for t in out], None), nb,
                           label, [M, K])
             del x, q, qT, s_r, s_c, s32
+    # stability variants (mxfp8_quantize_2d_opts) on one activation shape, both copies
+    M, K = 16384, 5120
+    x = synth.log_uniform_rows(M, K, seed=M + K, device=dev)
+    u8 = lambda *shape: torch.empty(shape, dtype=torch.uint8, device=dev)
+    q, qT = u8(M, K), u8(K, M)
+    s_r, s_c = u8(mx.mxfp8_scale_bytes(M, K, 1, 1)), u8(mx.mxfp8_scale_bytes_colgroups(K, M, 1))
+    for label, opts in (("row+col SR", 1), ("row+col RHT(col)", 4), ("row+col RHT(row,col)", 6),
+                        ("row+col SR+RHT(col)", 5)):
+        time_call(L.mxfp8_quantize_2d_opts, (sp(x), M, K, 3, 1, None, 0, opts, 0x5EED, sp(q), sp(s_r), sp(qT), sp(s_c),
+                                             None), M * K * (2 + 2 + 2 / 32), label, [M, K])
+    del x, q, qT, s_r, s_c
     G, N, K = 16, 8192, 5120
     w = synth.randn_bf16((G, N, K), 1.0, seed=7, device=dev)
     ce = lambda r, c: ((r + 127) // 128) * 128 * ((c + 127) // 128) * 4
@@ -755,8 +784,11 @@ def run_sweep(args) -> dict:
         nb = E * (2 + 2 + 2 / 32) if dirs & 3 == 3 else E * (2 + 1 + 1 / 32)
         time_call(L.mxfp8_quantize_3d_experts, (sp(w), G, N, K, dirs, 1, *[sp(t) for t in out], None), nb, label,
                   [G, N, K])
+    wall1 = time.time()
+    sampler.stop()
     best = max(r["frac_hbm"] for r in rows)
     return {"metric": "MXFP8 quantize GB/s (sweep)", "unit": "GB/s", "hbm_peak_gbs": pk["hbm"],
+            "clocks": sampler.summary(wall0, wall1),
             "peak_note": f"{pk['src']} copy bandwidth", "data": "synthetic",
             "config": {"workload": "quantization sweep: [M,K] M in 8192..131072, K in {5120, 8192}; "
                                    "3D [16,8192,5120]; N(0,1)*10^U(-4,4) per row"},
