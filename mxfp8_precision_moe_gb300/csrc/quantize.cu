@@ -204,9 +204,9 @@ constexpr int kQThreads = 288;                 // 8 consumer warps + 1 TMA produ
 constexpr int kQSmem = kQStages * kQTileBytes + 128;
 
 // kExt: the stability variants of ROW / COL / ROW|COL (runtime options p.opts, seed p.seed); fp32
-// working values, one CTA per SM.
+// working values.
 template <unsigned DIRS, bool kExt = false>
-__global__ void __launch_bounds__(kQThreads, kExt ? 1 : 2)
+__global__ void __launch_bounds__(kQThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
     constexpr bool kRow = (DIRS & MXFP8_ROW) != 0;
     constexpr bool kCol = (DIRS & MXFP8_COL) != 0;
@@ -341,15 +341,26 @@ __global__ void __launch_bounds__(kQThreads, kExt ? 1 : 2)
         // this warp's 32 x 64 sub-tile: lane rows 8li..8li+7, columns 8lj..8lj+7 (16 bytes each)
         const uint8_t* src = tiles + stage * kQTileBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
         uint32_t v[8][4];
+        if constexpr (!kExt) {
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-            const uint4 u = *reinterpret_cast<const uint4*>(src + rr * 256);
-            v[rr][0] = u.x; v[rr][1] = u.y; v[rr][2] = u.z; v[rr][3] = u.w;
+            for (int rr = 0; rr < 8; ++rr) {
+                const uint4 u = *reinterpret_cast<const uint4*>(src + rr * 256);
+                v[rr][0] = u.x; v[rr][1] = u.y; v[rr][2] = u.z; v[rr][3] = u.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
+        // the stability variants read their values from the stage while they work and free it after
+        const int cur_stage = stage;
+        auto release_stage = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[cur_stage]);
+        };
         if (++stage == kQStages) { stage = 0; phase ^= 1u; }
-        if (row0 >= R || col0 >= C) continue;  // warp-uniform
+        if (row0 >= R || col0 >= C) {  // warp-uniform
+            if constexpr (kExt) release_stage();
+            continue;
+        }
 
         const int64_t c8 = col0 + 8 * lj;  // first column of this lane
         const bool cval = c8 < C;          // C % 32 == 0: 8-column chunks are all-in or all-out
@@ -417,7 +428,8 @@ __global__ void __launch_bounds__(kQThreads, kExt ? 1 : 2)
             // Stability variants: fp32 values; optionally a Hadamard transform of every block of 32
             // along the copy's axis, y = c * H * (D x) (signs D, butterflies h = 1, 2, 4 inside the
             // lane, h = 8, 16 across lanes, in that order); codes by round-to-nearest-even or by
-            // stochastic rounding with per-element Philox words.
+            // stochastic rounding with per-element Philox words.  Rows (row copy) and columns
+            // (column copy) are processed 4 at a time to keep the fp32 values in registers.
             const bool sr = p.opts & MXFP8_OPT_STOCHASTIC;
             const uint32_t dsign = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)p.seed,
                                                  (uint32_t)(p.seed >> 32)).x;
@@ -425,165 +437,180 @@ __global__ void __launch_bounds__(kQThreads, kExt ? 1 : 2)
                 return sr ? e4m3_sr(z0, r0) | (e4m3_sr(z1, r1) << 8) : cvt_e4m3x2(z0, z1);
             };
             if constexpr (kRow) {
-                float y[8][8];
-#pragma unroll
-                for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) { y[rr][2 * k] = bf16lo(v[rr][k]); y[rr][2 * k + 1] = bf16hi(v[rr][k]); }
-                if (p.opts & MXFP8_OPT_HADAMARD_ROW) {
-                    // block position of (rr, c): 8 * (lj & 3) + c
-#pragma unroll
-                    for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            if ((dsign >> (8 * (lj & 3) + c)) & 1u) y[rr][c] = -y[rr][c];
-#pragma unroll
-                    for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                if ((c & h) == 0) {
-                                    const float a = y[rr][c], bb = y[rr][c + h];
-                                    y[rr][c] = a + bb;
-                                    y[rr][c + h] = a - bb;
-                                }
-#pragma unroll
-                    for (int m = 1; m <= 2; m <<= 1) {
-                        const bool upper = lane & m;
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const float o = __shfl_xor_sync(0xffffffffu, y[rr][c], m);
-                                y[rr][c] = upper ? o - y[rr][c] : y[rr][c] + o;
-                            }
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) y[rr][c] *= kRhtScale;
-                }
                 uint32_t s8[8];
-#pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) m = max(m, __float_as_uint(y[rr][c]) & 0x7FFFFFFFu);
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    s8[rr] = e8m0_from_f32bits(m);
-                }
                 uint8_t* qb = p.q_row + b * R * C;
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    const int64_t row = row0 + 8 * li + rr;
-                    const float f = inv_scale_from_e8m0(s8[rr]);
-                    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
-                    if (sr && row < R) {
-                        w0 = sr_words4((uint64_t)(row * C + c8), 0u, p.seed);
-                        w1 = sr_words4((uint64_t)(row * C + c8 + 4), 0u, p.seed);
-                    }
-                    uint2 q;
-                    q.x = code2(y[rr][0] * f, y[rr][1] * f, w0.x, w0.y) | (code2(y[rr][2] * f, y[rr][3] * f, w0.z, w0.w) << 16);
-                    q.y = code2(y[rr][4] * f, y[rr][5] * f, w1.x, w1.y) | (code2(y[rr][6] * f, y[rr][7] * f, w1.z, w1.w) << 16);
-                    if (s8[rr] == 0xFFu) {
-                        uint32_t sg[2] = {0u, 0u};
+                for (int hr = 0; hr < 2; ++hr) {
+                    float y[4][8];
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) sg[c >> 2] |= ((__float_as_uint(y[rr][c]) >> 24) & 0x80u) << (8 * (c & 3));
-                        q.x = 0x7F7F7F7Fu | sg[0];
-                        q.y = 0x7F7F7F7Fu | sg[1];
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(src + (4 * hr + i) * 256);
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            y[i][2 * k] = bf16lo(w[k]);
+                            y[i][2 * k + 1] = bf16hi(w[k]);
+                        }
                     }
-                    if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
+                    if (p.opts & MXFP8_OPT_HADAMARD_ROW) {
+                        // block position of (row, c): 8 * (lj & 3) + c
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                if ((dsign >> (8 * (lj & 3) + c)) & 1u) y[i][c] = -y[i][c];
+#pragma unroll
+                        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    if ((c & h) == 0) {
+                                        const float a = y[i][c], bb = y[i][c + h];
+                                        y[i][c] = a + bb;
+                                        y[i][c + h] = a - bb;
+                                    }
+#pragma unroll
+                        for (int m = 1; m <= 2; m <<= 1) {
+                            const bool upper = lane & m;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    const float o = __shfl_xor_sync(0xffffffffu, y[i][c], m);
+                                    y[i][c] = upper ? o - y[i][c] : y[i][c] + o;
+                                }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) y[i][c] *= kRhtScale;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t m = 0;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) m = max(m, __float_as_uint(y[i][c]) & 0x7FFFFFFFu);
+                        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                        s8[4 * hr + i] = e8m0_from_f32bits(m);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t sc = s8[4 * hr + i];
+                        const int64_t row = row0 + 8 * li + 4 * hr + i;
+                        const float f = inv_scale_from_e8m0(sc);
+                        uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                        if (sr && row < R) {
+                            w0 = sr_words4((uint64_t)(row * C + c8), 0u, p.seed);
+                            w1 = sr_words4((uint64_t)(row * C + c8 + 4), 0u, p.seed);
+                        }
+                        uint2 q;
+                        q.x = code2(y[i][0] * f, y[i][1] * f, w0.x, w0.y) | (code2(y[i][2] * f, y[i][3] * f, w0.z, w0.w) << 16);
+                        q.y = code2(y[i][4] * f, y[i][5] * f, w1.x, w1.y) | (code2(y[i][6] * f, y[i][7] * f, w1.z, w1.w) << 16);
+                        if (sc == 0xFFu) {
+                            uint32_t sg[2] = {0u, 0u};
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) sg[c >> 2] |= ((__float_as_uint(y[i][c]) >> 24) & 0x80u) << (8 * (c & 3));
+                            q.x = 0x7F7F7F7Fu | sg[0];
+                            q.y = 0x7F7F7F7Fu | sg[1];
+                        }
+                        if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
+                    }
                 }
                 if (cval) store_row_scales(s8);
             }
             if constexpr (kCol) {
-                float y[8][8];
-#pragma unroll
-                for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) { y[rr][2 * k] = bf16lo(v[rr][k]); y[rr][2 * k + 1] = bf16hi(v[rr][k]); }
-                if (p.opts & MXFP8_OPT_HADAMARD_COL) {
-                    // block position of (rr, c): 8 * li + rr
-#pragma unroll
-                    for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            if ((dsign >> (8 * li + rr)) & 1u) y[rr][c] = -y[rr][c];
-#pragma unroll
-                    for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr)
-                            if ((rr & h) == 0)
-#pragma unroll
-                                for (int c = 0; c < 8; ++c) {
-                                    const float a = y[rr][c], bb = y[rr + h][c];
-                                    y[rr][c] = a + bb;
-                                    y[rr + h][c] = a - bb;
-                                }
-#pragma unroll
-                    for (int m = 8; m <= 16; m <<= 1) {
-                        const bool upper = lane & m;
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const float o = __shfl_xor_sync(0xffffffffu, y[rr][c], m);
-                                y[rr][c] = upper ? o - y[rr][c] : y[rr][c] + o;
-                            }
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) y[rr][c] *= kRhtScale;
-                }
                 uint32_t sc[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) m = max(m, __float_as_uint(y[rr][c]) & 0x7FFFFFFFu);
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                    sc[c] = e8m0_from_f32bits(m);
-                }
-                // random words of the lane's elements for the column copy, [row][column]
-                uint32_t rw[8][8];
-#pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
-                    const int64_t row = row0 + 8 * li + rr;
-                    if (sr && row < R) {
-                        w0 = sr_words4((uint64_t)(row * C + c8), 1u, p.seed);
-                        w1 = sr_words4((uint64_t)(row * C + c8 + 4), 1u, p.seed);
-                    }
-                    rw[rr][0] = w0.x; rw[rr][1] = w0.y; rw[rr][2] = w0.z; rw[rr][3] = w0.w;
-                    rw[rr][4] = w1.x; rw[rr][5] = w1.y; rw[rr][6] = w1.z; rw[rr][7] = w1.w;
-                }
                 uint8_t* qb = p.q_col + b * R * C;
-                if (cval) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float f = inv_scale_from_e8m0(sc[c]);
-                        uint2 q;
-                        q.x = code2(y[0][c] * f, y[1][c] * f, rw[0][c], rw[1][c]) |
-                              (code2(y[2][c] * f, y[3][c] * f, rw[2][c], rw[3][c]) << 16);
-                        q.y = code2(y[4][c] * f, y[5][c] * f, rw[4][c], rw[5][c]) |
-                              (code2(y[6][c] * f, y[7][c] * f, rw[6][c], rw[7][c]) << 16);
-                        if (sc[c] == 0xFFu) {
+                for (int hc = 0; hc < 2; ++hc) {
+                    float y[8][4];  // columns 4hc .. 4hc+3 of the lane
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        const uint2 u = *reinterpret_cast<const uint2*>(src + rr * 256 + 8 * hc);
+                        y[rr][0] = bf16lo(u.x);
+                        y[rr][1] = bf16hi(u.x);
+                        y[rr][2] = bf16lo(u.y);
+                        y[rr][3] = bf16hi(u.y);
+                    }
+                    if (p.opts & MXFP8_OPT_HADAMARD_COL) {
+                        // block position of (rr, column): 8 * li + rr
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr)
+                            if ((dsign >> (8 * li + rr)) & 1u)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) y[rr][j] = -y[rr][j];
+#pragma unroll
+                        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                            for (int rr = 0; rr < 8; ++rr)
+                                if ((rr & h) == 0)
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        const float a = y[rr][j], bb = y[rr + h][j];
+                                        y[rr][j] = a + bb;
+                                        y[rr + h][j] = a - bb;
+                                    }
+#pragma unroll
+                        for (int m = 8; m <= 16; m <<= 1) {
+                            const bool upper = lane & m;
+#pragma unroll
+                            for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const float o = __shfl_xor_sync(0xffffffffu, y[rr][j], m);
+                                    y[rr][j] = upper ? o - y[rr][j] : y[rr][j] + o;
+                                }
+                        }
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) y[rr][j] *= kRhtScale;
+                    }
+                    float f[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t m = 0;
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr) m = max(m, __float_as_uint(y[rr][j]) & 0x7FFFFFFFu);
+                        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                        m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                        sc[4 * hc + j] = e8m0_from_f32bits(m);
+                        f[j] = inv_scale_from_e8m0(sc[4 * hc + j]);
+                    }
+                    // codes of the 4 columns, two rows at a time (the words of a row cover its 4 columns)
+                    uint32_t qc[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+#pragma unroll
+                    for (int rr = 0; rr < 8; rr += 2) {
+                        const int64_t row = row0 + 8 * li + rr;
+                        uint4 wa = make_uint4(0, 0, 0, 0), wb = wa;
+                        if (sr && row < R) {
+                            wa = sr_words4((uint64_t)(row * C + c8 + 4 * hc), 1u, p.seed);
+                            wb = sr_words4((uint64_t)((row + 1) * C + c8 + 4 * hc), 1u, p.seed);
+                        }
+                        const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            qc[j][rr >> 2] |= code2(y[rr][j] * f[j], y[rr + 1][j] * f[j], ra[j], rb[j]) << (8 * (rr & 3));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint2 q = make_uint2(qc[j][0], qc[j][1]);
+                        if (sc[4 * hc + j] == 0xFFu) {
                             uint32_t sg[2] = {0u, 0u};
 #pragma unroll
                             for (int rr = 0; rr < 8; ++rr)
-                                sg[rr >> 2] |= ((__float_as_uint(y[rr][c]) >> 24) & 0x80u) << (8 * (rr & 3));
+                                sg[rr >> 2] |= ((__float_as_uint(y[rr][j]) >> 24) & 0x80u) << (8 * (rr & 3));
                             q.x = 0x7F7F7F7Fu | sg[0];
                             q.y = 0x7F7F7F7Fu | sg[1];
                         }
-                        *reinterpret_cast<uint2*>(qb + (c8 + c) * R + row0 + 8 * li) = q;
+                        if (cval) *reinterpret_cast<uint2*>(qb + (c8 + 4 * hc + j) * R + row0 + 8 * li) = q;
                     }
-                    store_col_scales(sc);
                 }
+                if (cval) store_col_scales(sc);
             }
+            release_stage();
             continue;
         }
 
@@ -778,12 +805,12 @@ static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t
     }
 }
 
-// The stability variants (one CTA per SM: fp32 working values need the registers).
+// The stability variants.
 static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStream_t st) {
     if (p.ntiles == 0) return MXFP8_OK;
     CUtensorMap m;
     if (!make_x_map(&m, p)) return MXFP8_ERR_DRIVER;
-    const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms());
+    const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms() * 2);
     switch (dirs) {
         case MXFP8_ROW: return launch_dirs<MXFP8_ROW, true>(m, p, grid, st);
         case MXFP8_COL: return launch_dirs<MXFP8_COL, true>(m, p, grid, st);
