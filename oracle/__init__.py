@@ -79,6 +79,9 @@ def lib():
         L.oracle_e4m3_encode_sr.restype = ctypes.c_uint8
         L.oracle_rht_signs.argtypes = [ctypes.c_uint64, P]
         L.oracle_rht32.argtypes = [P, P, P]
+        L.oracle_quantize_block_at.argtypes = [P, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint, ctypes.c_uint64,
+                                               ctypes.c_uint32, P]
+        L.oracle_quantize_block_at.restype = ctypes.c_uint8
         L.oracle_quantize_rows_opts.argtypes = [P, I64, I64, ctypes.c_uint, ctypes.c_uint64, P, P]
         L.oracle_quantize_cols_opts.argtypes = [P, I64, I64, ctypes.c_uint, ctypes.c_uint64, P, P]
         _lib = L
@@ -354,3 +357,13 @@ def quantize_cols_opts(x_u16, opts: int, seed: int):
     sT = np.empty((C, R // 32), np.uint8)
     lib().oracle_quantize_cols_opts(_p(x), R, C, opts, seed, _p(qT), _p(sT))
     return qT, sT
+
+
+def quantize_block_at(x32_u16, n0: int, nstride: int, opts: int, seed: int, direction: int):
+    """One block of 32 bf16 values, element i at input index n0 + i * nstride, quantized with
+    options for copy `direction` (0 row-wise, 1 column-wise): (codes [32], scale byte)."""
+    x = _u16(x32_u16).reshape(-1)
+    assert x.size == 32
+    q = np.empty(32, np.uint8)
+    s_ = lib().oracle_quantize_block_at(_p(x), n0, nstride, opts, seed, direction, _p(q))
+    return q, int(s_)

@@ -436,6 +436,14 @@ static uint8_t quantize_block_opts(const uint16_t* x, int64_t xstride, uint64_t 
     return quantize_block_f64_rw(v, BLK, q, qstride, (opts & 1u) ? rw : NULL);
 }
 
+/* One block of 32 contiguous bf16 values whose element i has input index n0 + i * nstride,
+ * quantized with options for copy `dir`: 32 codes into q32, returns the scale byte (for
+ * checking single blocks of a large tensor). */
+uint8_t oracle_quantize_block_at(const uint16_t* x32, uint64_t n0, uint64_t nstride, unsigned opts, uint64_t seed,
+                                 uint32_t dir, uint8_t* q32) {
+    return quantize_block_opts(x32, 1, n0, nstride, opts, seed, dir, q32, 1);
+}
+
 /* Row-wise quantization of x[R, C] with options (see quantize_block_opts). */
 void oracle_quantize_rows_opts(const uint16_t* x, int64_t R, int64_t C, unsigned opts, uint64_t seed, uint8_t* q,
                                uint8_t* s) {

@@ -139,3 +139,41 @@ def test_composite_with_stability_options(mx):
     torch.cuda.synchronize()
     rel = lambda got: np.linalg.norm(f64(got) - exact) / np.linalg.norm(exact)
     assert rel(Wg.grad) < max(2.0 * rel(Wp.grad), 0.02), (rel(Wg.grad), rel(Wp.grad))
+
+
+def test_full_size_grouped_sampled(mx):
+    """The Scout activations' shape [16384, 5120] with its 8 token groups, every option at once
+    (stochastic rounding, Hadamard on both copies), sampled blocks against the oracle."""
+    sizes = synth.scout_group_sizes(0)
+    M, K = 16384, 5120
+    x = synth.log_uniform_rows(M, K, seed=3, device="cuda")
+    ends = sizes_to_ends(sizes)
+    starts = np.concatenate([[0], ends[:-1]])
+    offs = torch.tensor(ends.astype(np.int32), device="cuda")
+    opts = mx.OPT_STOCHASTIC | mx.OPT_HADAMARD_ROW | mx.OPT_HADAMARD_COL
+    st = mx.new_status()
+    q, s, qT, sT = mx.mxfp8_quantize_2d(x, mx.ROW | mx.COL, mx.SCALES_BLOCKED, offs, st, opts=opts, seed=SEED)
+    mx.read_status(st)
+    o_opts = oracle.OPT_SR | oracle.OPT_RHT
+    padded = np.concatenate([[0], np.cumsum([-(-int(m) // 128) * 128 for m in sizes])])
+    group_of = lambda r: int(np.searchsorted(ends, r, side="right"))
+    rng = np.random.default_rng(8)
+    rows = np.unique(np.concatenate([rng.integers(0, M, 24), ends[np.array(sizes) > 0] - 1]))
+    for r in rows:
+        g = group_of(int(r))
+        pr = padded[g] + int(r) - starts[g]
+        for b in rng.integers(0, K // 32, 3):
+            qo, so = oracle.quantize_block_at(u16(x[r, 32 * b:32 * b + 32]), int(r) * K + 32 * int(b), 1, o_opts, SEED, 0)
+            assert np.array_equal(u8(q[r, 32 * b:32 * b + 32]), qo)
+            assert int(s[oracle.blocked_offset(int(pr), int(b), K // 128)].item()) == so
+    ct = int(padded[-1]) // 128
+    for c in rng.integers(0, K, 12):
+        g = int(rng.integers(0, len(sizes)))
+        if sizes[g] == 0:
+            continue
+        t0 = int(starts[g]) + 32 * int(rng.integers(0, sizes[g] // 32))
+        qo, so = oracle.quantize_block_at(np.ascontiguousarray(u16(x[t0:t0 + 32, c])), t0 * K + int(c), K, o_opts,
+                                          SEED, 1)
+        assert np.array_equal(u8(qT[c, t0:t0 + 32]), qo)
+        cq = padded[g] // 32 + (t0 - starts[g]) // 32
+        assert int(sT[oracle.blocked_offset(int(c), int(cq), ct)].item()) == so

@@ -211,3 +211,77 @@ def test_fused_equals_unfused_gpu_path(mx):
     n_col = oracle.blocked_colgroups_bytes(H, ends)
     assert (u8(s)[:n_row] == u8(hs)[:n_row]).mean() >= 0.999
     assert (u8(sT)[:n_col] == u8(hTs)[:n_col]).mean() >= 0.999
+
+
+def test_full_size_sampled(mx):
+    """The SwiGLU expert's full gate/up shape (G=2, M=65600 as 39360 + 26240, D=5120, H=8192) in
+    the launch configuration the bench times, sampled: row blocks of h (including the first and
+    last row of each group) and token blocks of h^T, against the oracle's stage computed from the
+    oracle's own dot products, with the random-input bars above."""
+    s = synth.workload("swiglu", seed=0, device="cuda")
+    x, Wg, Wu, sizes = s["x"], s["Wg"], s["Wu"], s["sizes"]
+    M, D, H = s["M"], s["D"], s["H"]
+    ends = sizes_to_ends(sizes)
+    starts = np.concatenate([[0], ends[:-1]])
+    padded = np.concatenate([[0], np.cumsum([-(-int(m) // 128) * 128 for m in sizes])])
+    (h1, h3, hq, hs, hTq, hTs), status = run_fused(mx, x, Wg, Wu, sizes)
+    mx.read_status(status)
+    rng = np.random.default_rng(12)
+    xc, Wgc, Wuc = x.cpu(), Wg.cpu(), Wu.cpu()   # sampled rows are sliced on the host
+    qx = {}
+
+    def xrow(r):
+        if r not in qx:
+            qx[r] = oracle.quantize_rows(u16(xc[r:r + 1]))
+        return qx[r]
+
+    def h_oracle(r, g, cols):
+        """The oracle's h1, h3 (fp64) and h (bf16 patterns) at row r, columns `cols`."""
+        qa, sa = xrow(r)
+        out = []
+        for W in (Wgc, Wuc):
+            qw, sw = oracle.quantize_rows(u16(W[g, cols[0]:cols[-1] + 1]))
+            out.append(np.array([oracle.dot(qa[0], sa[0], qw[i], sw[i]) for i in range(len(cols))]))
+        b1, b3 = oracle.bf16_from_f64(out[0]), oracle.bf16_from_f64(out[1])
+        return out[0], out[1], oracle.swiglu_bf16(b1, b3)
+
+    ref13, got13 = [], []
+    q_o, q_g, s_o, s_g = [], [], [], []
+    rows = np.unique(np.concatenate([rng.integers(0, M, 10), starts, ends - 1]))
+    for r in rows:
+        r = int(r)
+        g = int(np.searchsorted(ends, r, side="right"))
+        j = int(rng.integers(0, H // 32))
+        cols = list(range(32 * j, 32 * j + 32))
+        o1, o3, h = h_oracle(r, g, cols)
+        ref13 += [o1, o3]
+        got13 += [f64(h1[r, 32 * j:32 * j + 32]), f64(h3[r, 32 * j:32 * j + 32])]
+        qo, so = oracle.quantize_vec(h)
+        q_o.append(qo)
+        s_o.append(so[0])
+        q_g.append(u8(hq[r, 32 * j:32 * j + 32]))
+        pr = int(padded[g]) + r - int(starts[g])
+        s_g.append(int(hs[oracle.blocked_offset(pr, j, H // 128)].item()))
+    # token blocks of h^T: column c, 32 tokens of one group
+    ct = int(padded[-1]) // 128
+    for _ in range(6):
+        g = int(rng.integers(0, len(sizes)))
+        t0 = int(starts[g]) + 32 * int(rng.integers(0, sizes[g] // 32))
+        c = int(rng.integers(0, H))
+        hcol = np.array([h_oracle(t, g, [c])[2][0] for t in range(t0, t0 + 32)], np.uint16)
+        qo, so = oracle.quantize_vec(hcol)
+        q_o.append(qo)
+        s_o.append(so[0])
+        q_g.append(u8(hTq[c, t0:t0 + 32]))
+        cq = int(padded[g]) // 32 + (t0 - int(starts[g])) // 32
+        s_g.append(int(hTs[oracle.blocked_offset(c, cq, ct)].item()))
+    assert_gemm_close(np.concatenate(got13), np.concatenate(ref13), what="h1/h3 sampled")
+    q_o, q_g = np.stack(q_o), np.stack(q_g)
+    s_o, s_g = np.array(s_o), np.array(s_g)
+    tab = oracle.e4m3_table()
+    dg = tab[q_g] * np.ldexp(1.0, s_g.astype(np.int64) - 127)[:, None]
+    do = tab[q_o] * np.ldexp(1.0, s_o.astype(np.int64) - 127)[:, None]
+    smax = np.maximum(s_g, s_o)[:, None].repeat(32, axis=1)
+    assert np.all(np.abs(s_g.astype(int) - s_o.astype(int)) <= 1)
+    assert np.all(np.abs(dg - do) <= e4m3_step(np.maximum(np.abs(dg), np.abs(do)), smax))
+    assert (q_g == q_o).mean() >= 0.99 and (s_g == s_o).mean() >= 0.95

@@ -118,3 +118,60 @@ def test_composite_with_block32_weights(mx):
     dTq, dTs = oracle.quantize_cols(u16(dO))
     aTq, aTs = oracle.quantize_cols(u16(A))
     assert_gemm_close(f64(Wg.grad), oracle.grouped_mm_wgrad(dTq, dTs, aTq, aTs, ends), what="dW")
+
+
+def test_full_size_block32_sampled(mx):
+    """The Scout expert weights [8, 8192, 5120] with 32x32 blocks, sampled blocks of both copies
+    against the oracle, and sampled forward / dgrad outputs on those weights."""
+    w = synth.workload("scout", seed=0, device="cuda")
+    W, A, D, sizes = w["W"], w["A"], w["dOut"], w["sizes"]
+    G, N, K, M = w["G"], w["N"], w["K"], w["M"]
+    st = mx.new_status()
+    wq, ws, wTq, wTs = mx.mxfp8_quantize_3d_experts(W, mx.ROW | mx.COL | mx.BLOCK32X32, mx.SCALES_BLOCKED, st)
+    mx.read_status(st)
+    rng = np.random.default_rng(13)
+    Wc = W.cpu()                       # sampled blocks are sliced on the host
+    for _ in range(12):
+        g, bn, bk = int(rng.integers(0, G)), int(rng.integers(0, N // 32)), int(rng.integers(0, K // 32))
+        qo, so = oracle.quantize_32x32(u16(Wc[g, 32 * bn:32 * bn + 32, 32 * bk:32 * bk + 32]))
+        assert np.array_equal(u8(wq[g, 32 * bn:32 * bn + 32, 32 * bk:32 * bk + 32]), qo)
+        assert np.array_equal(u8(wTq[g, 32 * bk:32 * bk + 32, 32 * bn:32 * bn + 32]), qo.T)
+        for i in (0, 17, 31):
+            assert int(ws[g, oracle.blocked_offset(32 * bn + i, bk, K // 128)].item()) == so[0, 0]
+            assert int(wTs[g, oracle.blocked_offset(32 * bk + i, bn, N // 128)].item()) == so[0, 0]
+    offs = w["offs"].cuda()
+    ends = sizes_to_ends(sizes)
+    aq, as_, _, _ = mx.mxfp8_quantize_2d(A, mx.ROW, mx.SCALES_BLOCKED, offs, st)
+    dq, ds, _, _ = mx.mxfp8_quantize_2d(D, mx.ROW, mx.SCALES_BLOCKED, offs, st)
+    out = mx.mxfp8_grouped_mm_fwd(aq, as_, wq, ws, offs, dev_status=st)
+    dA = mx.mxfp8_grouped_mm_dgrad(dq, ds, wTq, wTs, offs, dev_status=st)
+    mx.read_status(st)
+    ref, got, refd, gotd = [], [], [], []
+    for r in rng.integers(0, M, 8):
+        r = int(r)
+        g = int(np.searchsorted(ends, r, side="right"))
+        qa, sa = oracle.quantize_rows(u16(A[r:r + 1]))
+        qd, sd = oracle.quantize_rows(u16(D[r:r + 1]))
+        for bn in rng.integers(0, N // 32, 2):
+            blk_q, blk_s = [], []
+            for bk in range(K // 32):   # the 32 rows n of W[g] in block-row bn, all of K
+                q32, s32 = oracle.quantize_32x32(u16(Wc[g, 32 * bn:32 * bn + 32, 32 * bk:32 * bk + 32]))
+                blk_q.append(q32)
+                blk_s.append(s32[0, 0])
+            qrows = np.concatenate(blk_q, axis=1)                      # [32, K]
+            srows = np.tile(np.array(blk_s, np.uint8), (32, 1))         # [32, K/32]
+            n = int(rng.integers(0, 32))
+            ref.append(oracle.dot(qa[0], sa[0], qrows[n], srows[n]))
+            got.append(float(out[r, 32 * int(bn) + n].item()))
+        # dgrad: dA[r, k] = sum_n dOut[r, n] W[g][n, k], column k of W through its 32x32 blocks
+        k = int(rng.integers(0, K))
+        bk = k // 32
+        col_q, col_s = [], []
+        for bn in range(N // 32):
+            q32, s32 = oracle.quantize_32x32(u16(Wc[g, 32 * bn:32 * bn + 32, 32 * bk:32 * bk + 32]))
+            col_q.append(q32[:, k - 32 * bk])
+            col_s.append(s32[0, 0])
+        refd.append(oracle.dot(qd[0], sd[0], np.concatenate(col_q), np.array(col_s, np.uint8)))
+        gotd.append(float(dA[r, k].item()))
+    assert_gemm_close(np.array(got), np.array(ref), what="fwd sampled on 32x32 weights")
+    assert_gemm_close(np.array(gotd), np.array(refd), what="dgrad sampled on 32x32 weights")

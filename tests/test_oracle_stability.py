@@ -137,3 +137,18 @@ def test_options_reduce_and_transpose():
     q2, s2 = oracle.quantize_rows_opts(x, oracle.OPT_SR, 9)
     assert np.array_equal(s2, s)
     assert np.all(np.abs(E[q2 & 0x7F] - E[q & 0x7F]) <= np.maximum(E[q & 0x7F] / 8, 2.0 ** -9) + 1e-12)
+
+
+def test_block_at_matches_the_tensor_routines():
+    rng = np.random.default_rng(6)
+    x = bf16(rng.standard_normal((64, 96)))
+    for opts in (0, oracle.OPT_SR, oracle.OPT_RHT, oracle.OPT_SR | oracle.OPT_RHT):
+        q, s = oracle.quantize_rows_opts(x, opts, 77)
+        qT, sT = oracle.quantize_cols_opts(x, opts, 77)
+        for r, b in ((0, 0), (5, 1), (63, 2)):
+            qb, sb = oracle.quantize_block_at(x[r, 32 * b:32 * b + 32], r * 96 + 32 * b, 1, opts, 77, 0)
+            assert np.array_equal(qb, q[r, 32 * b:32 * b + 32]) and sb == s[r, b]
+        for c, b in ((0, 0), (7, 1), (95, 1)):
+            qc, sc = oracle.quantize_block_at(np.ascontiguousarray(x[32 * b:32 * b + 32, c]), 32 * b * 96 + c, 96,
+                                              opts, 77, 1)
+            assert np.array_equal(qc, qT[c, 32 * b:32 * b + 32]) and sc == sT[c, b]
