@@ -72,6 +72,7 @@ def lib():
         L.oracle_bf16_from_f64.restype = ctypes.c_uint16
         L.oracle_bf16_from_f64_array.argtypes = [P, I64, P]
         L.oracle_swiglu_bf16.argtypes = [P, P, I64, P]
+        L.oracle_swiglu_bwd_bf16.argtypes = [P, P, P, I64, P, P]
         L.oracle_philox4x32_10.argtypes = [P, P, P]
         L.oracle_sr_word.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
         L.oracle_sr_word.restype = ctypes.c_uint32
@@ -278,6 +279,28 @@ def swiglu_bf16(h1, h3) -> np.ndarray:
     assert h1.shape == h3.shape
     out = np.empty(h1.shape, np.uint16)
     lib().oracle_swiglu_bf16(_p(h1), _p(h3), h1.size, _p(out))
+    return out
+
+
+def swiglu_bwd_bf16(dh, h1, h3):
+    """(dh1, dh3) of h = silu(h1) * h3 at the rounding points of the bf16 autograd ops (uint16 patterns)."""
+    dh, h1, h3 = _u16(dh), _u16(h1), _u16(h3)
+    assert dh.shape == h1.shape == h3.shape
+    dh1 = np.empty(dh.shape, np.uint16)
+    dh3 = np.empty(dh.shape, np.uint16)
+    lib().oracle_swiglu_bwd_bf16(_p(dh), _p(h1), _p(h3), dh.size, _p(dh1), _p(dh3))
+    return dh1, dh3
+
+
+def swiglu_bwd_quantized(dh, h1, h3) -> dict:
+    """The SwiGLU backward stage followed by the quantization of dh1 and dh3 along the row (the
+    gate/up dgrads' contraction H) and along the tokens (their wgrads): compact scales."""
+    dh1, dh3 = swiglu_bwd_bf16(dh, h1, h3)
+    out = dict(dh1=dh1, dh3=dh3)
+    for name, t in (("dh1", dh1), ("dh3", dh3)):
+        out[name + "_q"], out[name + "_s"] = quantize_rows(t)
+        if t.shape[0] % 32 == 0:
+            out[name + "T_q"], out[name + "T_s"] = quantize_cols(t)
     return out
 
 

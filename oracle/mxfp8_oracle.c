@@ -513,6 +513,23 @@ void oracle_swiglu_bf16(const uint16_t* h1, const uint16_t* h3, int64_t n, uint1
     }
 }
 
+/* Backward of h = silu(h1) * h3 with the rounding points of the bf16 autograd ops, all
+ * values bf16 patterns, arithmetic in fp64 with one rounding per op:
+ *   dh3 = bf16(dh * bf16(silu(h1)))
+ *   dh1 = bf16(bf16(dh * h3) * sig * (1 + h1 * (1 - sig))),  sig = 1 / (1 + e^-h1)
+ * (the derivative of silu(x) = x * sig(x) is sig * (1 + x * (1 - sig))). */
+void oracle_swiglu_bwd_bf16(const uint16_t* dh, const uint16_t* h1, const uint16_t* h3, int64_t n, uint16_t* dh1,
+                            uint16_t* dh3) {
+    for (int64_t i = 0; i < n; ++i) {
+        double g = oracle_bf16_to_f64(dh[i]), a = oracle_bf16_to_f64(h1[i]), u = oracle_bf16_to_f64(h3[i]);
+        double sig = 1.0 / (1.0 + exp(-a));
+        double silu = oracle_bf16_to_f64(oracle_bf16_from_f64(a * sig));
+        dh3[i] = oracle_bf16_from_f64(g * silu);
+        double dsilu = oracle_bf16_to_f64(oracle_bf16_from_f64(g * u));
+        dh1[i] = oracle_bf16_from_f64(dsilu * sig * (1.0 + a * (1.0 - sig)));
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);

@@ -1,6 +1,7 @@
-"""Pins of the oracle's SwiGLU stage (no GPU): the fp64 -> bf16 rounding and
-h = bf16(bf16(silu(h1)) * h3), each checked against something other than itself
-(torch's fp32 -> bf16 cast, torch's fp64 silu, hand-worked values)."""
+"""Pins of the oracle's SwiGLU stage (no GPU): the fp64 -> bf16 rounding,
+h = bf16(bf16(silu(h1)) * h3) and its backward (dh1, dh3), each checked against something
+other than itself (torch's fp32 -> bf16 cast, torch's fp64 silu and silu_backward, hand-worked
+values)."""
 import numpy as np
 import pytest
 import torch
@@ -96,3 +97,35 @@ def test_swiglu_gate_up_reduces_to_the_parts():
     assert np.array_equal(o["h_q"], q) and np.array_equal(o["h_s"], s)
     qT, sT = oracle.quantize_cols(o["h"])
     assert np.array_equal(o["hT_q"], qT) and np.array_equal(o["hT_s"], sT)
+
+
+def test_swiglu_backward_against_torch_autograd_ops():
+    # fp64 torch ops restate the same derivative; the oracle rounds once per op, so on inputs
+    # whose fp64 results round the same either way the patterns agree exactly
+    rng = np.random.default_rng(7)
+    n = 4096
+    b16 = lambda a: oracle.bf16_from_f64(a)
+    h1 = b16(rng.standard_normal(n) * 3)
+    h3 = b16(rng.standard_normal(n))
+    dh = b16(rng.standard_normal(n) * 1e-2)
+    f = lambda u: torch.from_numpy((u.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    t1, t3, tg = f(h1), f(h3), f(dh)
+    silu = f(b16(torch.nn.functional.silu(t1).numpy()))
+    want3 = b16((tg * silu).numpy())
+    dsilu = f(b16((tg * t3).numpy()))
+    want1 = b16(torch.ops.aten.silu_backward(dsilu, t1).numpy())
+    got1, got3 = oracle.swiglu_bwd_bf16(dh, h1, h3)
+    assert np.array_equal(got3, want3)
+    assert (got1 == want1).mean() > 0.999   # silu_backward's fp64 evaluation order differs from the oracle's
+
+
+def test_swiglu_backward_hand_values():
+    b = lambda v: oracle.bf16_from_f64(np.array([v], np.float64))
+    one = lambda dh, a, u: [int(x[0]) for x in oracle.swiglu_bwd_bf16(b(dh), b(a), b(u))]
+    # h1 = 0: sig = 1/2, silu = 0, silu' = 1/2 -> dh1 = bf16(dh * h3) / 2, dh3 = 0
+    assert one(1.0, 0.0, 3.0) == [int(b(1.5)[0]), 0x0000]
+    # large h1: silu(h1) = h1, silu' = 1 -> dh1 = dh * h3, dh3 = dh * h1
+    assert one(0.5, 100.0, 2.0) == [int(b(1.0)[0]), int(b(50.0)[0])]
+    # very negative h1: silu and its derivative vanish
+    d1, d3 = one(1.0, -200.0, 3.0)
+    assert (d1 & 0x7FFF) == 0 and (d3 & 0x7FFF) == 0
