@@ -54,9 +54,9 @@ WORKLOAD_TEXT = {
                   "groups 0/7/15 empty, 1% x100 activation outliers",
     "swiglu": "SwiGLU routed expert fwd+bwd: G=2, M=65600 (39360/26240), D=5120, H=8192, gate/up W[2,8192,5120], "
               "down W[2,5120,8192]; gate/up GEMMs with the SwiGLU and its MXFP8 quantization fused into the "
-              "epilogue, 9 GEMMs, SwiGLU backward in torch bf16",
-    "swiglu_unfused": "SwiGLU routed expert fwd+bwd as swiglu, with separate gate and up GEMMs, the SwiGLU in "
-                      "torch bf16 and a separate ROW|COL quantization of h",
+              "epilogue, 9 GEMMs, the SwiGLU backward and the quantization of dh1, dh3 in one kernel",
+    "swiglu_unfused": "SwiGLU routed expert fwd+bwd as swiglu, with separate gate and up GEMMs, the SwiGLU and "
+                      "its backward in torch bf16 and separate ROW|COL quantizations of h, dh1, dh3",
     "swiglu_standin": "SwiGLU routed expert GEMMs: G=2, M=65600 (39360/26240), gate/up W[2,8192,5120], "
                       "down W[2,5120,8192]; 9 grouped GEMMs, seeded stand-ins for the SwiGLU intermediates",
     "tiny": "Tiny: G=2, A[256,256], offs [128,256], W[2,128,256] (latency-bound; parity case)",
@@ -345,11 +345,13 @@ class StepGroup:
 class SwiGLUStep:
     """One fwd+bwd of the SwiGLU routed expert y = (silu(x Wg^T) * (x Wu^T)) Wd^T through the C ABI.
 
-    fused:   the gate/up GEMMs write h1, h3 and h already quantized both ways (one kernel);
-    unfused: two forward GEMMs, h = silu(h1) * h3 in torch bf16, a ROW|COL quantization of h.
-    Both then run the down GEMM, and the backward: dY quantized both ways, down dgrad and wgrad,
-    the SwiGLU backward in torch bf16 ops, dh1/dh3 quantized both ways, two dgrads (summed) and two
-    wgrads.  Entries whose name starts with "torch." are torch elementwise glue, not library kernels."""
+    fused:   the gate/up GEMMs write h1, h3 and h already quantized both ways (one kernel); in the
+             backward one kernel computes dh1, dh3 and quantizes both both ways;
+    unfused: two forward GEMMs, h = silu(h1) * h3 in torch bf16, a ROW|COL quantization of h; in the
+             backward the SwiGLU backward in torch bf16 ops and two ROW|COL quantizations.
+    Both run the down GEMM, and in the backward: dY quantized both ways, down dgrad and wgrad, two
+    dgrads (summed) and two wgrads.  Entries whose name starts with "torch." are torch elementwise
+    glue, not library kernels."""
 
     def __init__(self, s: dict, device, fused: bool):
         import mxfp8_precision_moe_gb300 as mx
@@ -416,9 +418,15 @@ class SwiGLUStep:
             ("quant_dY", L.mxfp8_quantize_2d, (dY, M, D, RC, 1, offs, G, *q(dYq), st)),
             ("dgrad_down", L.mxfp8_grouped_mm_dgrad, (*q(dYq)[:2], *q(wq["Wd"])[2:], offs, G, M, D, H, P(dh), st)),
             ("wgrad_down", L.mxfp8_grouped_mm_wgrad, (*q(dYq)[2:], *q(hq)[2:], offs, G, M, D, H, P(dWd), st)),
-            ("torch.swiglu_bwd", glue(swiglu_bwd_torch), ()),
-            ("quant_dh1", L.mxfp8_quantize_2d, (P(dh1), M, H, RC, 1, offs, G, *q(a1), st)),
-            ("quant_dh3", L.mxfp8_quantize_2d, (P(dh3), M, H, RC, 1, offs, G, *q(a3), st)),
+        ]
+        if fused:
+            calls.append(("swiglu_bwd_quant", L.mxfp8_swiglu_bwd_quantize,
+                          (P(dh), P(h1), P(h3), M, H, offs, G, *q(a1), *q(a3), st)))
+        else:
+            calls += [("torch.swiglu_bwd", glue(swiglu_bwd_torch), ()),
+                      ("quant_dh1", L.mxfp8_quantize_2d, (P(dh1), M, H, RC, 1, offs, G, *q(a1), st)),
+                      ("quant_dh3", L.mxfp8_quantize_2d, (P(dh3), M, H, RC, 1, offs, G, *q(a3), st))]
+        calls += [
             ("dgrad_gate", L.mxfp8_grouped_mm_dgrad, (*q(a1)[:2], *q(wq["Wg"])[2:], offs, G, M, H, D, P(dx), st)),
             ("dgrad_up", L.mxfp8_grouped_mm_dgrad, (*q(a3)[:2], *q(wq["Wu"])[2:], offs, G, M, H, D, P(dx2), st)),
             ("torch.add", glue(lambda: dx.add_(dx2)), ()),
@@ -433,9 +441,12 @@ class SwiGLUStep:
         self.flops = 9 * f1
         qb = lambda e: e * (2 + 1 + 1 + 2 / 32)
         self.bytes = {"quant_x": qb(M * D), "quant_Wg": qb(G * H * D), "quant_Wu": qb(G * H * D),
-                      "quant_Wd": qb(G * D * H), "quant_dY": qb(M * D), "quant_dh1": qb(M * H), "quant_dh3": qb(M * H)}
-        if not fused:
-            self.bytes["quant_h"] = qb(M * H)
+                      "quant_Wd": qb(G * D * H), "quant_dY": qb(M * D)}
+        if fused:
+            # reads dh, h1, h3; writes dh1 and dh3 codes both ways with their scales
+            self.bytes["swiglu_bwd_quant"] = M * H * (6 + 2 * (2 + 2 / 32))
+        else:
+            self.bytes.update(quant_h=qb(M * H), quant_dh1=qb(M * H), quant_dh3=qb(M * H))
         self.roofline_key = "gateup_swiglu" if fused else "fwd_gate"
         self.roofline_name = "grouped_mm_swiglu_fwd (gate+up, fused epilogue)" if fused else "grouped_mm_fwd (gate)"
 

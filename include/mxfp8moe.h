@@ -256,6 +256,29 @@ mxfp8_status_t mxfp8_grouped_mm_swiglu_fwd(const void* x_q, const void* x_s, con
                                            mxfp8_stream_t stream);
 
 /* ----------------------------------------------------------------------------
+ * mxfp8_swiglu_bwd_quantize -- the SwiGLU backward of a routed expert with the
+ * MXFP8 quantization of its two outputs fused in.  [P3] "Neutralizing
+ * quantization overhead" (fuse quantization into the producing kernel); [P4]
+ * (gate/up/down routed-expert weights).  For h = silu(h1) * h3 and its
+ * gradient dh, elementwise at the rounding points of the bf16 autograd ops:
+ *   dh3 = bf16(dh * bf16(silu(h1)))
+ *   dh1 = bf16(bf16(dh * h3) * sig * (1 + h1 * (1 - sig))),  sig = 1 / (1 + e^-h1)
+ * in fp32, then each of dh1, dh3 quantized as mxfp8_quantize_2d(MXFP8_ROW |
+ * MXFP8_COL, MXFP8_SCALES_BLOCKED, offs) does: codes [M, H] + blocked row-group
+ * scales (the gate/up dgrads) and codes [H, M] + blocked token-group scales
+ * (their wgrads).
+ * Inputs dh, h1, h3: [M, H] bf16.  M % 32 == 0, H % 32 == 0, every group size
+ * % 32 == 0 (as for the column-wise quantization); scale buffers sized by
+ * mxfp8_scale_bytes(M, H, G, MXFP8_SCALES_BLOCKED) and
+ * mxfp8_scale_bytes_colgroups(H, M, G); all pointers caller-owned device memory,
+ * 16-byte aligned.  Errors: MXFP8_ERR_NULL / _SHAPE / _ALIGN / _ARCH.
+ * ------------------------------------------------------------------------- */
+mxfp8_status_t mxfp8_swiglu_bwd_quantize(const void* dh_bf16, const void* h1_bf16, const void* h3_bf16, int64_t M,
+                                         int64_t H, const int32_t* offs, int32_t G, void* dh1_q, void* dh1_s,
+                                         void* dh1T_q, void* dh1T_s, void* dh3_q, void* dh3_s, void* dh3T_q,
+                                         void* dh3T_s, int32_t* dev_status, mxfp8_stream_t stream);
+
+/* ----------------------------------------------------------------------------
  * Sizes and checks.
  * mxfp8_scale_bytes: bytes to allocate for the scales of an operand with `rows`
  *   rows of K elements (K % 32 == 0) quantized along K, its rows split into G

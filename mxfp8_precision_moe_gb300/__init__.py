@@ -30,6 +30,7 @@ __all__ = [
     "mxfp8_grouped_mm_wgrad", "mxfp8_scale_bytes", "mxfp8_scale_bytes_colgroups", "mxfp8_check_offsets",
     "mxfp8_debug_wait_timeout", "new_status", "read_status", "to_mxfp8_then_scaled_grouped_mm", "load",
     "quantize_expert_weights", "Mxfp8WeightCache", "mxfp8_grouped_mm_swiglu_fwd", "mxfp8_swiglu_expert",
+    "mxfp8_swiglu_bwd_quantize",
 ]
 
 
@@ -210,6 +211,29 @@ def mxfp8_grouped_mm_swiglu_fwd(x_q, x_s, wg_q, wg_s, wu_q, wu_s, offs, token_wi
                                             _p(dev_status), _stream(dev))
     check(st, "mxfp8_grouped_mm_swiglu_fwd")
     return h1, h3, h_q, h_s, hT_q, hT_s
+
+
+def mxfp8_swiglu_bwd_quantize(dh, h1, h3, offs, dev_status=None):
+    """SwiGLU backward with the quantization of both outputs fused in: from dh, h1, h3
+    [M, H] bf16 returns ((dh1_q, dh1_s, dh1T_q, dh1T_s), (dh3_q, dh3_s, dh3T_q, dh3T_s)),
+    each as mxfp8_quantize_2d(ROW | COL, SCALES_BLOCKED, offs) returns it."""
+    for t in (dh, h1, h3):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.shape != dh.shape:
+            raise ValueError("mxfp8_swiglu_bwd_quantize: dh, h1, h3 must be bf16 [M, H]")
+    _cuda(dh, h1, h3, offs, dev_status)
+    M, H = dh.shape
+    G = int(offs.numel())
+    dev = dh.device
+
+    def outs():
+        return (_u8((M, H), dev), _u8((mxfp8_scale_bytes(M, H, G, SCALES_BLOCKED),), dev), _u8((H, M), dev),
+                _u8((mxfp8_scale_bytes_colgroups(H, M, G),), dev))
+
+    o1, o3 = outs(), outs()
+    st = load().mxfp8_swiglu_bwd_quantize(_p(dh), _p(h1), _p(h3), M, H, _p(offs), G, *[_p(t) for t in o1],
+                                          *[_p(t) for t in o3], _p(dev_status), _stream(dev))
+    check(st, "mxfp8_swiglu_bwd_quantize")
+    return o1, o3
 
 
 def mxfp8_check_offsets(offs: torch.Tensor, M: int, align: int, dev_status: torch.Tensor) -> None:

@@ -51,6 +51,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return (uint32_t)r;
 }
 
+// Two fp32 -> a bf16 pair (round to nearest even); lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // bf16 pair packed in a u32 -> the two fp32 values (exact).
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

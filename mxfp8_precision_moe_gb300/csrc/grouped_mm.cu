@@ -193,12 +193,6 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, co
     return ti;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 __device__ __forceinline__ void st_shared_u8(void* p, uint32_t v) {
     asm volatile("st.shared.u8 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }

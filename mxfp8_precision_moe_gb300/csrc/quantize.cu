@@ -47,7 +47,16 @@ struct QParams {
     int64_t tiles_r, tiles_c, ntiles;
     unsigned opts;       // MXFP8_OPT_* (the stability-variant kernels only)
     uint64_t seed;
+    // the fused SwiGLU backward only: x = dh, the second output set (dh3); dh1 goes to q_row.. s_col
+    uint8_t* q_row2;
+    uint8_t* s_row2;
+    uint8_t* q_col2;
+    uint8_t* s_col2;
 };
+
+// Kernel modes: plain MX quantization; the stability variants (fp32 values, Hadamard transform,
+// stochastic rounding); the fused SwiGLU backward (three inputs dh, h1, h3; two quantized outputs).
+enum QuantMode : int { kModePlain = 0, kModeExt = 1, kModeSwiBwd = 2 };
 
 // Warp 0 builds, for G groups over R rows, the clamped monotone end rows and
 // the padded start rows P[g] = sum_{h<g} ceil(size_h/128)*128 (also the scale
@@ -203,11 +212,18 @@ constexpr int kQTileBytes = 128 * 128 * 2;     // one 128 x 128 bf16 tile
 constexpr int kQThreads = 288;                 // 8 consumer warps + 1 TMA producer warp
 constexpr int kQSmem = kQStages * kQTileBytes + 128;
 
-// kExt: the stability variants of ROW / COL / ROW|COL (runtime options p.opts, seed p.seed); fp32
-// working values.
-template <unsigned DIRS, bool kExt = false>
-__global__ void __launch_bounds__(kQThreads, 2)
-    quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
+// kModeExt: the stability variants of ROW / COL / ROW|COL (runtime options p.opts, seed p.seed);
+// fp32 working values.  kModeSwiBwd (ROW|COL only): each stage holds the tiles of dh (xmap), h1
+// (xmap2) and h3 (xmap3); dh1 and dh3 are computed and each quantized both ways.
+template <unsigned DIRS, int kMode = kModePlain>
+__global__ void __launch_bounds__(kQThreads, kMode == kModeSwiBwd ? 1 : 2)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xmap2,
+                      const __grid_constant__ CUtensorMap xmap3, QParams p) {
+    constexpr bool kExt = kMode == kModeExt;
+    constexpr bool kSwiBwd = kMode == kModeSwiBwd;
+    constexpr int kNumIn = kSwiBwd ? 3 : 1;                     // input tiles per stage
+    constexpr int kStages = kSwiBwd ? 2 : kQStages;
+    constexpr uint32_t kStageBytes = kNumIn * kQTileBytes;
     constexpr bool kRow = (DIRS & MXFP8_ROW) != 0;
     constexpr bool kCol = (DIRS & MXFP8_COL) != 0;
     constexpr bool kB32 = (DIRS & MXFP8_BLOCK32X32) != 0;
@@ -235,6 +251,10 @@ __global__ void __launch_bounds__(kQThreads, 2)
         abort_s = 0;
         fence_barrier_init();
         prefetch_tmap(&xmap);
+        if (kSwiBwd) {
+            prefetch_tmap(&xmap2);
+            prefetch_tmap(&xmap3);
+        }
     }
     __syncthreads();
     volatile int* abort_flag = &abort_s;
@@ -253,7 +273,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
             uint32_t phase = 0, issued = 0, last_phase = 0;
             for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kQTimeoutNs, abort_flag, p.dev_status)) {
-                    for (int s = 0; s < kQStages; ++s)
+                    for (int s = 0; s < kStages; ++s)
                         if (issued & (1u << s)) {
                             volatile int no_abort = 0;
                             mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, kQTimeoutNs, &no_abort, nullptr);
@@ -262,12 +282,18 @@ __global__ void __launch_bounds__(kQThreads, 2)
                 }
                 const uint32_t tt = (uint32_t)t, b = tt / per_b, rem = tt - b * per_b;
                 const uint32_t tr = rem / tiles_c, tc = rem - tr * tiles_c;
-                mbar_arrive_expect_tx(&full[stage], kQTileBytes);
-                tma_load_3d(tiles + stage * kQTileBytes, &xmap, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
-                            &full[stage]);
+                mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                uint8_t* dst = tiles + stage * kStageBytes;
+                tma_load_3d(dst, &xmap, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b, &full[stage]);
+                if constexpr (kSwiBwd) {
+                    tma_load_3d(dst + kQTileBytes, &xmap2, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
+                                &full[stage]);
+                    tma_load_3d(dst + 2 * kQTileBytes, &xmap3, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
+                                &full[stage]);
+                }
                 issued |= 1u << stage;
                 last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == kQStages) { stage = 0; phase ^= 1u; }
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
         }
         return;
@@ -278,7 +304,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     //   row layout:    (batch, group, 32-row chunk) of the group's padding rows, every column tile;
     //   column layout: (batch, group, 128-row slice) of the group's padding block-columns, and
     //                  (batch) the padding rows C .. ceil(C/128)*128, every column tile.
-    if (p.blocked && (kRow || kCol)) {
+    auto zero_padding = [&](uint8_t* s_row, uint8_t* s_col) {
         const int G_eff = grouped ? p.G : 1;
         const int64_t rslices = (C + 127) / 128;
         const int64_t units_row = kRow ? (int64_t)p.batch * G_eff * 4 : 0;
@@ -293,7 +319,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
                 const int64_t size = grouped ? ends_s[g] - start : R;
                 const int64_t P = grouped ? pstart_s[g] : 0;
                 const int64_t r0 = size + chunk * 32, r1 = min64(r0 + 32, ((size + 127) / 128) * 128);
-                uint8_t* sb = p.s_row + bb * p.s_row_bstride;
+                uint8_t* sb = s_row + bb * p.s_row_bstride;
                 for (int64_t i = tid; i < (r1 - r0) * ct_row; i += 256) {
                     const int64_t pr = P + r0 + i / ct_row, t = i % ct_row;
                     *reinterpret_cast<uint32_t*>(sb + ((pr >> 7) * ct_row + t) * 512 + (pr & 31) * 16 +
@@ -309,7 +335,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
                 const int64_t Q = grouped ? pstart_s[g] / kBlk : 0;
                 const int64_t c0 = Q + size / kBlk, c1 = Q + ((size + 127) / 128) * 4;
                 const int64_t rlo = rs * 128, rn = min64(128, C - rlo);
-                uint8_t* sb = p.s_col + bb * p.s_col_bstride;
+                uint8_t* sb = s_col + bb * p.s_col_bstride;
                 for (int64_t i = tid; i < rn * (c1 - c0); i += 256) {
                     const int64_t r = rlo + i / (c1 - c0), c = c0 + i % (c1 - c0);
                     sb[blocked_off(r, c, ct_col)] = 0;
@@ -317,7 +343,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
             } else {
                 const int64_t bb = u - units_row - units_colg;
                 const int64_t rows_p = ((C + 127) / 128) * 128;
-                uint8_t* sb = p.s_col + bb * p.s_col_bstride;
+                uint8_t* sb = s_col + bb * p.s_col_bstride;
                 for (int64_t i = tid; i < (rows_p - C) * ct_col; i += 256) {
                     const int64_t r = C + i / ct_col, t = i % ct_col;
                     *reinterpret_cast<uint32_t*>(sb + ((r >> 7) * ct_col + t) * 512 + (r & 31) * 16 +
@@ -325,6 +351,10 @@ __global__ void __launch_bounds__(kQThreads, 2)
                 }
             }
         }
+    };
+    if (p.blocked && (kRow || kCol)) {
+        zero_padding(p.s_row, p.s_col);
+        if constexpr (kSwiBwd) zero_padding(p.s_row2, p.s_col2);
     }
 
     const int wi = warp >> 1, wj = warp & 1;
@@ -339,9 +369,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
         const int64_t row0 = (int64_t)tr * 128 + wi * 32, col0 = (int64_t)tc * 128 + wj * 64;
         if (!mbar_wait_bounded(&full[stage], phase, kQTimeoutNs, abort_flag, p.dev_status)) break;
         // this warp's 32 x 64 sub-tile: lane rows 8li..8li+7, columns 8lj..8lj+7 (16 bytes each)
-        const uint8_t* src = tiles + stage * kQTileBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
+        const uint8_t* src = tiles + stage * kStageBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
         uint32_t v[8][4];
-        if constexpr (!kExt) {
+        if constexpr (kMode == kModePlain) {
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
                 const uint4 u = *reinterpret_cast<const uint4*>(src + rr * 256);
@@ -350,15 +380,15 @@ __global__ void __launch_bounds__(kQThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
         }
-        // the stability variants read their values from the stage while they work and free it after
+        // the other modes read their values from the stage while they work and free it after
         const int cur_stage = stage;
         auto release_stage = [&]() {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[cur_stage]);
         };
-        if (++stage == kQStages) { stage = 0; phase ^= 1u; }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
         if (row0 >= R || col0 >= C) {  // warp-uniform
-            if constexpr (kExt) release_stage();
+            if constexpr (kMode != kModePlain) release_stage();
             continue;
         }
 
@@ -372,8 +402,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
 
         // Row-wise scales s8[rr] of this lane's 8 rows: the 4 lanes of a 32-column block each write
         // two of the rows (2*q4, 2*q4 + 1).  Called with cval true.
-        auto store_row_scales = [&](const uint32_t (&s8)[8]) {
-            uint8_t* sb = p.s_row + b * p.s_row_bstride;
+        auto store_row_scales = [&](uint8_t* s_row, const uint32_t (&s8)[8]) {
+            uint8_t* sb = s_row + b * p.s_row_bstride;
             const int64_t cb = c8 / kBlk;
             const int q4 = lj & 3;
             // this lane's two rows (register selects, no local-memory indexing)
@@ -405,8 +435,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
         };
         // Column-wise scales sc[cc] of this lane's 8 columns: each of the 4 lanes li writes two of
         // them.  Called with cval true.
-        auto store_col_scales = [&](const uint32_t (&sc)[8]) {
-            uint8_t* sb = p.s_col + b * p.s_col_bstride;
+        auto store_col_scales = [&](uint8_t* s_col, const uint32_t (&sc)[8]) {
+            uint8_t* sb = s_col + b * p.s_col_bstride;
             const int64_t rb = row0 / kBlk;
             int64_t pc = rb;
             bool ok = true;
@@ -518,7 +548,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
                         if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
                     }
                 }
-                if (cval) store_row_scales(s8);
+                if (cval) store_row_scales(p.s_row, s8);
             }
             if constexpr (kCol) {
                 uint32_t sc[8];
@@ -608,13 +638,15 @@ __global__ void __launch_bounds__(kQThreads, 2)
                         if (cval) *reinterpret_cast<uint2*>(qb + (c8 + 4 * hc + j) * R + row0 + 8 * li) = q;
                     }
                 }
-                if (cval) store_col_scales(sc);
+                if (cval) store_col_scales(p.s_col, sc);
             }
             release_stage();
             continue;
         }
 
-        if constexpr (!kExt) {  // the plain MX quantization
+        // the plain MX quantization of one 8 x 8 patch per lane (bf16 pairs v) into one output set
+        auto quant_rowcol = [&](const uint32_t (&v)[8][4], uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                                uint8_t* s_col) {
             // magnitude bits of every element (bf16 pairs), shared by both directions
             uint32_t mg[8][4];
 #pragma unroll
@@ -664,7 +696,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
 #pragma unroll
                 for (int rr = 0; rr < 8; ++rr) nonfinite |= s8[rr] == 0xFFu;
                 const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
-                uint8_t* qb = p.q_row + b * R * C;
+                uint8_t* qb = q_row + b * R * C;
 #pragma unroll
                 for (int rr = 0; rr < 8; ++rr) {
                     const int64_t row = row0 + 8 * li + rr;
@@ -678,13 +710,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
                 }
                 // scales: the 4 lanes of a 32-column block each write two of the 8 rows
                 if (cval) {
-                    uint8_t* sb = p.s_row + b * p.s_row_bstride;
+                    uint8_t* sb = s_row + b * p.s_row_bstride;
                     const int64_t cb = c8 / kBlk;
                     const int q4 = lj & 3;
                     if constexpr (kB32Only) {
                         if (li == 0 && q4 == 0) sb[(row0 / kBlk) * Cb + cb] = (uint8_t)s8[0];
                     } else {
-                        store_row_scales(s8);
+                        store_row_scales(s_row, s8);
                     }
                 }
             }
@@ -714,7 +746,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) nonfinite |= sc[cc] == 0xFFu;
                 const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
-                uint8_t* qb = p.q_col + b * R * C;
+                uint8_t* qb = q_col + b * R * C;
                 if (cval) {
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc) {
@@ -744,9 +776,43 @@ __global__ void __launch_bounds__(kQThreads, 2)
                         }
                         *reinterpret_cast<uint2*>(qb + (c8 + cc) * R + row0 + 8 * li) = q;
                     }
-                    store_col_scales(sc);
+                    store_col_scales(s_col, sc);
                 }
             }
+        };
+
+        if constexpr (kSwiBwd) {
+            // fused SwiGLU backward: dh1 and dh3 of h = silu(h1) * h3 at the rounding points of the
+            // bf16 autograd ops (silu(h1), dh*h3, their products each rounded to bf16), fp32 inside
+            uint32_t a[8][4], u3[8][4];
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                const uint4 g = *reinterpret_cast<const uint4*>(src + rr * 256);
+                const uint4 x1 = *reinterpret_cast<const uint4*>(src + kQTileBytes + rr * 256);
+                const uint4 x3 = *reinterpret_cast<const uint4*>(src + 2 * kQTileBytes + rr * 256);
+                v[rr][0] = g.x; v[rr][1] = g.y; v[rr][2] = g.z; v[rr][3] = g.w;
+                a[rr][0] = x1.x; a[rr][1] = x1.y; a[rr][2] = x1.z; a[rr][3] = x1.w;
+                u3[rr][0] = x3.x; u3[rr][1] = x3.y; u3[rr][2] = x3.z; u3[rr][3] = x3.w;
+            }
+            release_stage();
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float g0 = bf16lo(v[rr][k]), g1 = bf16hi(v[rr][k]);
+                    const float x0 = bf16lo(a[rr][k]), x1 = bf16hi(a[rr][k]);
+                    const float sg0 = 1.0f / (1.0f + expf(-x0)), sg1 = 1.0f / (1.0f + expf(-x1));
+                    const uint32_t sl = pack_bf16x2(x0 * sg0, x1 * sg1);                 // bf16(silu(h1))
+                    const uint32_t d3 = pack_bf16x2(g0 * bf16lo(sl), g1 * bf16hi(sl));   // dh3
+                    const uint32_t ds = pack_bf16x2(g0 * bf16lo(u3[rr][k]), g1 * bf16hi(u3[rr][k]));  // dh * h3
+                    a[rr][k] = pack_bf16x2(bf16lo(ds) * sg0 * (1.0f + x0 * (1.0f - sg0)),
+                                           bf16hi(ds) * sg1 * (1.0f + x1 * (1.0f - sg1)));     // dh1
+                    u3[rr][k] = d3;
+                }
+            quant_rowcol(a, p.q_row, p.s_row, p.q_col, p.s_col);
+            quant_rowcol(u3, p.q_row2, p.s_row2, p.q_col2, p.s_col2);
+        } else {
+            quant_rowcol(v, p.q_row, p.s_row, p.q_col, p.s_col);
         }
     }
 
@@ -765,42 +831,45 @@ __global__ void check_offsets_kernel(const int32_t* offs, int32_t G, int64_t M, 
 }
 
 // ---------------------------------------------------------------- host side
-// x viewed as [batch][R][C] bf16 with 128 x 128 boxes, no swizzle, zero fill outside.
-static bool make_x_map(CUtensorMap* m, const QParams& p) {
+// base (x or another input of x's shape) viewed as [batch][R][C] bf16 with 128 x 128 boxes, no
+// swizzle, zero fill outside.
+static bool make_x_map(CUtensorMap* m, const QParams& p, const uint16_t* base) {
     host::EncodeTiledFn fn = host::encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)p.C, (cuuint64_t)p.R, (cuuint64_t)p.batch};
     cuuint64_t strides[2] = {(cuuint64_t)(p.C * 2), (cuuint64_t)(p.R * p.C * 2)};
     cuuint32_t box[3] = {128, 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(p.x), dims, strides, box, estr,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <unsigned DIRS, bool kExt = false>
-static mxfp8_status_t launch_dirs(const CUtensorMap& m, const QParams& p, int64_t grid, cudaStream_t st) {
+template <unsigned DIRS, int kMode = kModePlain>
+static mxfp8_status_t launch_dirs(const CUtensorMap& m, const CUtensorMap& m2, const CUtensorMap& m3, const QParams& p,
+                                  int64_t grid, cudaStream_t st) {
+    constexpr int smem = kMode == kModeSwiBwd ? 2 * 3 * kQTileBytes + 128 : kQSmem;
     static std::atomic<int> attr_set[host::kMaxDevices];
-    if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS, kExt>), kQSmem, attr_set))
+    if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS, kMode>), smem, attr_set))
         return MXFP8_ERR_LAUNCH;
-    quant_tile_kernel<DIRS, kExt><<<(unsigned)grid, kQThreads, kQSmem, st>>>(m, p);
+    quant_tile_kernel<DIRS, kMode><<<(unsigned)grid, kQThreads, smem, st>>>(m, m2, m3, p);
     return host::last_launch_status();
 }
 
 static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t st) {
     if (p.ntiles == 0) return MXFP8_OK;
     CUtensorMap m;
-    if (!make_x_map(&m, p)) return MXFP8_ERR_DRIVER;
+    if (!make_x_map(&m, p, p.x)) return MXFP8_ERR_DRIVER;
     const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms() * 2);
     switch (dirs) {
-        case MXFP8_ROW: return launch_dirs<MXFP8_ROW>(m, p, grid, st);
-        case MXFP8_COL: return launch_dirs<MXFP8_COL>(m, p, grid, st);
-        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL>(m, p, grid, st);
-        case MXFP8_BLOCK32X32: return launch_dirs<MXFP8_BLOCK32X32>(m, p, grid, st);
-        case MXFP8_BLOCK32X32 | MXFP8_ROW: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW>(m, p, grid, st);
-        case MXFP8_BLOCK32X32 | MXFP8_COL: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_COL>(m, p, grid, st);
+        case MXFP8_ROW: return launch_dirs<MXFP8_ROW>(m, m, m, p, grid, st);
+        case MXFP8_COL: return launch_dirs<MXFP8_COL>(m, m, m, p, grid, st);
+        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL>(m, m, m, p, grid, st);
+        case MXFP8_BLOCK32X32: return launch_dirs<MXFP8_BLOCK32X32>(m, m, m, p, grid, st);
+        case MXFP8_BLOCK32X32 | MXFP8_ROW: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW>(m, m, m, p, grid, st);
+        case MXFP8_BLOCK32X32 | MXFP8_COL: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_COL>(m, m, m, p, grid, st);
         case MXFP8_BLOCK32X32 | MXFP8_ROW | MXFP8_COL:
-            return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW | MXFP8_COL>(m, p, grid, st);
+            return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW | MXFP8_COL>(m, m, m, p, grid, st);
         default: return MXFP8_ERR_LAYOUT;
     }
 }
@@ -809,14 +878,23 @@ static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t
 static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStream_t st) {
     if (p.ntiles == 0) return MXFP8_OK;
     CUtensorMap m;
-    if (!make_x_map(&m, p)) return MXFP8_ERR_DRIVER;
+    if (!make_x_map(&m, p, p.x)) return MXFP8_ERR_DRIVER;
     const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms() * 2);
     switch (dirs) {
-        case MXFP8_ROW: return launch_dirs<MXFP8_ROW, true>(m, p, grid, st);
-        case MXFP8_COL: return launch_dirs<MXFP8_COL, true>(m, p, grid, st);
-        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, true>(m, p, grid, st);
+        case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeExt>(m, m, m, p, grid, st);
+        case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeExt>(m, m, m, p, grid, st);
+        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeExt>(m, m, m, p, grid, st);
         default: return MXFP8_ERR_LAYOUT;
     }
+}
+
+// The fused SwiGLU backward: p.x = dh, h1 and h3 of the same shape (one CTA per SM: 3 tiles a stage).
+static mxfp8_status_t launch_swiglu_bwd(const QParams& p, const uint16_t* h1, const uint16_t* h3, cudaStream_t st) {
+    if (p.ntiles == 0) return MXFP8_OK;
+    CUtensorMap m, m1, m3;
+    if (!make_x_map(&m, p, p.x) || !make_x_map(&m1, p, h1) || !make_x_map(&m3, p, h3)) return MXFP8_ERR_DRIVER;
+    const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms());
+    return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeSwiBwd>(m, m1, m3, p, grid, st);
 }
 
 static mxfp8_status_t quantize_2d(const void* x_bf16, int64_t M, int64_t K, unsigned dirs, int scale_layout,
@@ -916,4 +994,35 @@ extern "C" mxfp8_status_t mxfp8_check_offsets(const int32_t* offs, int32_t G, in
     if (mxfp8_status_t a = host::check_arch(); a != MXFP8_OK) return a;
     check_offsets_kernel<<<1, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(offs, G, M, align, dev_status);
     return host::last_launch_status();
+}
+
+extern "C" mxfp8_status_t mxfp8_swiglu_bwd_quantize(const void* dh_bf16, const void* h1_bf16, const void* h3_bf16,
+                                                    int64_t M, int64_t H, const int32_t* offs, int32_t G,
+                                                    void* dh1_q, void* dh1_s, void* dh1T_q, void* dh1T_s, void* dh3_q,
+                                                    void* dh3_s, void* dh3T_q, void* dh3T_s, int32_t* dev_status,
+                                                    mxfp8_stream_t stream) {
+    if (!dh_bf16 || !h1_bf16 || !h3_bf16 || !offs || !dh1_q || !dh1_s || !dh1T_q || !dh1T_s || !dh3_q || !dh3_s ||
+        !dh3T_q || !dh3T_s)
+        return MXFP8_ERR_NULL;
+    if (M < 0 || H <= 0 || G < 1 || G > MXFP8_MAX_GROUPS || M > INT32_MAX) return MXFP8_ERR_SHAPE;
+    if (H % 32 || M % 32) return MXFP8_ERR_ALIGN;
+    const void* ptrs[] = {dh_bf16, h1_bf16, h3_bf16, dh1_q, dh1_s, dh1T_q, dh1T_s, dh3_q, dh3_s, dh3T_q, dh3T_s};
+    for (const void* q : ptrs)
+        if (!host::aligned16(q)) return MXFP8_ERR_ALIGN;
+    if (mxfp8_status_t a = host::check_arch(); a != MXFP8_OK) return a;
+    if (M == 0) return MXFP8_OK;
+    QParams p{};
+    p.x = static_cast<const uint16_t*>(dh_bf16);
+    p.R = M; p.C = H; p.batch = 1;
+    p.q_row = static_cast<uint8_t*>(dh1_q); p.s_row = static_cast<uint8_t*>(dh1_s);
+    p.q_col = static_cast<uint8_t*>(dh1T_q); p.s_col = static_cast<uint8_t*>(dh1T_s);
+    p.q_row2 = static_cast<uint8_t*>(dh3_q); p.s_row2 = static_cast<uint8_t*>(dh3_s);
+    p.q_col2 = static_cast<uint8_t*>(dh3T_q); p.s_col2 = static_cast<uint8_t*>(dh3T_s);
+    p.blocked = 1;
+    p.offs = offs; p.G = G;
+    p.dev_status = dev_status;
+    p.tiles_r = (M + 127) / 128; p.tiles_c = (H + 127) / 128; p.ntiles = p.tiles_r * p.tiles_c;
+    if (p.ntiles >= INT32_MAX) return MXFP8_ERR_SHAPE;
+    return launch_swiglu_bwd(p, static_cast<const uint16_t*>(h1_bf16), static_cast<const uint16_t*>(h3_bf16),
+                             reinterpret_cast<cudaStream_t>(stream));
 }

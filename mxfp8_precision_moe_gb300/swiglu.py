@@ -12,16 +12,18 @@ Forward: x is quantized along D (and along the tokens for the wgrads); one fused
 kernel runs both gate and up GEMMs and writes h1, h3 (bf16, kept for the backward)
 and h already quantized along H (for the down GEMM) and along the tokens (for the
 down wgrad); the down GEMM reads those codes directly.  Backward: dY is quantized
-both ways; dgrad and wgrad of the down GEMM; the SwiGLU backward in bf16 (the ops
-autograd runs for ``silu(h1) * h3``); dh1 and dh3 quantized both ways; dgrads and
-wgrads of gate and up.  Quantization is the identity for gradients.
+both ways; dgrad and wgrad of the down GEMM; one kernel computes the SwiGLU backward
+(dh1, dh3 at the rounding points of the bf16 autograd ops for ``silu(h1) * h3``) and
+quantizes both results both ways; dgrads and wgrads of gate and up.  Quantization is
+the identity for gradients.
 """
 from __future__ import annotations
 
 import torch
 
 from . import (COL, ROW, SCALES_BLOCKED, _check_quad, mxfp8_grouped_mm_dgrad, mxfp8_grouped_mm_fwd,
-               mxfp8_grouped_mm_swiglu_fwd, mxfp8_grouped_mm_wgrad, mxfp8_quantize_2d, quantize_expert_weights)
+               mxfp8_grouped_mm_swiglu_fwd, mxfp8_grouped_mm_wgrad, mxfp8_quantize_2d, mxfp8_swiglu_bwd_quantize,
+               quantize_expert_weights)
 
 
 def swiglu_backward_bf16(dh: torch.Tensor, h1: torch.Tensor, h3: torch.Tensor):
@@ -58,10 +60,8 @@ class _Mxfp8SwiGLUExpert(torch.autograd.Function):
         dx = dWg = dWu = None
         if need_front:
             dh = mxfp8_grouped_mm_dgrad(dq, ds, dTq, dTs, offs)
-            dh1, dh3 = swiglu_backward_bf16(dh, h1, h3)
-            hdirs = (ROW if need_dx else 0) | (COL if (need_dWg or need_dWu) else 0)
-            a1q, a1s, a1Tq, a1Ts = mxfp8_quantize_2d(dh1, hdirs, SCALES_BLOCKED, offs)
-            a3q, a3s, a3Tq, a3Ts = mxfp8_quantize_2d(dh3, hdirs, SCALES_BLOCKED, offs)
+            # the SwiGLU backward and the quantization of dh1, dh3 (both ways) in one kernel
+            (a1q, a1s, a1Tq, a1Ts), (a3q, a3s, a3Tq, a3Ts) = mxfp8_swiglu_bwd_quantize(dh, h1, h3, offs)
             if need_dx:
                 dx = mxfp8_grouped_mm_dgrad(a1q, a1s, gTq, gTs, offs)
                 dx += mxfp8_grouped_mm_dgrad(a3q, a3s, uTq, uTs, offs)
