@@ -47,7 +47,10 @@ struct QParams {
     int64_t tiles_r, tiles_c, ntiles;
     unsigned opts;       // MXFP8_OPT_* (the stability-variant kernels only)
     uint64_t seed;
-    // the fused SwiGLU backward only: x = dh, the second output set (dh3); dh1 goes to q_row.. s_col
+    // the fused SwiGLU backward only: x = dh, x2 = h1, x3 = h3; dh1 goes to q_row .. s_col, dh3 to the
+    // second output set
+    const uint16_t* x2;
+    const uint16_t* x3;
     uint8_t* q_row2;
     uint8_t* s_row2;
     uint8_t* q_col2;
@@ -211,19 +214,19 @@ constexpr int kQStages = 3;                    // SMEM ring depth (tiles in flig
 constexpr int kQTileBytes = 128 * 128 * 2;     // one 128 x 128 bf16 tile
 constexpr int kQThreads = 288;                 // 8 consumer warps + 1 TMA producer warp
 constexpr int kQSmem = kQStages * kQTileBytes + 128;
+constexpr int kQConsumerThreads = 256;           // 8 consumer warps (the producer warp is the ninth)
 
 // kModeExt: the stability variants of ROW / COL / ROW|COL (runtime options p.opts, seed p.seed);
-// fp32 working values.  kModeSwiBwd (ROW|COL only): each stage holds the tiles of dh (xmap), h1
-// (xmap2) and h3 (xmap3); dh1 and dh3 are computed and each quantized both ways.
+// fp32 working values.  kModeSwiBwd (ROW|COL only): 256 threads, no TMA ring: each warp loads its
+// patches of dh, h1 and h3 straight from global memory (three inputs a stage would leave room for
+// too few warps to hide the arithmetic's latency), computes dh1 and dh3 and quantizes each both ways.
 template <unsigned DIRS, int kMode = kModePlain>
-__global__ void __launch_bounds__(kQThreads, kMode == kModeSwiBwd ? 1 : 2)
-    quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xmap2,
-                      const __grid_constant__ CUtensorMap xmap3, QParams p) {
+__global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQThreads, 2)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
     constexpr bool kExt = kMode == kModeExt;
     constexpr bool kSwiBwd = kMode == kModeSwiBwd;
-    constexpr int kNumIn = kSwiBwd ? 3 : 1;                     // input tiles per stage
-    constexpr int kStages = kSwiBwd ? 2 : kQStages;
-    constexpr uint32_t kStageBytes = kNumIn * kQTileBytes;
+    constexpr int kStages = kQStages;
+    constexpr uint32_t kStageBytes = kQTileBytes;
     constexpr bool kRow = (DIRS & MXFP8_ROW) != 0;
     constexpr bool kCol = (DIRS & MXFP8_COL) != 0;
     constexpr bool kB32 = (DIRS & MXFP8_BLOCK32X32) != 0;
@@ -251,10 +254,6 @@ __global__ void __launch_bounds__(kQThreads, kMode == kModeSwiBwd ? 1 : 2)
         abort_s = 0;
         fence_barrier_init();
         prefetch_tmap(&xmap);
-        if (kSwiBwd) {
-            prefetch_tmap(&xmap2);
-            prefetch_tmap(&xmap3);
-        }
     }
     __syncthreads();
     volatile int* abort_flag = &abort_s;
@@ -283,14 +282,8 @@ __global__ void __launch_bounds__(kQThreads, kMode == kModeSwiBwd ? 1 : 2)
                 const uint32_t tt = (uint32_t)t, b = tt / per_b, rem = tt - b * per_b;
                 const uint32_t tr = rem / tiles_c, tc = rem - tr * tiles_c;
                 mbar_arrive_expect_tx(&full[stage], kStageBytes);
-                uint8_t* dst = tiles + stage * kStageBytes;
-                tma_load_3d(dst, &xmap, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b, &full[stage]);
-                if constexpr (kSwiBwd) {
-                    tma_load_3d(dst + kQTileBytes, &xmap2, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
-                                &full[stage]);
-                    tma_load_3d(dst + 2 * kQTileBytes, &xmap3, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
-                                &full[stage]);
-                }
+                tma_load_3d(tiles + stage * kStageBytes, &xmap, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
+                            &full[stage]);
                 issued |= 1u << stage;
                 last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -367,28 +360,32 @@ __global__ void __launch_bounds__(kQThreads, kMode == kModeSwiBwd ? 1 : 2)
         const uint32_t tr = rem / tiles_c, tc = rem - tr * tiles_c;
         const int64_t b = b32;
         const int64_t row0 = (int64_t)tr * 128 + wi * 32, col0 = (int64_t)tc * 128 + wj * 64;
-        if (!mbar_wait_bounded(&full[stage], phase, kQTimeoutNs, abort_flag, p.dev_status)) break;
         // this warp's 32 x 64 sub-tile: lane rows 8li..8li+7, columns 8lj..8lj+7 (16 bytes each)
-        const uint8_t* src = tiles + stage * kStageBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
+        const uint8_t* src = nullptr;
         uint32_t v[8][4];
-        if constexpr (kMode == kModePlain) {
+        int cur_stage = 0;
+        if constexpr (!kSwiBwd) {
+            if (!mbar_wait_bounded(&full[stage], phase, kQTimeoutNs, abort_flag, p.dev_status)) break;
+            src = tiles + stage * kStageBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
+            if constexpr (kMode == kModePlain) {
 #pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                const uint4 u = *reinterpret_cast<const uint4*>(src + rr * 256);
-                v[rr][0] = u.x; v[rr][1] = u.y; v[rr][2] = u.z; v[rr][3] = u.w;
+                for (int rr = 0; rr < 8; ++rr) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(src + rr * 256);
+                    v[rr][0] = u.x; v[rr][1] = u.y; v[rr][2] = u.z; v[rr][3] = u.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
+            cur_stage = stage;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        // the other modes read their values from the stage while they work and free it after
-        const int cur_stage = stage;
+        // the stability variants read their values from the stage while they work and free it after
         auto release_stage = [&]() {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[cur_stage]);
         };
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
         if (row0 >= R || col0 >= C) {  // warp-uniform
-            if constexpr (kMode != kModePlain) release_stage();
+            if constexpr (kExt) release_stage();
             continue;
         }
 
@@ -783,18 +780,23 @@ __global__ void __launch_bounds__(kQThreads, kMode == kModeSwiBwd ? 1 : 2)
 
         if constexpr (kSwiBwd) {
             // fused SwiGLU backward: dh1 and dh3 of h = silu(h1) * h3 at the rounding points of the
-            // bf16 autograd ops (silu(h1), dh*h3, their products each rounded to bf16), fp32 inside
+            // bf16 autograd ops (silu(h1), dh*h3, their products each rounded to bf16), fp32 inside.
+            // Rows past the matrix read as zeros (what the TMA path's fill gives).
             uint32_t a[8][4], u3[8][4];
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
-                const uint4 g = *reinterpret_cast<const uint4*>(src + rr * 256);
-                const uint4 x1 = *reinterpret_cast<const uint4*>(src + kQTileBytes + rr * 256);
-                const uint4 x3 = *reinterpret_cast<const uint4*>(src + 2 * kQTileBytes + rr * 256);
+                const int64_t row = row0 + 8 * li + rr;
+                uint4 g = make_uint4(0, 0, 0, 0), x1 = g, x3 = g;
+                if (row < R && cval) {
+                    const int64_t off = row * C + c8;
+                    g = __ldg(reinterpret_cast<const uint4*>(p.x + off));
+                    x1 = __ldg(reinterpret_cast<const uint4*>(p.x2 + off));
+                    x3 = __ldg(reinterpret_cast<const uint4*>(p.x3 + off));
+                }
                 v[rr][0] = g.x; v[rr][1] = g.y; v[rr][2] = g.z; v[rr][3] = g.w;
                 a[rr][0] = x1.x; a[rr][1] = x1.y; a[rr][2] = x1.z; a[rr][3] = x1.w;
                 u3[rr][0] = x3.x; u3[rr][1] = x3.y; u3[rr][2] = x3.z; u3[rr][3] = x3.w;
             }
-            release_stage();
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr)
 #pragma unroll
@@ -846,13 +848,13 @@ static bool make_x_map(CUtensorMap* m, const QParams& p, const uint16_t* base) {
 }
 
 template <unsigned DIRS, int kMode = kModePlain>
-static mxfp8_status_t launch_dirs(const CUtensorMap& m, const CUtensorMap& m2, const CUtensorMap& m3, const QParams& p,
-                                  int64_t grid, cudaStream_t st) {
-    constexpr int smem = kMode == kModeSwiBwd ? 2 * 3 * kQTileBytes + 128 : kQSmem;
+static mxfp8_status_t launch_dirs(const CUtensorMap& m, const QParams& p, int64_t grid, cudaStream_t st) {
+    constexpr bool direct = kMode == kModeSwiBwd;  // no TMA ring: no dynamic shared memory, no producer warp
+    constexpr int smem = direct ? 0 : kQSmem;
     static std::atomic<int> attr_set[host::kMaxDevices];
     if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS, kMode>), smem, attr_set))
         return MXFP8_ERR_LAUNCH;
-    quant_tile_kernel<DIRS, kMode><<<(unsigned)grid, kQThreads, smem, st>>>(m, m2, m3, p);
+    quant_tile_kernel<DIRS, kMode><<<(unsigned)grid, direct ? kQConsumerThreads : kQThreads, smem, st>>>(m, p);
     return host::last_launch_status();
 }
 
@@ -862,14 +864,14 @@ static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t
     if (!make_x_map(&m, p, p.x)) return MXFP8_ERR_DRIVER;
     const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms() * 2);
     switch (dirs) {
-        case MXFP8_ROW: return launch_dirs<MXFP8_ROW>(m, m, m, p, grid, st);
-        case MXFP8_COL: return launch_dirs<MXFP8_COL>(m, m, m, p, grid, st);
-        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL>(m, m, m, p, grid, st);
-        case MXFP8_BLOCK32X32: return launch_dirs<MXFP8_BLOCK32X32>(m, m, m, p, grid, st);
-        case MXFP8_BLOCK32X32 | MXFP8_ROW: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW>(m, m, m, p, grid, st);
-        case MXFP8_BLOCK32X32 | MXFP8_COL: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_COL>(m, m, m, p, grid, st);
+        case MXFP8_ROW: return launch_dirs<MXFP8_ROW>(m, p, grid, st);
+        case MXFP8_COL: return launch_dirs<MXFP8_COL>(m, p, grid, st);
+        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL>(m, p, grid, st);
+        case MXFP8_BLOCK32X32: return launch_dirs<MXFP8_BLOCK32X32>(m, p, grid, st);
+        case MXFP8_BLOCK32X32 | MXFP8_ROW: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW>(m, p, grid, st);
+        case MXFP8_BLOCK32X32 | MXFP8_COL: return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_COL>(m, p, grid, st);
         case MXFP8_BLOCK32X32 | MXFP8_ROW | MXFP8_COL:
-            return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW | MXFP8_COL>(m, m, m, p, grid, st);
+            return launch_dirs<MXFP8_BLOCK32X32 | MXFP8_ROW | MXFP8_COL>(m, p, grid, st);
         default: return MXFP8_ERR_LAYOUT;
     }
 }
@@ -881,20 +883,20 @@ static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStre
     if (!make_x_map(&m, p, p.x)) return MXFP8_ERR_DRIVER;
     const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms() * 2);
     switch (dirs) {
-        case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeExt>(m, m, m, p, grid, st);
-        case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeExt>(m, m, m, p, grid, st);
-        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeExt>(m, m, m, p, grid, st);
+        case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeExt>(m, p, grid, st);
+        case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeExt>(m, p, grid, st);
+        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeExt>(m, p, grid, st);
         default: return MXFP8_ERR_LAYOUT;
     }
 }
 
-// The fused SwiGLU backward: p.x = dh, h1 and h3 of the same shape (one CTA per SM: 3 tiles a stage).
-static mxfp8_status_t launch_swiglu_bwd(const QParams& p, const uint16_t* h1, const uint16_t* h3, cudaStream_t st) {
+// The fused SwiGLU backward: p.x = dh, p.x2 = h1, p.x3 = h3 (direct loads; the tensor map is unused).
+static mxfp8_status_t launch_swiglu_bwd(const QParams& p, cudaStream_t st) {
     if (p.ntiles == 0) return MXFP8_OK;
-    CUtensorMap m, m1, m3;
-    if (!make_x_map(&m, p, p.x) || !make_x_map(&m1, p, h1) || !make_x_map(&m3, p, h3)) return MXFP8_ERR_DRIVER;
-    const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms());
-    return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeSwiBwd>(m, m1, m3, p, grid, st);
+    CUtensorMap m;
+    if (!make_x_map(&m, p, p.x)) return MXFP8_ERR_DRIVER;
+    const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms() * 2);
+    return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeSwiBwd>(m, p, grid, st);
 }
 
 static mxfp8_status_t quantize_2d(const void* x_bf16, int64_t M, int64_t K, unsigned dirs, int scale_layout,
@@ -1023,6 +1025,7 @@ extern "C" mxfp8_status_t mxfp8_swiglu_bwd_quantize(const void* dh_bf16, const v
     p.dev_status = dev_status;
     p.tiles_r = (M + 127) / 128; p.tiles_c = (H + 127) / 128; p.ntiles = p.tiles_r * p.tiles_c;
     if (p.ntiles >= INT32_MAX) return MXFP8_ERR_SHAPE;
-    return launch_swiglu_bwd(p, static_cast<const uint16_t*>(h1_bf16), static_cast<const uint16_t*>(h3_bf16),
-                             reinterpret_cast<cudaStream_t>(stream));
+    p.x2 = static_cast<const uint16_t*>(h1_bf16);
+    p.x3 = static_cast<const uint16_t*>(h3_bf16);
+    return launch_swiglu_bwd(p, reinterpret_cast<cudaStream_t>(stream));
 }
