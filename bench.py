@@ -346,7 +346,8 @@ class SwiGLUStep:
     """One fwd+bwd of the SwiGLU routed expert y = (silu(x Wg^T) * (x Wu^T)) Wd^T through the C ABI.
 
     fused:   the gate/up GEMMs write h1, h3 and h already quantized both ways (one kernel); in the
-             backward one kernel computes dh1, dh3 and quantizes both both ways;
+             backward one kernel computes dh1, dh3 and quantizes both both ways, and one GEMM gives
+             dx = dh1 Wg + dh3 Wu;
     unfused: two forward GEMMs, h = silu(h1) * h3 in torch bf16, a ROW|COL quantization of h; in the
              backward the SwiGLU backward in torch bf16 ops and two ROW|COL quantizations.
     Both run the down GEMM, and in the backward: dY quantized both ways, down dgrad and wgrad, two
@@ -426,17 +427,22 @@ class SwiGLUStep:
             calls += [("torch.swiglu_bwd", glue(swiglu_bwd_torch), ()),
                       ("quant_dh1", L.mxfp8_quantize_2d, (P(dh1), M, H, RC, 1, offs, G, *q(a1), st)),
                       ("quant_dh3", L.mxfp8_quantize_2d, (P(dh3), M, H, RC, 1, offs, G, *q(a3), st))]
+        if fused:
+            calls.append(("dgrad_gate_up", L.mxfp8_grouped_mm_dgrad2,
+                          (*q(a1)[:2], *q(wq["Wg"])[2:], *q(a3)[:2], *q(wq["Wu"])[2:], offs, G, M, H, D, P(dx), st)))
+        else:
+            calls += [
+                ("dgrad_gate", L.mxfp8_grouped_mm_dgrad, (*q(a1)[:2], *q(wq["Wg"])[2:], offs, G, M, H, D, P(dx), st)),
+                ("dgrad_up", L.mxfp8_grouped_mm_dgrad, (*q(a3)[:2], *q(wq["Wu"])[2:], offs, G, M, H, D, P(dx2), st)),
+                ("torch.add", glue(lambda: dx.add_(dx2)), ())]
         calls += [
-            ("dgrad_gate", L.mxfp8_grouped_mm_dgrad, (*q(a1)[:2], *q(wq["Wg"])[2:], offs, G, M, H, D, P(dx), st)),
-            ("dgrad_up", L.mxfp8_grouped_mm_dgrad, (*q(a3)[:2], *q(wq["Wu"])[2:], offs, G, M, H, D, P(dx2), st)),
-            ("torch.add", glue(lambda: dx.add_(dx2)), ()),
             ("wgrad_gate", L.mxfp8_grouped_mm_wgrad, (*q(a1)[2:], *q(xq)[2:], offs, G, M, H, D, P(dWg), st)),
             ("wgrad_up", L.mxfp8_grouped_mm_wgrad, (*q(a3)[2:], *q(xq)[2:], offs, G, M, H, D, P(dWu), st)),
         ]
         self.calls = calls
         self.launches = {n: (0 if n.startswith("torch.") else 1) for n, _, _ in calls}
         f1 = 2.0 * M * D * H
-        self.gemm_flops = {n: (2 * f1 if n == "gateup_swiglu" else f1) for n, _, _ in calls
+        self.gemm_flops = {n: (2 * f1 if n in ("gateup_swiglu", "dgrad_gate_up") else f1) for n, _, _ in calls
                            if n.startswith(("fwd_", "dgrad_", "wgrad_", "gateup"))}
         self.flops = 9 * f1
         qb = lambda e: e * (2 + 1 + 1 + 2 / 32)

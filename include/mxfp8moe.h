@@ -220,6 +220,17 @@ mxfp8_status_t mxfp8_grouped_mm_fwd(const void* a_q, const void* a_s, const void
 mxfp8_status_t mxfp8_grouped_mm_dgrad(const void* dout_q, const void* dout_s, const void* wt_q, const void* wt_s,
                                       const int32_t* offs, int32_t G, int64_t M, int64_t N, int64_t K,
                                       void* da_bf16, int32_t* dev_status, mxfp8_stream_t stream);
+/* mxfp8_grouped_mm_dgrad2: the sum of two dgrads over the same groups, in one GEMM whose contraction
+ *   runs first over (dout1, wt1) and then over (dout2, wt2) into one fp32 accumulator, rounded to bf16
+ *   once: dA[m, k] = sum_n dOut1[m,n] W1[g][n,k] + sum_n dOut2[m,n] W2[g][n,k].  Both pairs have the
+ *   shapes and layouts of mxfp8_grouped_mm_dgrad.  The SwiGLU expert's input gradient
+ *   dx = dh1 Wg + dh3 Wu is one call (the gate/up branches of "feat(moe): add MoK MXFP8 expert
+ *   support").
+ */
+mxfp8_status_t mxfp8_grouped_mm_dgrad2(const void* dout1_q, const void* dout1_s, const void* wt1_q, const void* wt1_s,
+                                       const void* dout2_q, const void* dout2_s, const void* wt2_q, const void* wt2_s,
+                                       const int32_t* offs, int32_t G, int64_t M, int64_t N, int64_t K, void* da_bf16,
+                                       int32_t* dev_status, mxfp8_stream_t stream);
 mxfp8_status_t mxfp8_grouped_mm_wgrad(const void* doutT_q, const void* doutT_s, const void* aT_q,
                                       const void* aT_s, const int32_t* offs, int32_t G, int64_t M, int64_t N,
                                       int64_t K, void* dw_bf16, int32_t* dev_status, mxfp8_stream_t stream);

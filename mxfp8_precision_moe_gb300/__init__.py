@@ -30,7 +30,7 @@ __all__ = [
     "mxfp8_grouped_mm_wgrad", "mxfp8_scale_bytes", "mxfp8_scale_bytes_colgroups", "mxfp8_check_offsets",
     "mxfp8_debug_wait_timeout", "new_status", "read_status", "to_mxfp8_then_scaled_grouped_mm", "load",
     "quantize_expert_weights", "Mxfp8WeightCache", "mxfp8_grouped_mm_swiglu_fwd", "mxfp8_swiglu_expert",
-    "mxfp8_swiglu_bwd_quantize",
+    "mxfp8_swiglu_bwd_quantize", "mxfp8_grouped_mm_dgrad2",
 ]
 
 
@@ -168,6 +168,24 @@ def mxfp8_grouped_mm_dgrad(dout_q, dout_s, wt_q, wt_s, offs, out=None, dev_statu
     st = load().mxfp8_grouped_mm_dgrad(_p(dout_q), _p(dout_s), _p(wt_q), _p(wt_s), _p(offs), G, M, N, K, _p(out),
                                        _p(dev_status), _stream(dout_q.device))
     check(st, "mxfp8_grouped_mm_dgrad")
+    return out
+
+
+def mxfp8_grouped_mm_dgrad2(dout1_q, dout1_s, wt1_q, wt1_s, dout2_q, dout2_s, wt2_q, wt2_s, offs, out=None,
+                            dev_status=None):
+    """dA = dOut1 W1[g] + dOut2 W2[g] in one GEMM (one fp32 accumulator, one bf16 rounding);
+    operands as for mxfp8_grouped_mm_dgrad."""
+    _cuda(dout1_q, dout1_s, wt1_q, wt1_s, dout2_q, dout2_s, wt2_q, wt2_s, offs, out, dev_status)
+    M, N = dout1_q.shape
+    G, K, _ = wt1_q.shape
+    if tuple(dout2_q.shape) != (M, N) or tuple(wt2_q.shape) != (G, K, N):
+        raise ValueError("mxfp8_grouped_mm_dgrad2: both operand pairs must have the same shapes")
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=dout1_q.device)
+    st = load().mxfp8_grouped_mm_dgrad2(_p(dout1_q), _p(dout1_s), _p(wt1_q), _p(wt1_s), _p(dout2_q), _p(dout2_s),
+                                        _p(wt2_q), _p(wt2_s), _p(offs), G, M, N, K, _p(out), _p(dev_status),
+                                        _stream(dout1_q.device))
+    check(st, "mxfp8_grouped_mm_dgrad2")
     return out
 
 

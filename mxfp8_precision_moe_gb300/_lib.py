@@ -57,6 +57,8 @@ def load():
     L.mxfp8_grouped_mm_swiglu_fwd.restype = S
     L.mxfp8_swiglu_bwd_quantize.argtypes = [P, P, P, I64, I64, P, I32, P, P, P, P, P, P, P, P, P, P]
     L.mxfp8_swiglu_bwd_quantize.restype = S
+    L.mxfp8_grouped_mm_dgrad2.argtypes = [P, P, P, P, P, P, P, P, P, I32, I64, I64, I64, P, P, P]
+    L.mxfp8_grouped_mm_dgrad2.restype = S
     L.mxfp8_scale_bytes.argtypes = [I64, I64, I32, INT]
     L.mxfp8_scale_bytes.restype = ctypes.c_size_t
     L.mxfp8_scale_bytes_colgroups.argtypes = [I64, I64, I32]

@@ -89,7 +89,8 @@ struct GemmParams {
     // SwiGLU gate/up variant only: B rows 0-127 of a tile come from the gate weights (sfb), rows
     // 128-255 from the up weights (sfb2); out = h1, out2 = h3; h = silu(h1) * h3 quantized along
     // its row into hq/hs (blocked, row groups) and along the tokens into hTq/hTs (blocked, token groups).
-    const uint8_t* sfb2;
+    const uint8_t* sfb2;      // also: second B operand's scales of the two-operand dgrad
+    const uint8_t* sfa2;      // two-operand dgrad only: second A operand's scales
     __nv_bfloat16* out2;
     uint8_t* hq;
     uint8_t* hs;
@@ -124,7 +125,9 @@ __device__ __forceinline__ int band_split(int64_t l, int64_t mt, int64_t nt, int
 
 // kSwi: a tile is 128 output columns wide and its 256 B rows are those 128 rows of the gate
 // weights followed by the same 128 rows of the up weights.
-template <int BN, bool kSwi = false>
+// kDualK (ROWGROUPED): the contraction runs over two operand pairs one after the other, k-tiles
+// 0 .. k/2-1 over (A, B) and k/2 .. k-1 over (A2, B2), into one accumulator.
+template <int BN, bool kSwi = false, bool kDualK = false>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, const int32_t* ends_s,
                                               const int32_t* pstart_s, int64_t ptotal) {
     constexpr int TN = kSwi ? 128 : BN;  // output columns per tile
@@ -147,7 +150,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, co
         ti.a_row = start + m * BM;
         ti.b_row = (int64_t)g * p.nb + n * TN;
         ti.a_x0 = 0;
-        ti.k_tiles = (int)((p.kc + BK - 1) / BK);
+        ti.k_tiles = (int)((p.kc + BK - 1) / BK) * (kDualK ? 2 : 1);
         ti.sfa_base = ((int64_t)(pstart_s[g] / BM + m) * p.sfa_ct) * 512;
         const int64_t last_chunk = (p.nb + 127) / 128 - 1;
 #pragma unroll
@@ -205,10 +208,11 @@ __device__ __forceinline__ uint32_t nonfinite_codes2(uint32_t v) {
 // One bf16 pair times f (a power of two, exact) -> two E4M3 codes (RNE, satfinite).
 __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float f) { return cvt_e4m3x2(bf16lo(v) * f, bf16hi(v) * f); }
 
-template <int BN, bool kSwi>
+template <int BN, bool kSwi, bool kDualK = false>
 __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
     grouped_mm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                      const __grid_constant__ CUtensorMap tmap_b2, const GemmParams p) {
+                      const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_a2,
+                      const GemmParams p) {
     using C = Cfg<BN>;
     static_assert(!kSwi || BN == 256, "the SwiGLU variant pairs 128 gate with 128 up rows");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -272,7 +276,8 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             abort_s = 0;
             prefetch_tmap(&tmap_a);
             prefetch_tmap(&tmap_b);
-            if (kSwi) prefetch_tmap(&tmap_b2);
+            if (kSwi || kDualK) prefetch_tmap(&tmap_b2);
+            if (kDualK) prefetch_tmap(&tmap_a2);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -313,7 +318,8 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
+                const int kt_half = kDualK ? ti.k_tiles / 2 : ti.k_tiles;
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
@@ -324,9 +330,11 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                     uint8_t* ssa = smem + C::kOffSfa + stage * C::kSfaBytes;
                     uint8_t* ssb = smem + C::kOffSfb + stage * C::kSfbBytes;
                     mbar_arrive_expect_tx(&full[stage], C::kTx);
-                    const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kt * BK);
-                    tma_load_2d(sa, &tmap_a, kx, (int32_t)ti.a_row, &full[stage]);
-                    bulk_load(ssa, p.sfa + ti.sfa_base + kt * ti.sf_kstep, 512, &full[stage]);
+                    const bool second = kDualK && kt >= kt_half;  // second operand pair of a two-operand dgrad
+                    const int kk = second ? kt - kt_half : kt;
+                    const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kk * BK);
+                    tma_load_2d(sa, second ? &tmap_a2 : &tmap_a, kx, (int32_t)ti.a_row, &full[stage]);
+                    bulk_load(ssa, (second ? p.sfa2 : p.sfa) + ti.sfa_base + kk * ti.sf_kstep, 512, &full[stage]);
                     if constexpr (kSwi) {
                         // rows 0-127: gate weights, rows 128-255: the same rows of the up weights
                         tma_load_2d(sb, &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
@@ -334,10 +342,11 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                         bulk_load(ssb, p.sfb + ti.sfb_base[0] + kt * ti.sf_kstep, 512, &full[stage]);
                         bulk_load(ssb + 512, p.sfb2 + ti.sfb_base[1] + kt * ti.sf_kstep, 512, &full[stage]);
                     } else {
-                        tma_load_2d(sb, &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
+                        tma_load_2d(sb, second ? &tmap_b2 : &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
 #pragma unroll
                         for (int j = 0; j < BN / 128; ++j)
-                            bulk_load(ssb + j * 512, p.sfb + ti.sfb_base[j] + kt * ti.sf_kstep, 512, &full[stage]);
+                            bulk_load(ssb + j * 512, (second ? p.sfb2 : p.sfb) + ti.sfb_base[j] + kk * ti.sf_kstep, 512,
+                                      &full[stage]);
                     }
                     issued_mask |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -358,7 +367,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
                 if (ti.k_tiles == 0) continue;
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
@@ -418,7 +427,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             const int64_t ct_T = ptotal / 128;  // column tiles of the token-grouped h^T scales
             uint32_t acc_phase = 0;
             for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
                 if (!mbar_wait_bounded(&tfull[0], acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
                 uint32_t hg[16], hu[16];  // bf16 pairs (columns 2i, 2i+1 of the block) of h1 and h3
@@ -526,7 +535,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kSwi>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
                 const bool row_ok = r < ti.valid_rows;
                 __nv_bfloat16* orow = ti.out + (int64_t)r * ti.ldo;
                 __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo;  // first row of this warp
@@ -966,22 +975,25 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// b2 (SwiGLU variant only): the up weights, same shape as b; each B map then has 128-row boxes.
-template <int BN, bool kSwi = false>
+// b2: SwiGLU variant: the up weights, same shape as b (each B map then has 128-row boxes); two-operand
+// dgrad (kDualK): the second B operand.  a2: two-operand dgrad only, the second A operand.
+template <int BN, bool kSwi = false, bool kDualK = false>
 static mxfp8_status_t launch_gemm(const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
                                   int64_t b_cols, GemmParams& p, int64_t tiles_bound, cudaStream_t st,
-                                  const void* b2 = nullptr) {
+                                  const void* b2 = nullptr, const void* a2 = nullptr) {
     using C = Cfg<BN>;
-    CUtensorMap ma, mb, mb2;
+    CUtensorMap ma, mb, mb2, ma2;
     const int b_box = kSwi ? 128 : BN;
     if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, b_box)) return MXFP8_ERR_DRIVER;
-    if (kSwi ? !make_map(&mb2, b2, b_rows, b_cols, b_box) : false) return MXFP8_ERR_DRIVER;
-    if (!kSwi) mb2 = mb;
+    if ((kSwi || kDualK) ? !make_map(&mb2, b2, b_rows, b_cols, b_box) : false) return MXFP8_ERR_DRIVER;
+    if (kDualK ? !make_map(&ma2, a2, a_rows, a_cols, BM) : false) return MXFP8_ERR_DRIVER;
+    if (!kSwi && !kDualK) mb2 = mb;
+    if (!kDualK) ma2 = ma;
     static std::atomic<int> attr_set[host::kMaxDevices];
-    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_kernel<BN, kSwi>), C::kSmem, attr_set))
+    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_kernel<BN, kSwi, kDualK>), C::kSmem, attr_set))
         return MXFP8_ERR_LAUNCH;
     const int grid = (int)max64(1, min64(tiles_bound, host::num_sms()));
-    grouped_mm_kernel<BN, kSwi><<<grid, kSwi ? kThreadsSwi : kThreads, C::kSmem, st>>>(ma, mb, mb2, p);
+    grouped_mm_kernel<BN, kSwi, kDualK><<<grid, kSwi ? kThreadsSwi : kThreads, C::kSmem, st>>>(ma, mb, mb2, ma2, p);
     return host::last_launch_status();
 }
 
@@ -1051,11 +1063,18 @@ static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols,
     return host::last_launch_status();
 }
 
-// fwd and dgrad: token operand tok_q [M, Kc], expert operand ex_q [G, Nb, Kc].
+// fwd and dgrad: token operand tok_q [M, Kc], expert operand ex_q [G, Nb, Kc].  With tok2_q (two-operand
+// dgrad) a second pair tok2 / ex2 of the same shapes is contracted into the same output.
 static mxfp8_status_t rowgrouped(const void* tok_q, const void* tok_s, const void* ex_q, const void* ex_s,
                                  const int32_t* offs, int32_t G, int64_t M, int64_t Nb, int64_t Kc, void* out,
-                                 int32_t* dev_status, cudaStream_t st) {
+                                 int32_t* dev_status, cudaStream_t st, const void* tok2_q = nullptr,
+                                 const void* tok2_s = nullptr, const void* ex2_q = nullptr, const void* ex2_s = nullptr) {
     if (!tok_q || !tok_s || !ex_q || !ex_s || !offs || !out) return MXFP8_ERR_NULL;
+    const bool dual = tok2_q != nullptr;
+    if (dual && (!tok2_s || !ex2_q || !ex2_s)) return MXFP8_ERR_NULL;
+    if (dual && (!host::aligned16(tok2_q) || !host::aligned16(tok2_s) || !host::aligned16(ex2_q) ||
+                 !host::aligned16(ex2_s)))
+        return MXFP8_ERR_ALIGN;
     if (G < 1 || G > MXFP8_MAX_GROUPS || M < 0 || Nb <= 0 || Kc <= 0 || M > INT32_MAX || (int64_t)G * Nb > INT32_MAX)
         return MXFP8_ERR_SHAPE;
     if (Kc % 32 || Nb % 32) return MXFP8_ERR_ALIGN;
@@ -1080,6 +1099,16 @@ static mxfp8_status_t rowgrouped(const void* tok_q, const void* tok_s, const voi
     p.mode = ROWGROUPED;
     p.dev_status = dev_status;
     p.timeout_ns = default_timeout_ns();
+    if (dual) {
+        p.sfa2 = static_cast<const uint8_t*>(tok2_s);
+        p.sfb2 = static_cast<const uint8_t*>(ex2_s);
+        if (Nb >= 256) {
+            const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 255) / 256);
+            return launch_gemm<256, false, true>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st, ex2_q, tok2_q);
+        }
+        const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 127) / 128);
+        return launch_gemm<128, false, true>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st, ex2_q, tok2_q);
+    }
     if (Nb >= 256 && kPairForRowGrouped) {
         const int64_t bound = ((M + 255) / 256 + G) * ((Nb + 255) / 256);
         const int64_t sfa_bytes = ((M + 127) / 128 + G) * 128 * p.sfa_ct * 4;
@@ -1202,4 +1231,14 @@ extern "C" mxfp8_status_t mxfp8_grouped_mm_swiglu_fwd(const void* x_q, const voi
     p.timeout_ns = default_timeout_ns();
     const int64_t bound = ((M + BM - 1) / BM + G) * ((H + 127) / 128);
     return launch_gemm<256, true>(x_q, M, D, wg_q, (int64_t)G * H, D, p, bound, st, wu_q);
+}
+
+extern "C" mxfp8_status_t mxfp8_grouped_mm_dgrad2(const void* dout1_q, const void* dout1_s, const void* wt1_q,
+                                                  const void* wt1_s, const void* dout2_q, const void* dout2_s,
+                                                  const void* wt2_q, const void* wt2_s, const int32_t* offs, int32_t G,
+                                                  int64_t M, int64_t N, int64_t K, void* da_bf16, int32_t* dev_status,
+                                                  mxfp8_stream_t stream) {
+    if (!dout2_q) return MXFP8_ERR_NULL;
+    return rowgrouped(dout1_q, dout1_s, wt1_q, wt1_s, offs, G, M, K, N, da_bf16, dev_status,
+                      reinterpret_cast<cudaStream_t>(stream), dout2_q, dout2_s, wt2_q, wt2_s);
 }

@@ -14,14 +14,15 @@ and h already quantized along H (for the down GEMM) and along the tokens (for th
 down wgrad); the down GEMM reads those codes directly.  Backward: dY is quantized
 both ways; dgrad and wgrad of the down GEMM; one kernel computes the SwiGLU backward
 (dh1, dh3 at the rounding points of the bf16 autograd ops for ``silu(h1) * h3``) and
-quantizes both results both ways; dgrads and wgrads of gate and up.  Quantization is
-the identity for gradients.
+quantizes both results both ways; one GEMM for dx = dh1 Wg + dh3 Wu; the wgrads of
+gate and up.  Quantization is the identity for gradients.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (COL, ROW, SCALES_BLOCKED, _check_quad, mxfp8_grouped_mm_dgrad, mxfp8_grouped_mm_fwd,
+from . import (COL, ROW, SCALES_BLOCKED, _check_quad, mxfp8_grouped_mm_dgrad, mxfp8_grouped_mm_dgrad2,
+               mxfp8_grouped_mm_fwd,
                mxfp8_grouped_mm_swiglu_fwd, mxfp8_grouped_mm_wgrad, mxfp8_quantize_2d, mxfp8_swiglu_bwd_quantize,
                quantize_expert_weights)
 
@@ -62,9 +63,8 @@ class _Mxfp8SwiGLUExpert(torch.autograd.Function):
             dh = mxfp8_grouped_mm_dgrad(dq, ds, dTq, dTs, offs)
             # the SwiGLU backward and the quantization of dh1, dh3 (both ways) in one kernel
             (a1q, a1s, a1Tq, a1Ts), (a3q, a3s, a3Tq, a3Ts) = mxfp8_swiglu_bwd_quantize(dh, h1, h3, offs)
-            if need_dx:
-                dx = mxfp8_grouped_mm_dgrad(a1q, a1s, gTq, gTs, offs)
-                dx += mxfp8_grouped_mm_dgrad(a3q, a3s, uTq, uTs, offs)
+            if need_dx:  # dx = dh1 Wg + dh3 Wu, one GEMM over both
+                dx = mxfp8_grouped_mm_dgrad2(a1q, a1s, gTq, gTs, a3q, a3s, uTq, uTs, offs)
             if need_dWg:
                 dWg = mxfp8_grouped_mm_wgrad(a1Tq, a1Ts, xTq, xTs, offs)
             if need_dWu:

@@ -353,3 +353,28 @@ def test_bounded_wait_times_out_cleanly(mx):
     x = torch.ones((32, 32), dtype=torch.bfloat16, device="cuda")
     q, s, _, _ = mx.mxfp8_quantize_2d(x, mx.ROW, mx.SCALES_COMPACT)
     assert int(s[0, 0].item()) == 0x77 and int(q[0, 0].item()) == 0x78
+
+
+def test_dgrad2_equals_the_sum_of_two_dgrads(mx):
+    """dA = dOut1 W1 + dOut2 W2 in one GEMM (the SwiGLU expert's dx = dh1 Wg + dh3 Wu) against the
+    oracle's two fp64 dgrads summed, within the GEMM bound; empty and ragged groups included."""
+    sizes = [96, 0, 160, 64]
+    G, N, K = len(sizes), 256, 384
+    M = sum(sizes)
+    ends = sizes_to_ends(sizes)
+    offs = offs_dev(sizes)
+    D1, D2 = synth.randn_bf16((M, N), 1.0, seed=41), synth.randn_bf16((M, N), 1.0, seed=42)
+    W1, W2 = synth.randn_bf16((G, N, K), 0.02, seed=43), synth.randn_bf16((G, N, K), 0.02, seed=44)
+    st = mx.new_status()
+    q = [mx.mxfp8_quantize_2d(D.cuda(), mx.ROW, mx.SCALES_BLOCKED, offs, st)[:2] for D in (D1, D2)]
+    wt = [mx.mxfp8_quantize_3d_experts(W.cuda(), mx.COL, mx.SCALES_BLOCKED, st)[2:] for W in (W1, W2)]
+    dA = mx.mxfp8_grouped_mm_dgrad2(*q[0], *wt[0], *q[1], *wt[1], offs, dev_status=st)
+    mx.read_status(st)
+    ref = 0
+    for D, W in ((D1, W1), (D2, W2)):
+        dq, ds = oracle.quantize_rows(u16(D))
+        wTq, wTs = zip(*[oracle.quantize_cols(u16(W[g])) for g in range(G)])
+        ref = ref + oracle.grouped_mm_rows(dq, ds, np.stack(wTq), np.stack(wTs), ends)
+    assert_gemm_close(f64(dA), ref, what="dgrad2")
+    with pytest.raises(ValueError):
+        mx.mxfp8_grouped_mm_dgrad2(*q[0], *wt[0], q[1][0][:, :128].contiguous(), q[1][1], *wt[1], offs)
