@@ -169,6 +169,26 @@ __device__ __forceinline__ uint32_t e8m0_from_f32bits(uint32_t a) {
 
 constexpr float kRhtScale = 0x1.6a09e6p-3f;  // fp32(1 / sqrt(32))
 
+// Scale bytes of two blocks at once from their packed bf16 magnitude amaxes (one per 16-bit half):
+// s = max(E - 8, 0) per half, E the exponent field.  E = 255 (Inf/NaN) comes out as 247 here, a value
+// no finite amax gives; nonfinite_pairs() finds it and fix_nonfinite_pair() turns it into 0xFF.
+__device__ __forceinline__ uint32_t e8m0_pair(uint32_t m) {
+    return vmax_u16x2((m >> 7) & 0x00FF00FFu, 0x00080008u) - 0x00080008u;
+}
+// Bit 8 of a half is set iff that half of s + 9 reached 256, i.e. s == 247 (halves never carry).
+constexpr uint32_t kNonfiniteAdd = 0x00090009u, kNonfiniteBits = 0x01000100u;
+__device__ __forceinline__ uint32_t fix_nonfinite_pair(uint32_t s) {
+    const uint32_t lo = s & 0xFFFFu, hi = s >> 16;
+    return (lo == 247u ? 0xFFu : lo) | ((hi == 247u ? 0xFFu : hi) << 16);
+}
+// 2^(127 - s) for the low (h = 0) or high (h = 1) half of a scale pair with both halves <= 247:
+// the fp32 exponent field 254 - s, taken from the packed difference.
+__device__ __forceinline__ float inv_scale_pair(uint32_t s, int h) {
+    const uint32_t d = 0x00FE00FEu - s;
+    return __uint_as_float(h ? ((d << 7) & 0x7F800000u) : (d << 23));
+}
+__device__ __forceinline__ uint32_t pair_half(uint32_t s, int h) { return h ? s >> 16 : s & 0xFFFFu; }
+
 __device__ __forceinline__ uint32_t shfl_xor_max16x2(uint32_t v, int m) {
     return vmax_u16x2(v, __shfl_xor_sync(0xffffffffu, v, m));
 }
@@ -394,61 +414,63 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
         int wg0 = 0, wg1 = 0;              // groups of the warp's first and last row (warp-uniform)
         if (grouped && p.blocked) {
             wg0 = find_group(ends_s, p.G, row0);
-            wg1 = find_group(ends_s, p.G, min64(row0 + 31, R - 1));
+            const int64_t rl = min64(row0 + 31, R - 1);
+            wg1 = (wg0 < p.G && rl < ends_s[wg0]) ? wg0 : find_group(ends_s, p.G, rl);
         }
 
-        // Row-wise scales s8[rr] of this lane's 8 rows: the 4 lanes of a 32-column block each write
-        // two of the rows (2*q4, 2*q4 + 1).  Called with cval true.
-        auto store_row_scales = [&](uint8_t* s_row, const uint32_t (&s8)[8]) {
+        // Row-wise scales of the warp's 32 rows x 2 block-columns.  P0 / P1: this lane's scale bytes of
+        // rows 0-3 / 4-7 of its 8-row patch (the same in the 4 lanes of a 32-column block).  Lane l
+        // writes row row0 + l, both block-columns with one 16-bit store, or 32-bit with two zero bytes
+        // when the rest of the layout's 4-byte word lies past C.  The whole warp calls it.
+        auto store_row_scales = [&](uint8_t* s_row, uint32_t P0, uint32_t P1) {
+            const int src = lane & ~7;  // lanes of rows 8i..8i+7: block 0 at 8i, block 1 at 8i + 4
+            const uint32_t x0 = __shfl_sync(0xffffffffu, P0, src), x1 = __shfl_sync(0xffffffffu, P1, src);
+            const uint32_t y0 = __shfl_sync(0xffffffffu, P0, src + 4), y1 = __shfl_sync(0xffffffffu, P1, src + 4);
+            const int64_t cb = col0 / kBlk;
+            const bool two = col0 + kBlk < C;
+            const uint32_t b0 = __byte_perm(x0, x1, lane & 7) & 0xFFu;
+            const uint32_t b1 = two ? __byte_perm(y0, y1, lane & 7) & 0xFFu : 0u;
+            const int64_t row = row0 + lane;
+            if (row >= R) return;
             uint8_t* sb = s_row + b * p.s_row_bstride;
-            const int64_t cb = c8 / kBlk;
-            const int q4 = lj & 3;
-            // this lane's two rows (register selects, no local-memory indexing)
-            const uint32_t my_s[2] = {q4 == 0 ? s8[0] : q4 == 1 ? s8[2] : q4 == 2 ? s8[4] : s8[6],
-                                      q4 == 0 ? s8[1] : q4 == 1 ? s8[3] : q4 == 2 ? s8[5] : s8[7]};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int rr = 2 * q4 + h;
-                const int64_t row = row0 + 8 * li + rr;
-                if (row >= R) continue;
-                const uint8_t sv = (uint8_t)my_s[h];
-                if (!p.blocked) {
-                    sb[row * Cb + cb] = sv;
-                    continue;
-                }
-                int64_t pr = row;
-                if (grouped) {
-                    int g = wg0;
-                    if (wg0 != wg1) g = find_group(ends_s, p.G, row);
-                    if (g >= p.G) continue;
-                    pr = pstart_s[g] + (row - (g ? ends_s[g - 1] : 0));
-                }
-                const int64_t off = blocked_off(pr, cb, ct_row);
-                sb[off] = sv;
-                // last block-column of a row whose K/32 is not a multiple of 4: zero the rest of the word
-                if (cb == Cb - 1)
-                    for (int64_t z = (Cb & 3); z != 0 && z < 4; ++z) sb[off + z - (Cb & 3) + 1] = 0;
+            if (!p.blocked) {
+                sb[row * Cb + cb] = (uint8_t)b0;
+                if (two) sb[row * Cb + cb + 1] = (uint8_t)b1;
+                return;
             }
+            int64_t pr = row;
+            if (grouped) {
+                int g = wg0;
+                if (wg0 != wg1) g = find_group(ends_s, p.G, row);
+                if (g >= p.G) return;
+                pr = pstart_s[g] + (row - (g ? ends_s[g - 1] : 0));
+            }
+            uint8_t* w = sb + ((pr >> 7) * ct_row + (cb >> 2)) * 512 + (pr & 31) * 16 + ((pr >> 5) & 3) * 4 + (cb & 3);
+            if ((cb & 3) == 0 && col0 + 2 * kBlk >= C) *reinterpret_cast<uint32_t*>(w) = b0 | (b1 << 8);
+            else *reinterpret_cast<uint16_t*>(w) = (uint16_t)(b0 | (b1 << 8));
         };
-        // Column-wise scales sc[cc] of this lane's 8 columns: each of the 4 lanes li writes two of
-        // them.  Called with cval true.
-        auto store_col_scales = [&](uint8_t* s_col, const uint32_t (&sc)[8]) {
+        // Column-wise scales of the warp's 64 columns (one 32-row block).  s2c[k]: scale bytes of this
+        // lane's columns 2k (low half) and 2k+1 (high half); lane (li, lj) writes columns
+        // 8lj + 2li and 8lj + 2li + 1, 16 bytes apart in the blocked layout.
+        auto store_col_scales = [&](uint8_t* s_col, const uint32_t (&s2c)[4]) {
+            if (!cval) return;
+            const uint32_t my = li == 0 ? s2c[0] : li == 1 ? s2c[1] : li == 2 ? s2c[2] : s2c[3];
             uint8_t* sb = s_col + b * p.s_col_bstride;
             const int64_t rb = row0 / kBlk;
+            const int64_t c = c8 + 2 * li;
+            if (!p.blocked) {
+                sb[c * (R / kBlk) + rb] = (uint8_t)my;
+                sb[(c + 1) * (R / kBlk) + rb] = (uint8_t)(my >> 16);
+                return;
+            }
             int64_t pc = rb;
-            bool ok = true;
-            if (p.blocked && grouped) {
-                ok = wg0 < p.G;
-                if (ok) pc = pstart_s[wg0] / kBlk + (row0 - (wg0 ? ends_s[wg0 - 1] : 0)) / kBlk;
+            if (grouped) {
+                if (wg0 >= p.G) return;
+                pc = pstart_s[wg0] / kBlk + (row0 - (wg0 ? ends_s[wg0 - 1] : 0)) / kBlk;
             }
-            const uint32_t my_s[2] = {li == 0 ? sc[0] : li == 1 ? sc[2] : li == 2 ? sc[4] : sc[6],
-                                      li == 0 ? sc[1] : li == 1 ? sc[3] : li == 2 ? sc[5] : sc[7]};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int64_t c = c8 + 2 * li + h;
-                if (!p.blocked) sb[c * (R / kBlk) + rb] = (uint8_t)my_s[h];
-                else if (ok) sb[blocked_off(c, pc, ct_col)] = (uint8_t)my_s[h];
-            }
+            uint8_t* w = sb + ((c >> 7) * ct_col + (pc >> 2)) * 512 + (c & 31) * 16 + ((c >> 5) & 3) * 4 + (pc & 3);
+            w[0] = (uint8_t)my;
+            w[16] = (uint8_t)(my >> 16);
         };
 
         if constexpr (kExt) {
@@ -545,7 +567,8 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
                     }
                 }
-                if (cval) store_row_scales(p.s_row, s8);
+                store_row_scales(p.s_row, s8[0] | (s8[1] << 8) | (s8[2] << 16) | (s8[3] << 24),
+                                 s8[4] | (s8[5] << 8) | (s8[6] << 16) | (s8[7] << 24));
             }
             if constexpr (kCol) {
                 uint32_t sc[8];
@@ -635,7 +658,9 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         if (cval) *reinterpret_cast<uint2*>(qb + (c8 + 4 * hc + j) * R + row0 + 8 * li) = q;
                     }
                 }
-                if (cval) store_col_scales(p.s_col, sc);
+                const uint32_t s2c[4] = {sc[0] | (sc[1] << 16), sc[2] | (sc[3] << 16), sc[4] | (sc[5] << 16),
+                                         sc[6] | (sc[7] << 16)};
+                store_col_scales(p.s_col, s2c);
             }
             release_stage();
             continue;
@@ -676,79 +701,72 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                                                   vmax_u16x2(mg[2 * k + 1][2], mg[2 * k + 1][3]));
                     pp[k] = vmax_u16x2(__byte_perm(a, c, 0x5410), __byte_perm(a, c, 0x7632));
                 }
-                uint32_t s8[8];
-                if constexpr (kB32) {
+                // s2[k]: scale bytes of rows 2k (low half) and 2k+1 (high half); 247 marks Inf/NaN
+                uint32_t s2[4];
 #pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) s8[rr] = sblk;
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < 4; ++k) {
+                    if constexpr (kB32) {
+                        s2[k] = min(sblk, 247u) * 0x00010001u;
+                    } else {
                         uint32_t m = shfl_xor_max16x2(pp[k], 1);
                         m = shfl_xor_max16x2(m, 2);
-                        s8[2 * k] = e8m0_from_absbits(m & 0xFFFFu);
-                        s8[2 * k + 1] = e8m0_from_absbits(m >> 16);
+                        s2[k] = e8m0_pair(m);
                     }
                 }
-                bool nonfinite = false;
+                uint32_t nf = 0;
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) nonfinite |= s8[rr] == 0xFFu;
-                const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
+                for (int k = 0; k < 4; ++k) nf |= s2[k] + kNonfiniteAdd;
+                const bool any_nonfinite = __any_sync(0xffffffffu, (nf & kNonfiniteBits) != 0u);
                 uint8_t* qb = q_row + b * R * C;
 #pragma unroll
                 for (int rr = 0; rr < 8; ++rr) {
                     const int64_t row = row0 + 8 * li + rr;
-                    uint2 q = quant8(v[rr], inv_scale_from_e8m0(s8[rr]));
-                    if (any_nonfinite && s8[rr] == 0xFFu) {
+                    uint2 q = quant8(v[rr], inv_scale_pair(s2[rr >> 1], rr & 1));
+                    if (any_nonfinite && pair_half(s2[rr >> 1], rr & 1) == 247u) {
                         const uint2 sg = signs8(v[rr]);
                         q.x = 0x7F7F7F7Fu | sg.x;
                         q.y = 0x7F7F7F7Fu | sg.y;
                     }
                     if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
                 }
-                // scales: the 4 lanes of a 32-column block each write two of the 8 rows
-                if (cval) {
-                    uint8_t* sb = s_row + b * p.s_row_bstride;
-                    const int64_t cb = c8 / kBlk;
-                    const int q4 = lj & 3;
-                    if constexpr (kB32Only) {
-                        if (li == 0 && q4 == 0) sb[(row0 / kBlk) * Cb + cb] = (uint8_t)s8[0];
-                    } else {
-                        store_row_scales(s_row, s8);
-                    }
+                if (any_nonfinite) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) s2[k] = fix_nonfinite_pair(s2[k]);
+                }
+                if constexpr (kB32Only) {
+                    // one compact scale per 32x32 block
+                    if (cval && li == 0 && (lj & 3) == 0) s_row[b * p.s_row_bstride + (row0 / kBlk) * Cb + c8 / kBlk] = (uint8_t)sblk;
+                } else {
+                    store_row_scales(s_row, __byte_perm(s2[0], s2[1], 0x6420), __byte_perm(s2[2], s2[3], 0x6420));
                 }
             }
 
             if constexpr (kCol) {
-                uint32_t sc[8];
-                if constexpr (kB32) {
+                // s2c[k]: scale bytes of this lane's columns 2k (low half) and 2k+1 (high half)
+                uint32_t s2c[4];
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) sc[cc] = sblk;
-                } else {
-                    // column amax over 32 rows: 8 here (packed pairs of columns), then lanes li = 0..3
-                    uint32_t cm[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < 4; ++k) {
+                    if constexpr (kB32) {
+                        s2c[k] = min(sblk, 247u) * 0x00010001u;
+                    } else {
+                        // column amax over 32 rows: 8 here (packed pairs of columns), then lanes li = 0..3
                         uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mg[0][k], mg[1][k]), vmax_u16x2(mg[2][k], mg[3][k])),
                                                 vmax_u16x2(vmax_u16x2(mg[4][k], mg[5][k]), vmax_u16x2(mg[6][k], mg[7][k])));
                         m = shfl_xor_max16x2(m, 8);
-                        cm[k] = shfl_xor_max16x2(m, 16);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        sc[2 * k] = e8m0_from_absbits(cm[k] & 0xFFFFu);
-                        sc[2 * k + 1] = e8m0_from_absbits(cm[k] >> 16);
+                        m = shfl_xor_max16x2(m, 16);
+                        s2c[k] = e8m0_pair(m);
                     }
                 }
-                bool nonfinite = false;
+                uint32_t nf = 0;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) nonfinite |= sc[cc] == 0xFFu;
-                const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
+                for (int k = 0; k < 4; ++k) nf |= s2c[k] + kNonfiniteAdd;
+                const bool any_nonfinite = __any_sync(0xffffffffu, (nf & kNonfiniteBits) != 0u);
                 uint8_t* qb = q_col + b * R * C;
                 if (cval) {
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc) {
-                        const float f = inv_scale_from_e8m0(sc[cc]);
                         const int k = cc >> 1;
+                        const float f = inv_scale_pair(s2c[k], cc & 1);
                         uint32_t w[4];
 #pragma unroll
                         for (int rr = 0; rr < 8; rr += 2) {
@@ -760,7 +778,7 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         uint2 q;
                         q.x = w[0] | (w[1] << 16);
                         q.y = w[2] | (w[3] << 16);
-                        if (any_nonfinite && sc[cc] == 0xFFu) {
+                        if (any_nonfinite && pair_half(s2c[k], cc & 1) == 247u) {
                             uint32_t sg[4];
 #pragma unroll
                             for (int rr = 0; rr < 8; rr += 2) {
@@ -773,8 +791,12 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         }
                         *reinterpret_cast<uint2*>(qb + (c8 + cc) * R + row0 + 8 * li) = q;
                     }
-                    store_col_scales(s_col, sc);
                 }
+                if (any_nonfinite) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) s2c[k] = fix_nonfinite_pair(s2c[k]);
+                }
+                store_col_scales(s_col, s2c);
             }
         };
 
