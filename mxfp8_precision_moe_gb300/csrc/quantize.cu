@@ -23,6 +23,8 @@
 // cvt.rn.satfinite.e4m3x2.  Stores are 8-byte vectors.  The grid is persistent
 // (a multiple of the SM count), striding over tiles.
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "host_common.h"
 
@@ -188,6 +190,47 @@ __device__ __forceinline__ float inv_scale_pair(uint32_t s, int h) {
     return __uint_as_float(h ? ((d << 7) & 0x7F800000u) : (d << 23));
 }
 __device__ __forceinline__ uint32_t pair_half(uint32_t s, int h) { return h ? s >> 16 : s & 0xFFFFu; }
+// Both inverse scales of a pair (halves <= 247) as bf16 bit patterns: (254 - s) << 7 in each half.
+__device__ __forceinline__ uint32_t inv_scale_pair_bf16(uint32_t s) { return (0x00FE00FEu - s) << 7; }
+
+// max(|a|, |b|) per bf16 half (NaN wins); the sign bits of the result are garbage (xor of the
+// inputs' signs) and are ignored by e8m0_pair.
+__device__ __forceinline__ uint32_t amax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t shfl_xor_amax(uint32_t v, int m) {
+    return amax_bf16x2(v, __shfl_xor_sync(0xffffffffu, v, m));
+}
+
+// The bf16 in half HW of w times the bf16 power of two in half HF of f2, as an exact fp32: one
+// mixed-precision fma with a -0 addend (keeps the sign of a zero product).
+template <int HW, int HF>
+__device__ __forceinline__ float scale_bf16(uint32_t w, uint32_t f2) {
+    float d;
+    if constexpr (HW == 0 && HF == 0)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a0, b0, 0f80000000;\n\t}" : "=f"(d) : "r"(w), "r"(f2));
+    else if constexpr (HW == 1 && HF == 0)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a1, b0, 0f80000000;\n\t}" : "=f"(d) : "r"(w), "r"(f2));
+    else if constexpr (HW == 0 && HF == 1)
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a0, b1, 0f80000000;\n\t}" : "=f"(d) : "r"(w), "r"(f2));
+    else
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, a1, b1, 0f80000000;\n\t}" : "=f"(d) : "r"(w), "r"(f2));
+    return d;
+}
+// Eight bf16 (4 packed words) times the scale in half HF of f2 -> eight E4M3 codes.
+template <int HF>
+__device__ __forceinline__ uint2 quant8_bf16(const uint32_t (&w)[4], uint32_t f2) {
+    uint32_t c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = cvt_e4m3x2(scale_bf16<0, HF>(w[k], f2), scale_bf16<1, HF>(w[k], f2));
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
 
 __device__ __forceinline__ uint32_t shfl_xor_max16x2(uint32_t v, int m) {
     return vmax_u16x2(v, __shfl_xor_sync(0xffffffffu, v, m));
@@ -669,13 +712,8 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
         // the plain MX quantization of one 8 x 8 patch per lane (bf16 pairs v) into one output set
         auto quant_rowcol = [&](const uint32_t (&v)[8][4], uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                                 uint8_t* s_col) {
-            // magnitude bits of every element (bf16 pairs), shared by both directions
-            uint32_t mg[8][4];
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) mg[rr][k] = v[rr][k] & 0x7FFF7FFFu;
-
+            // amaxes are taken on the raw bf16 pairs (max of magnitudes; the sign bits they carry are
+            // ignored when the scale byte is read off the exponent field)
             uint32_t sblk = 0;  // the 32x32 block's scale
             if constexpr (kB32) {
                 // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1), 4 down (li)
@@ -683,24 +721,15 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
 #pragma unroll
                 for (int rr = 0; rr < 8; ++rr)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) m = vmax_u16x2(m, mg[rr][k]);
-                m = shfl_xor_max16x2(m, 1);
-                m = shfl_xor_max16x2(m, 2);
-                m = shfl_xor_max16x2(m, 8);
-                m = shfl_xor_max16x2(m, 16);
-                sblk = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
+                    for (int k = 0; k < 4; ++k) m = amax_bf16x2(m, v[rr][k]);
+                m = shfl_xor_amax(m, 1);
+                m = shfl_xor_amax(m, 2);
+                m = shfl_xor_amax(m, 8);
+                m = shfl_xor_amax(m, 16);
+                sblk = e8m0_from_absbits(max(m & 0x7FFFu, (m >> 16) & 0x7FFFu));
             }
 
             if constexpr (kRowOut) {
-                // two rows per word: pp[k] = (amax of row 2k, amax of row 2k+1) over this lane's 8 columns
-                uint32_t pp[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t a = vmax_u16x2(vmax_u16x2(mg[2 * k][0], mg[2 * k][1]), vmax_u16x2(mg[2 * k][2], mg[2 * k][3]));
-                    const uint32_t c = vmax_u16x2(vmax_u16x2(mg[2 * k + 1][0], mg[2 * k + 1][1]),
-                                                  vmax_u16x2(mg[2 * k + 1][2], mg[2 * k + 1][3]));
-                    pp[k] = vmax_u16x2(__byte_perm(a, c, 0x5410), __byte_perm(a, c, 0x7632));
-                }
                 // s2[k]: scale bytes of rows 2k (low half) and 2k+1 (high half); 247 marks Inf/NaN
                 uint32_t s2[4];
 #pragma unroll
@@ -708,8 +737,13 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                     if constexpr (kB32) {
                         s2[k] = min(sblk, 247u) * 0x00010001u;
                     } else {
-                        uint32_t m = shfl_xor_max16x2(pp[k], 1);
-                        m = shfl_xor_max16x2(m, 2);
+                        // (amax of row 2k, amax of row 2k+1) over this lane's 8 columns, then its 4 lanes
+                        const uint32_t a = amax_bf16x2(amax_bf16x2(v[2 * k][0], v[2 * k][1]), amax_bf16x2(v[2 * k][2], v[2 * k][3]));
+                        const uint32_t c = amax_bf16x2(amax_bf16x2(v[2 * k + 1][0], v[2 * k + 1][1]),
+                                                       amax_bf16x2(v[2 * k + 1][2], v[2 * k + 1][3]));
+                        uint32_t m = amax_bf16x2(__byte_perm(a, c, 0x5410), __byte_perm(a, c, 0x7632));
+                        m = shfl_xor_amax(m, 1);
+                        m = shfl_xor_amax(m, 2);
                         s2[k] = e8m0_pair(m);
                     }
                 }
@@ -719,15 +753,20 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                 const bool any_nonfinite = __any_sync(0xffffffffu, (nf & kNonfiniteBits) != 0u);
                 uint8_t* qb = q_row + b * R * C;
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    const int64_t row = row0 + 8 * li + rr;
-                    uint2 q = quant8(v[rr], inv_scale_pair(s2[rr >> 1], rr & 1));
-                    if (any_nonfinite && pair_half(s2[rr >> 1], rr & 1) == 247u) {
-                        const uint2 sg = signs8(v[rr]);
-                        q.x = 0x7F7F7F7Fu | sg.x;
-                        q.y = 0x7F7F7F7Fu | sg.y;
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t f2 = inv_scale_pair_bf16(s2[k]);
+                    uint2 q[2] = {quant8_bf16<0>(v[2 * k], f2), quant8_bf16<1>(v[2 * k + 1], f2)};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int rr = 2 * k + h;
+                        const int64_t row = row0 + 8 * li + rr;
+                        if (any_nonfinite && pair_half(s2[k], h) == 247u) {
+                            const uint2 sg = signs8(v[rr]);
+                            q[h].x = 0x7F7F7F7Fu | sg.x;
+                            q[h].y = 0x7F7F7F7Fu | sg.y;
+                        }
+                        if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q[h];
                     }
-                    if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
                 }
                 if (any_nonfinite) {
 #pragma unroll
@@ -750,10 +789,10 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         s2c[k] = min(sblk, 247u) * 0x00010001u;
                     } else {
                         // column amax over 32 rows: 8 here (packed pairs of columns), then lanes li = 0..3
-                        uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mg[0][k], mg[1][k]), vmax_u16x2(mg[2][k], mg[3][k])),
-                                                vmax_u16x2(vmax_u16x2(mg[4][k], mg[5][k]), vmax_u16x2(mg[6][k], mg[7][k])));
-                        m = shfl_xor_max16x2(m, 8);
-                        m = shfl_xor_max16x2(m, 16);
+                        uint32_t m = amax_bf16x2(amax_bf16x2(amax_bf16x2(v[0][k], v[1][k]), amax_bf16x2(v[2][k], v[3][k])),
+                                                 amax_bf16x2(amax_bf16x2(v[4][k], v[5][k]), amax_bf16x2(v[6][k], v[7][k])));
+                        m = shfl_xor_amax(m, 8);
+                        m = shfl_xor_amax(m, 16);
                         s2c[k] = e8m0_pair(m);
                     }
                 }
@@ -762,34 +801,36 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                 for (int k = 0; k < 4; ++k) nf |= s2c[k] + kNonfiniteAdd;
                 const bool any_nonfinite = __any_sync(0xffffffffu, (nf & kNonfiniteBits) != 0u);
                 uint8_t* qb = q_col + b * R * C;
+                // codes of column 2k + h: elements (rr, half h of word k) times half h of the scale pair
+                auto col_codes = [&](auto hc, int k, uint32_t f2) -> uint2 {
+                    constexpr int h = decltype(hc)::value;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int rr = 0; rr < 8; rr += 2)
+                        w[rr >> 1] = cvt_e4m3x2(scale_bf16<h, h>(v[rr][k], f2), scale_bf16<h, h>(v[rr + 1][k], f2));
+                    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+                };
                 if (cval) {
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const int k = cc >> 1;
-                        const float f = inv_scale_pair(s2c[k], cc & 1);
-                        uint32_t w[4];
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t f2 = inv_scale_pair_bf16(s2c[k]);
+                        uint2 q[2] = {col_codes(std::integral_constant<int, 0>{}, k, f2),
+                                      col_codes(std::integral_constant<int, 1>{}, k, f2)};
 #pragma unroll
-                        for (int rr = 0; rr < 8; rr += 2) {
-                            const float a = (cc & 1) ? bf16hi(v[rr][k]) : bf16lo(v[rr][k]);
-                            const float c = (cc & 1) ? bf16hi(v[rr + 1][k]) : bf16lo(v[rr + 1][k]);
-                            const float2 y = mul2(a, c, f);
-                            w[rr >> 1] = cvt_e4m3x2(y.x, y.y);
-                        }
-                        uint2 q;
-                        q.x = w[0] | (w[1] << 16);
-                        q.y = w[2] | (w[3] << 16);
-                        if (any_nonfinite && pair_half(s2c[k], cc & 1) == 247u) {
-                            uint32_t sg[4];
+                        for (int h = 0; h < 2; ++h) {
+                            if (any_nonfinite && pair_half(s2c[k], h) == 247u) {
+                                uint32_t sg[4];
 #pragma unroll
-                            for (int rr = 0; rr < 8; rr += 2) {
-                                const uint32_t a = (cc & 1) ? (v[rr][k] >> 31) : ((v[rr][k] >> 15) & 1u);
-                                const uint32_t c = (cc & 1) ? (v[rr + 1][k] >> 31) : ((v[rr + 1][k] >> 15) & 1u);
-                                sg[rr >> 1] = (a << 7) | (c << 15);
+                                for (int rr = 0; rr < 8; rr += 2) {
+                                    const uint32_t a = h ? (v[rr][k] >> 31) : ((v[rr][k] >> 15) & 1u);
+                                    const uint32_t c = h ? (v[rr + 1][k] >> 31) : ((v[rr + 1][k] >> 15) & 1u);
+                                    sg[rr >> 1] = (a << 7) | (c << 15);
+                                }
+                                q[h].x = 0x7F7F7F7Fu | sg[0] | (sg[1] << 16);
+                                q[h].y = 0x7F7F7F7Fu | sg[2] | (sg[3] << 16);
                             }
-                            q.x = 0x7F7F7F7Fu | sg[0] | (sg[1] << 16);
-                            q.y = 0x7F7F7F7Fu | sg[2] | (sg[3] << 16);
+                            *reinterpret_cast<uint2*>(qb + (c8 + 2 * k + h) * R + row0 + 8 * li) = q[h];
                         }
-                        *reinterpret_cast<uint2*>(qb + (c8 + cc) * R + row0 + 8 * li) = q;
                     }
                 }
                 if (any_nonfinite) {
