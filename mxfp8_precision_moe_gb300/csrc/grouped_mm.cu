@@ -614,6 +614,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
 // epilogue reports a drained accumulator to the even CTA with a remote mbarrier arrive.
 // ============================================================================================
 constexpr int kPairStages = 5;
+constexpr int kSortGroups = 128;  // K-grouped schedules rank at most this many groups (O(G^2) per CTA)
 
 struct CfgPair {
     static constexpr int BN = 256;
@@ -648,8 +649,10 @@ struct PairTile {
 };
 
 // Tile t of the pair schedule, seen from CTA `half` (0: rows 0-127 of the pair tile, 1: 128-255).
+// K-grouped: tile t belongs to the group at position t / per_g of gorder_s (or of the natural order).
 __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, int half, const int32_t* ends_s,
-                                              const int32_t* pstart_s, const int32_t* tstart_s, int64_t ptotal) {
+                                              const int32_t* pstart_s, const int32_t* tstart_s, int64_t ptotal,
+                                              const int32_t* gorder_s, bool sorted) {
     constexpr int BN = 256;
     PairTile ti;
     const int64_t ntb = (p.nb + BN - 1) / BN;
@@ -685,9 +688,10 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
     } else {
         const int64_t nta2 = (p.na + 255) / 256;
         const int64_t per_g = nta2 * ntb;
-        const int g = (int)(t / per_g);
+        const int gp = (int)(t / per_g);
+        const int g = sorted ? gorder_s[gp] : gp;
         int64_t m2, n;
-        band_split(t - g * per_g, nta2, ntb, m2, n);
+        band_split(t - gp * per_g, nta2, ntb, m2, n);
         const int64_t start = g ? ends_s[g - 1] : 0, size = ends_s[g] - start;
         const int64_t ct = ptotal / 128, kt0 = pstart_s[g] / 128;
         const int64_t rows0 = m2 * 256 + half * 128;
@@ -718,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int32_t ends_s[kMaxGroups];
     __shared__ int32_t pstart_s[kMaxGroups];
     __shared__ int32_t tstart_s[kMaxGroups];  // ROWGROUPED: first pair tile (256 rows) of each group
+    __shared__ int32_t gorder_s[kMaxGroups];  // K-grouped, G <= kSortGroups: groups by size, largest first
     __shared__ int32_t ptotal_s;
     __shared__ int32_t bad_s;
     __shared__ uint32_t tmem_base_s;
@@ -822,13 +827,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             ntiles = (int64_t)p.G * ((p.na + 255) / 256) * ntb;
         }
         const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+        // K-grouped (wgrad) tiles cost their group's k-tiles (tokens / 128), so plain round robin leaves
+        // the clusters' totals several percent apart.  With few groups the schedule takes the groups
+        // largest first and deals each round of ncl tiles out in alternating cluster order (snake):
+        // on the 8-expert Scout-like token split, busiest cluster 1.01x the mean instead of 1.04x.
+        // Both CTAs of a pair derive the same order; every role walks the same sequence.
+        const bool sorted = p.mode == KGROUPED && p.G <= kSortGroups;
+        if (sorted) {
+            for (int g = threadIdx.x; g < p.G; g += blockDim.x) {
+                const int32_t sg = ends_s[g] - (g ? ends_s[g - 1] : 0);
+                int r = 0;
+                for (int h = 0; h < p.G; ++h) {
+                    const int32_t sh = ends_s[h] - (h ? ends_s[h - 1] : 0);
+                    r += (sh > sg) || (sh == sg && h < g);
+                }
+                gorder_s[r] = g;
+            }
+        }
+        __syncthreads();
+        auto tile_at = [&](int64_t j) -> int64_t { return j * ncl + ((sorted && (j & 1)) ? ncl - 1 - cid : cid); };
 
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
             int stage = 0;
             uint32_t phase = 0;
-            for (int64_t t = cid; t < ntiles; t += ncl) {
-                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal);
+            for (int64_t j = 0; j * ncl < ntiles; ++j) {
+                const int64_t t = tile_at(j);
+                if (t >= ntiles) continue;
+                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 bool ok = true;
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
@@ -856,8 +882,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             constexpr uint32_t idesc0 = idesc_mxf8(256, BN, 0, 0);
-            for (int64_t t = cid; t < ntiles && ok; t += ncl) {
-                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal);
+            for (int64_t j = 0; j * ncl < ntiles && ok; ++j) {
+                const int64_t t = tile_at(j);
+                if (t >= ntiles) continue;
+                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 if (ti.k_tiles == 0) continue;
                 if (!mbar_wait_bounded(tempty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
@@ -900,8 +928,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* stg = smem + C::kOffStage + (warp - 2) * (32 * 128);
             const uint32_t tempty_leader = cluster_addr(tempty, 0);
             uint32_t acc_phase = 0;
-            for (int64_t t = cid; t < ntiles; t += ncl) {
-                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal);
+            for (int64_t j = 0; j * ncl < ntiles; ++j) {
+                const int64_t t = tile_at(j);
+                if (t >= ntiles) continue;
+                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo;
                 const int vrows = ti.valid_rows - quarter * 32;
                 if (ti.k_tiles == 0) {
