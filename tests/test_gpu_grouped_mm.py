@@ -133,6 +133,26 @@ def test_wgrad(mx, sizes, N, K):
     assert_gemm_close(got, ref, what="wgrad")
 
 
+@pytest.mark.parametrize("G", [100, 140])
+def test_wgrad_many_groups(mx, G):
+    """Many small token groups (multiples of 32, a fifth of them empty) through the CTA-pair wgrad:
+    G <= 128 runs the schedule that ranks groups by size (ties between equal sizes included),
+    G > 128 the plain round-robin one.  Every group's dW against the oracle; empty groups zero."""
+    rng = np.random.default_rng(G)
+    sizes = [int(x) for x in rng.integers(0, 6, G) * 32]
+    for g in rng.choice(G, G // 5, replace=False):
+        sizes[int(g)] = 0
+    M, N, K = sum(sizes), 160, 288   # N = 160: the pair's second CTA holds 32 valid rows
+    D = synth.randn_bf16((M, N), 1e-3, seed=G + 11)
+    A = synth.randn_bf16((M, K), 1.0, seed=G + 13)
+    got = gpu_wgrad(mx, D, A, sizes)
+    ref = oracle_wgrad(D, A, sizes)
+    for g, m in enumerate(sizes):
+        if m == 0:
+            assert np.all(got[g] == 0.0), f"empty group {g} must give zero dW"
+    assert_gemm_close(got, ref, what=f"wgrad G={G}")
+
+
 def test_identity_weights_exact(mx):
     """W[g] = I: every weight scale is 2^-8 and every diagonal code 256, so the
     product is the dequantized activation, exact in fp32; bf16 rounding of that
