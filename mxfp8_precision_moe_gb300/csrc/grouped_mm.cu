@@ -453,15 +453,28 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                 const bool rvalid = r < ti.valid_rows;          // this row lies inside the group
                 const int64_t row = ti.a_row + r;
                 const int64_t c0 = ti.col0 + 32 * jb;           // first column of the block
-                if (bvalid && rvalid) {
-                    uint4* g1 = reinterpret_cast<uint4*>(p.out + row * H + c0);
-                    uint4* g3 = reinterpret_cast<uint4*>(p.out2 + row * H + c0);
+                // h1 and h3 through the warp's 1 KB staging buffer, 16 columns (32 bytes) of each of the
+                // 32 rows per pass, so every store instruction writes 16 whole 32-byte row segments
+                // instead of 32 scattered 16-byte pieces.  Chunk c of row l sits at l * 32 + 16 (c ^ s),
+                // s = (l >> 2) & 1, which spreads a pass's writes over all banks.
+                auto stage_store = [&](const uint32_t* w, __nv_bfloat16* dst_base, int h) {
+                    const int sw = (lane >> 2) & 1;
+                    st_shared_v4(stg + lane * 32 + 16 * (0 ^ sw), make_uint4(w[0], w[1], w[2], w[3]));
+                    st_shared_v4(stg + lane * 32 + 16 * (1 ^ sw), make_uint4(w[4], w[5], w[6], w[7]));
+                    __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        g1[i] = make_uint4(hg[4 * i], hg[4 * i + 1], hg[4 * i + 2], hg[4 * i + 3]);
-                        g3[i] = make_uint4(hu[4 * i], hu[4 * i + 1], hu[4 * i + 2], hu[4 * i + 3]);
+                    for (int k = 0; k < 2; ++k) {
+                        const int rl = (lane >> 1) + 16 * k, ch = lane & 1;
+                        const uint4 v = ld_shared_v4(stg + rl * 32 + 16 * (ch ^ ((rl >> 2) & 1)));
+                        if (bvalid && quarter * 32 + rl < ti.valid_rows)
+                            *reinterpret_cast<uint4*>(dst_base + (ti.a_row + quarter * 32 + rl) * H + c0 + 16 * h + 8 * ch) = v;
                     }
-                }
+                    __syncwarp();
+                };
+                stage_store(hg, p.out, 0);
+                stage_store(hg + 8, p.out, 1);
+                stage_store(hu, p.out2, 0);
+                stage_store(hu + 8, p.out2, 1);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float a = bf16lo(hg[i]), b = bf16hi(hg[i]);
