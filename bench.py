@@ -45,7 +45,7 @@ L2_BYTES = 129 * 2 ** 20
 # DRAM traffic of one grouped-GEMM forward launch on this workload, from the
 # ncu capture summarised in profiles/grouped_mm_fwd_scout.md, valid only while
 # the kernel sources hash to the value recorded with it.
-FWD_TRAFFIC = {"bytes": 761294336, "src_sha": "47c6ea314d90ea5c"}
+FWD_TRAFFIC = {"bytes": 771875584, "src_sha": "d06a053bdd32ff51"}
 
 
 WORKLOAD_TEXT = {
