@@ -326,6 +326,34 @@ def test_full_size_sweep_sampled(mx, oracle_lib, M, K):
         assert np.array_equal(u8(s32[br]), so[0])
 
 
+def test_full_size_single_directions_sampled(mx, oracle_lib):
+    """The row-only and column-only launches the sweep times, at its largest 5120-wide shape, and the
+    3D expert weights [16, 8192, 5120] quantized along K only and along N only: sampled rows and
+    columns byte-exact against the oracle (codes and blocked scales)."""
+    M, K = 131072, 5120
+    x = synth.log_uniform_rows(M, K, seed=13, device="cuda")
+    status = mx.new_status()
+    q, s, _, _ = mx.mxfp8_quantize_2d(x, mx.ROW, mx.SCALES_BLOCKED, None, status)
+    mx.read_status(status)
+    _check_rows_sampled(oracle_lib, x, q, s, _sample_rows(M, 32, 8))
+    del q, s
+    _, _, qT, sT = mx.mxfp8_quantize_2d(x, mx.COL, mx.SCALES_BLOCKED, None, status)
+    mx.read_status(status)
+    _check_cols_sampled(oracle_lib, x, qT, sT, _sample_rows(K, 3, 9))
+    del x, qT, sT
+    G, N, K = 16, 8192, 5120
+    w = synth.randn_bf16((G, N, K), 0.02, seed=4, device="cuda")
+    q, s, _, _ = mx.mxfp8_quantize_3d_experts(w, mx.ROW, mx.SCALES_BLOCKED, status)
+    mx.read_status(status)
+    for g in (1, 14):
+        _check_rows_sampled(oracle_lib, w[g], q[g], s[g], _sample_rows(N, 8, 20 + g))
+    del q, s
+    _, _, qT, sT = mx.mxfp8_quantize_3d_experts(w, mx.COL, mx.SCALES_BLOCKED, status)
+    mx.read_status(status)
+    for g in (2, 15):
+        _check_cols_sampled(oracle_lib, w[g], qT[g], sT[g], _sample_rows(K, 2, 30 + g))
+
+
 def test_full_size_3d_weights_sampled(mx, oracle_lib):
     G, N, K = 16, 8192, 5120
     w = synth.randn_bf16((G, N, K), 0.02, seed=2, device="cuda")
