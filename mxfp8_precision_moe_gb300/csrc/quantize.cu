@@ -17,11 +17,12 @@
 // and columns 8j..8j+7 of it in registers (8 x 16-byte loads; every warp load
 // instruction reads four fully used 128-byte row segments).  Row blocks of 32
 // span 4 lanes (2 shuffles), column blocks of 32 span the 4 lanes i = 0..3
-// (2 shuffles); amax is an integer max over bf16 magnitude bits (two per
-// max.u16x2), the scale byte comes from the exponent field, the elements are
-// multiplied by 2^(127-s) exactly in fp32 and converted with
-// cvt.rn.satfinite.e4m3x2.  Stores are 8-byte vectors.  The grid is persistent
-// (a multiple of the SM count), striding over tiles.
+// (2 shuffles); amax is max.NaN.xorsign.abs.bf16x2 on the raw bf16 pairs, two
+// scale bytes come from the exponent fields with one packed max and subtract,
+// each element is scaled by 2^(127-s) with one mixed-precision bf16 fma (exact)
+// and pairs are converted with cvt.rn.satfinite.e4m3x2.  Code stores are 8-byte
+// vectors; a row's scale bytes of a warp leave as one 16/32-bit store.  The grid
+// is persistent (a multiple of the SM count), striding over tiles.
 
 #include <type_traits>
 
@@ -173,7 +174,8 @@ constexpr float kRhtScale = 0x1.6a09e6p-3f;  // fp32(1 / sqrt(32))
 
 // Scale bytes of two blocks at once from their packed bf16 magnitude amaxes (one per 16-bit half):
 // s = max(E - 8, 0) per half, E the exponent field.  E = 255 (Inf/NaN) comes out as 247 here, a value
-// no finite amax gives; nonfinite_pairs() finds it and fix_nonfinite_pair() turns it into 0xFF.
+// no finite amax gives; adding kNonfiniteAdd and testing kNonfiniteBits finds it, and
+// fix_nonfinite_pair() turns it into 0xFF.
 __device__ __forceinline__ uint32_t e8m0_pair(uint32_t m) {
     return vmax_u16x2((m >> 7) & 0x00FF00FFu, 0x00080008u) - 0x00080008u;
 }
@@ -182,12 +184,6 @@ constexpr uint32_t kNonfiniteAdd = 0x00090009u, kNonfiniteBits = 0x01000100u;
 __device__ __forceinline__ uint32_t fix_nonfinite_pair(uint32_t s) {
     const uint32_t lo = s & 0xFFFFu, hi = s >> 16;
     return (lo == 247u ? 0xFFu : lo) | ((hi == 247u ? 0xFFu : hi) << 16);
-}
-// 2^(127 - s) for the low (h = 0) or high (h = 1) half of a scale pair with both halves <= 247:
-// the fp32 exponent field 254 - s, taken from the packed difference.
-__device__ __forceinline__ float inv_scale_pair(uint32_t s, int h) {
-    const uint32_t d = 0x00FE00FEu - s;
-    return __uint_as_float(h ? ((d << 7) & 0x7F800000u) : (d << 23));
 }
 __device__ __forceinline__ uint32_t pair_half(uint32_t s, int h) { return h ? s >> 16 : s & 0xFFFFu; }
 // Both inverse scales of a pair (halves <= 247) as bf16 bit patterns: (254 - s) << 7 in each half.
@@ -230,37 +226,6 @@ __device__ __forceinline__ uint2 quant8_bf16(const uint32_t (&w)[4], uint32_t f2
 #pragma unroll
     for (int k = 0; k < 4; ++k) c[k] = cvt_e4m3x2(scale_bf16<0, HF>(w[k], f2), scale_bf16<1, HF>(w[k], f2));
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
-__device__ __forceinline__ uint32_t shfl_xor_max16x2(uint32_t v, int m) {
-    return vmax_u16x2(v, __shfl_xor_sync(0xffffffffu, v, m));
-}
-
-// (a*f, c*f) with one packed fp32x2 multiply (exact: f is a power of two).
-__device__ __forceinline__ float2 mul2(float a, float c, float f) {
-    float2 r;
-    asm("{\n\t.reg .b64 x, y, d;\n\t"
-        "mov.b64 x, {%2, %3};\n\t"
-        "mov.b64 y, {%4, %4};\n\t"
-        "mul.rn.f32x2 d, x, y;\n\t"
-        "mov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a), "f"(c), "f"(f));
-    return r;
-}
-
-// One bf16 pair times f -> two E4M3 codes (16 bits).
-__device__ __forceinline__ uint32_t quant2(uint32_t w, float f) {
-    const float2 y = mul2(bf16lo(w), bf16hi(w), f);
-    return cvt_e4m3x2(y.x, y.y);
-}
-
-// Eight bf16 (4 packed words) times f -> eight E4M3 codes (little-endian in a u64).
-__device__ __forceinline__ uint2 quant8(const uint32_t (&w)[4], float f) {
-    uint2 r;
-    r.x = quant2(w[0], f) | (quant2(w[1], f) << 16);
-    r.y = quant2(w[2], f) | (quant2(w[3], f) << 16);
-    return r;
 }
 
 // Sign bits of eight bf16 moved to bit 7 of each byte; used to give the codes
