@@ -96,3 +96,41 @@ def test_argument_errors_need_no_device(lib):
     assert lib.mxfp8_grouped_mm_dgrad(fake, fake, fake, fake, None, 2, 64, 64, 64, fake, None, None) == 1
     assert lib.mxfp8_grouped_mm_wgrad(fake, fake, fake, fake, fake, 2, 48, 64, 64, fake, None, None) == 3
     assert lib.mxfp8_quantize_3d_experts(fake, 0, 64, 64, 1, 0, fake, fake, None, None, None, None) == 2
+
+
+def test_argument_errors_of_the_fused_and_option_calls(lib):
+    """The calls added for the SwiGLU expert, the stability variants, the 32x32 weights and the
+    two-operand dgrad reject bad arguments before touching a device as well."""
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    odd = P((1 << 20) + 8)  # 8-byte aligned only
+    q2o = lib.mxfp8_quantize_2d_opts
+    # unknown option bit; an option with 32x32 blocks; Hadamard on a copy that is not written
+    assert q2o(fake, 64, 64, 3, 1, None, 0, 8, 0, fake, fake, fake, fake, None, None) == 4
+    assert q2o(fake, 64, 64, 4, 0, None, 0, 1, 0, fake, fake, None, None, None, None) == 4
+    assert q2o(fake, 64, 64, 2, 1, None, 0, 2, 0, None, None, fake, fake, None, None) == 4
+    assert q2o(fake, 64, 64, 1, 1, None, 0, 4, 0, fake, fake, None, None, None, None) == 4
+    # 3D experts: 32x32 blocks need ROW and/or COL; the transposed copy needs its buffers
+    assert lib.mxfp8_quantize_3d_experts(fake, 2, 64, 64, 4, 1, fake, fake, None, None, None, None) == 4
+    assert lib.mxfp8_quantize_3d_experts(fake, 2, 64, 64, 4 | 2, 1, None, None, None, fake, None, None) == 1
+    # fused gate/up GEMM: (x, xs, wg, wgs, wu, wus, offs, G, M, H, D, h1, h3, hq, hs, hTq, hTs, status, stream)
+    sw = lib.mxfp8_grouped_mm_swiglu_fwd
+    ok = [fake] * 7
+    assert sw(*ok[:4], None, fake, fake, 2, 64, 64, 64, fake, fake, fake, fake, None, None, None, None) == 1
+    assert sw(*ok, 2, 64, 64, 64, fake, fake, fake, fake, fake, None, None, None) == 1   # hT_q without hT_s
+    assert sw(*ok, 0, 64, 64, 64, fake, fake, fake, fake, None, None, None, None) == 2
+    assert sw(*ok, 2, 64, 48, 64, fake, fake, fake, fake, None, None, None, None) == 3   # H % 32
+    assert sw(*ok, 2, 40, 64, 64, fake, fake, fake, fake, fake, fake, None, None) == 3   # token-wise, M % 32
+    assert sw(*ok, 2, 64, 64, 64, odd, fake, fake, fake, None, None, None, None) == 3
+    # fused SwiGLU backward: (dh, h1, h3, M, H, offs, G, 8 outputs, status, stream)
+    bw = lib.mxfp8_swiglu_bwd_quantize
+    assert bw(fake, fake, None, 64, 64, fake, 2, *[fake] * 8, None, None) == 1
+    assert bw(fake, fake, fake, 64, 64, fake, 0, *[fake] * 8, None, None) == 2
+    assert bw(fake, fake, fake, 40, 64, fake, 2, *[fake] * 8, None, None) == 3
+    assert bw(fake, fake, fake, 64, 64, fake, 2, *[fake] * 7, odd, None, None) == 3
+    # two-operand dgrad: (d1, d1s, w1, w1s, d2, d2s, w2, w2s, offs, G, M, N, K, dA, status, stream)
+    d2 = lib.mxfp8_grouped_mm_dgrad2
+    assert d2(*[fake] * 4, None, fake, fake, fake, fake, 2, 64, 64, 64, fake, None, None) == 1
+    assert d2(*[fake] * 4, fake, None, fake, fake, fake, 2, 64, 64, 64, fake, None, None) == 1
+    assert d2(*[fake] * 6, odd, fake, fake, 2, 64, 64, 64, fake, None, None) == 3
+    assert d2(*[fake] * 9, 2, 64, 48, 64, fake, None, None) == 3                        # contraction N % 32
