@@ -35,13 +35,16 @@
  * independently in the tests, torch's float8_e4m3fn cast on unsaturated values,
  * round-trip error bounds, transpose invariance, blocked-layout bijection and
  * hand-computed positions, brute-force tiny GEMMs, the identity-weight case.
- * NaN/Inf input blocks: parity unpinned (one hand-made block only).
+ * NaN/Inf input blocks: the OCP NaN scale (every element dequantizes to NaN)
+ * and torch's float8_e4m3fn cast of a NaN with each element's sign.
  * SwiGLU stage: bf16 rounding pinned against torch's fp32->bf16 cast, hand
  * ties and a double-rounding case; silu against torch's fp64 silu.
  * Stability variants: Philox4x32-10 against its published known-answer
- * vectors; stochastic rounding by hand cases, exactness on the grid and its
- * mean; the Hadamard butterflies against scipy's Hadamard matrix on inputs
- * where fp32 is exact, and orthogonality.
+ * vectors; the Hadamard signs and the stochastic-rounding words (which output
+ * word, which counter) against values written by an independent pure-Python
+ * Philox4x32-10 (tests/golden/stability_words.txt); stochastic rounding by hand
+ * cases, exactness on the grid and its mean; the Hadamard butterflies against
+ * scipy's Hadamard matrix on inputs where fp32 is exact, and orthogonality.
  */
 #include <math.h>
 #include <stdint.h>
@@ -149,7 +152,7 @@ static uint8_t quantize_block_f64_rw(const double* v, int64_t n, uint8_t* q, int
     }
     if (nonfinite) {
         /* Reading for non-finite input (the pages are silent): NaN scale and
-         * NaN codes with the element's sign.  Parity unpinned. */
+         * NaN codes with the element's sign. */
         for (int64_t i = 0; i < n; ++i) q[i * qstride] = (uint8_t)(0x7F | (signbit(v[i]) ? 0x80 : 0));
         return E8M0_NAN;
     }

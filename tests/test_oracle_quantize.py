@@ -180,8 +180,40 @@ def test_32x32_transpose_invariant_and_max_of_row_scales(oracle_lib):
 
 
 def test_nonfinite_block_reading(oracle_lib):
-    # Parity unpinned: one hand-made block for the NaN/Inf reading.
+    """The reading for a block holding Inf or NaN (the pages are silent): the E8M0 NaN scale 0xFF,
+    which the OCP MX format defines as making every element of its block NaN, and each code the
+    E4M3 NaN carrying the element's own sign.  Pinned against two things outside the oracle: the
+    block dequantizes to all-NaN through the format definition, and every code equals torch's
+    float8_e4m3fn cast of a NaN with the element's sign (its NaN encoding 0x7F / 0xFF); blocks
+    without a non-finite value next to it are quantized as usual."""
     vals = np.zeros(32)
     vals[0], vals[1], vals[2] = np.inf, -1.0, 2.0
     q, s = oracle_lib.quantize_vec(bf16_bits(vals))
     assert s[0] == 0xFF and q[0] == 0x7F and q[1] == 0xFF and q[2] == 0x7F
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((8, 96)) * 10.0 ** rng.uniform(-3, 3, (8, 1))
+    x[rng.random(x.shape) < 0.05] = 0.0
+    x[rng.random(x.shape) < 0.05] *= -0.0
+    planted = [(0, 3, np.inf), (1, 40, -np.inf), (2, 70, np.nan), (3, 0, -np.nan), (3, 31, np.inf),
+               (5, 33, np.nan), (5, 34, -np.inf), (7, 95, -np.inf)]
+    for r, c, v in planted:
+        x[r, c] = v
+    xb = bf16_bits(x.ravel()).reshape(x.shape)
+    q, s = oracle_lib.quantize_rows(xb)
+    xv = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).float()
+    nan_signed = torch.where(torch.signbit(xv), -torch.tensor(float("nan")), torch.tensor(float("nan")))
+    want_nan_codes = nan_signed.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    bad_blocks = {(r, c // 32) for r, c, _ in planted}
+    qc, sc = oracle_lib.quantize_rows(np.where(np.isfinite(xv.numpy()), xb, np.uint16(0)).astype(np.uint16))
+    for r in range(8):
+        for b in range(3):
+            sl = slice(32 * b, 32 * b + 32)
+            if (r, b) in bad_blocks:
+                assert s[r, b] == 0xFF
+                assert np.all(np.isnan(oracle_lib.dequant(q[r, sl], np.full(32, s[r, b], np.uint8))))
+                assert np.array_equal(q[r, sl], want_nan_codes[r, sl])
+            else:
+                assert s[r, b] == sc[r, b] and np.array_equal(q[r, sl], qc[r, sl])
+    # the column and 32x32 forms follow the same reading
+    qT, sT = oracle_lib.quantize_cols(np.ascontiguousarray(np.tile(xb, (4, 1))))
+    assert sT[3, 0] == 0xFF and np.array_equal(qT[3, :32], np.tile(want_nan_codes[:, 3], 4))

@@ -1,6 +1,8 @@
 """Pins of the oracle's stability variants ("MXFP8 (Micro-scaling FP8)", "Numerical
 stability": random Hadamard transforms and stochastic rounding), no GPU:
 - Philox4x32-10 against the published known-answer vectors (tests/golden);
+- the Hadamard signs and the stochastic-rounding words against values written by an independent
+  pure-Python Philox4x32-10 (tests/golden/stability_words.txt, make_stability_words.py);
 - stochastic rounding against hand-worked cases, against an independent fp32 bit-pattern
   algorithm (add the top 20 random bits to the 20 mantissa bits E4M3 drops, truncate) on the
   normal E4M3 range, and for unbiasedness;
@@ -28,13 +30,44 @@ def test_philox_known_answers(row):
     assert oracle.philox4x32_10(row[0:4], row[4:6]) == row[6:10]
 
 
-def test_sr_word_is_word_n_mod_4_of_counter_n_div_4():
-    seed = 0x0123456789ABCDEF
-    for n in (0, 1, 2, 3, 4, 7, 12345, 2 ** 34 + 5):
-        for d in (0, 1):
-            w = oracle.philox4x32_10([(n >> 2) & 0xFFFFFFFF, (n >> 34) & 0xFFFFFFFF, d, 0],
-                                     [seed & 0xFFFFFFFF, seed >> 32])
-            assert oracle.sr_word(seed, n, d) == w[n & 3]
+STAB = os.path.join(os.path.dirname(__file__), "golden", "stability_words.txt")
+
+
+def stability_rows(kind):
+    for line in open(STAB):
+        f = line.split()
+        if f and f[0] == kind:
+            yield f[1:]
+
+
+def test_independent_philox_meets_the_known_answers():
+    """The pure-Python generator that wrote stability_words.txt reproduces the published vectors."""
+    from tests.golden import make_stability_words as ref
+    for row in kat_rows():
+        assert ref.philox4x32_10(row[0:4], row[4:6]) == row[6:10]
+
+
+@pytest.mark.parametrize("seed,n,d,word", list(stability_rows("sr")))
+def test_sr_word_golden(seed, n, d, word):
+    """oracle_sr_word against words written by an independent Philox (tests/golden/stability_words.txt):
+    word n mod 4 of counter (n / 4, n / 2^34, dir, 0), key = the seed's two halves."""
+    assert oracle.sr_word(int(seed, 16), int(n, 16), int(d)) == int(word, 16)
+
+
+def test_golden_words_tell_plausible_misreadings_apart():
+    """The stored words pin the selection: a wrong word index, a counter high word taken at bit 32
+    instead of 34, or the two directions swapped each give other words for the golden triples."""
+    from tests.golden import make_stability_words as ref
+    M = 0xFFFFFFFF
+    for seed, n, d, word in stability_rows("sr"):
+        seed, n, d, word = int(seed, 16), int(n, 16), int(d), int(word, 16)
+        key = [seed & M, seed >> 32]
+        out = ref.philox4x32_10([(n >> 2) & M, (n >> 34) & M, d, 0], key)
+        assert out[n & 3] == word
+        assert out[(n + 1) & 3] != word
+        assert ref.philox4x32_10([(n >> 2) & M, (n >> 34) & M, 1 - d, 0], key)[n & 3] != word
+        if n >> 34:
+            assert ref.philox4x32_10([(n >> 2) & M, (n >> 32) & M, d, 0], key)[n & 3] != word
 
 
 E = oracle.e4m3_table()
@@ -89,11 +122,18 @@ def test_sr_is_unbiased():
         assert abs(vals.mean() - y) <= 5 * se + 1e-12
 
 
-def test_rht_signs():
-    d0, d1 = oracle.rht_signs(0), oracle.rht_signs(1)
-    assert set(np.unique(d0)) <= {-1, 1} and d0.size == 32
-    assert not np.array_equal(d0, d1)
-    assert np.array_equal(d0, oracle.rht_signs(0))
+@pytest.mark.parametrize("seed,signs", list(stability_rows("sign")))
+def test_rht_signs_golden(seed, signs):
+    """oracle_rht_signs against signs written by an independent Philox: sign i is -1 iff bit i of
+    word 0 of counter (0, 0, 2, 0) is set.  The stored strings are not palindromes, so a reversed
+    bit order fails, and they differ from the bits of words 1-3."""
+    from tests.golden import make_stability_words as ref
+    d = oracle.rht_signs(int(seed, 16))
+    assert "".join("-" if v < 0 else "+" for v in d) == signs
+    assert signs != signs[::-1]
+    out = ref.philox4x32_10([0, 0, 2, 0], [int(seed, 16) & 0xFFFFFFFF, int(seed, 16) >> 32])
+    for w in out[1:]:
+        assert "".join("-" if (w >> i) & 1 else "+" for i in range(32)) != signs
 
 
 def test_rht_matches_hadamard_matrix_exactly_on_integers():
