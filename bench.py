@@ -342,6 +342,13 @@ class StepGroup:
             st.check_status()
 
 
+def swiglu_backward_bf16(dh: torch.Tensor, h1: torch.Tensor, h3: torch.Tensor):
+    """(dh1, dh3) of h = silu(h1) * h3 with torch's bf16 autograd ops (the unfused comparison route)."""
+    dh3 = dh * torch.nn.functional.silu(h1)
+    dh1 = torch.ops.aten.silu_backward(dh * h3, h1)
+    return dh1, dh3
+
+
 class SwiGLUStep:
     """One fwd+bwd of the SwiGLU routed expert y = (silu(x Wg^T) * (x Wu^T)) Wd^T through the C ABI.
 
@@ -356,7 +363,6 @@ class SwiGLUStep:
 
     def __init__(self, s: dict, device, fused: bool):
         import mxfp8_precision_moe_gb300 as mx
-        from mxfp8_precision_moe_gb300.swiglu import swiglu_backward_bf16
 
         L = mx.load()
         self.mx, self.L = mx, L

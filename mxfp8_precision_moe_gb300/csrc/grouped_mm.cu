@@ -15,7 +15,10 @@
 //   ROWGROUPED (fwd, dgrad): the token operand's rows are split by group; each
 //     group's rows are tiled by 128 and contracted with that expert's matrix.
 //   KGROUPED (wgrad): every group owns a full output matrix; its contraction
-//     runs over the group's own tokens only (empty group -> zeros).
+//     runs over the group's own tokens only (empty group -> zeros).  A group's
+//     last 128-token box may reach into the next group; only the 32-token
+//     blocks inside the group are multiplied, so another group's values
+//     (NaN included) never enter its sum.
 //
 // Kernel structure (one CTA per SM, persistent over a static tile order):
 //   warp 0      TMA producer: 128B-swizzled A/B tiles (128 x 128 B and BN x 128 B)
@@ -104,6 +107,8 @@ struct TileInfo {
     int64_t a_row, b_row;     // TMA row coordinates
     int64_t a_x0;             // TMA contraction coordinate of k-tile 0
     int k_tiles;
+    int kb_last;              // 32-wide K blocks of the last k-tile that belong to the tile (KGROUPED: the
+                              // group's own tokens; the rest of that TMA box is the next group's)
     int64_t sfa_base;         // byte offset of k-tile 0's A scale tile
     int64_t sfb_base[2];      // byte offsets of k-tile 0's B scale tiles
     int64_t sf_kstep;         // bytes between consecutive k-tiles' scale tiles (always 512)
@@ -151,6 +156,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, co
         ti.b_row = (int64_t)g * p.nb + n * TN;
         ti.a_x0 = 0;
         ti.k_tiles = (int)((p.kc + BK - 1) / BK) * (kDualK ? 2 : 1);
+        ti.kb_last = BK / 32;  // a K tail past the contraction reads TMA's zero fill
         ti.sfa_base = ((int64_t)(pstart_s[g] / BM + m) * p.sfa_ct) * 512;
         const int64_t last_chunk = (p.nb + 127) / 128 - 1;
 #pragma unroll
@@ -178,6 +184,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, co
         ti.b_row = n * BN;
         ti.a_x0 = start;
         ti.k_tiles = (int)((size + BK - 1) / BK);
+        ti.kb_last = (int)(((size - 1) & (BK - 1)) / 32) + 1;  // size % 32 == 0 (checked)
         ti.sfa_base = (m * ct + kt0) * 512;
         const int64_t last_chunk = (p.nb + 127) / 128 - 1;
 #pragma unroll
@@ -395,11 +402,22 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                     const uint32_t sfb_t = sfa_t + 4;
                     const uint32_t a_s = smem_u32(smem + cur * C::kABytes);
                     const uint32_t b_s = smem_u32(smem + C::kOffB + cur * C::kBBytes);
+                    if (kt + 1 < ti.k_tiles || ti.kb_last == BK / 32) {
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k) {
-                        const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
-                        const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
-                        tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, k, k), sfa_t, sfb_t, (kt | k) != 0);
+                        for (int k = 0; k < BK / 32; ++k) {
+                            const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
+                            const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
+                            tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, k, k), sfa_t, sfb_t, (kt | k) != 0);
+                        }
+                    } else {
+                        // K-grouped last k-tile: only the group's own 32-token blocks (the box's other
+                        // columns hold the next group's tokens, whose codes may be NaN)
+#pragma unroll 1
+                        for (int k = 0; k < ti.kb_last; ++k) {
+                            const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
+                            const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
+                            tc_mma_mxf8(d_tmem, ad, bd, idesc_mxf8(BM, BN, k, k), sfa_t, sfb_t, (kt | k) != 0);
+                        }
                     }
                     tc_commit(&empty[cur]);
                 }
@@ -655,6 +673,7 @@ struct PairTile {
     int g;
     int64_t a_row, b_row, a_x0;
     int k_tiles;
+    int kb_last;                      // 32-wide K blocks of the last k-tile inside the tile's contraction
     int64_t sfa_chunk, sfb_chunk[2];  // 512-byte scale tiles of k-tile 0 (index = byte offset / 512)
     __nv_bfloat16* out;               // first element of this CTA's 128 rows
     int64_t ldo;
@@ -687,6 +706,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
         ti.b_row = (int64_t)g * p.nb + n * BN + half * 128;
         ti.a_x0 = 0;
         ti.k_tiles = (int)((p.kc + BK - 1) / BK);
+        ti.kb_last = BK / 32;
         const int64_t cA = min64(2 * m2 + half, (size + 127) / 128 - 1);  // clamp: rows past the group are masked
         ti.sfa_chunk = (pstart_s[g] / 128 + cA) * p.sfa_ct;
 #pragma unroll
@@ -713,6 +733,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
         ti.b_row = n * BN + half * 128;
         ti.a_x0 = start;
         ti.k_tiles = (int)((size + BK - 1) / BK);
+        ti.kb_last = (int)(((size - 1) & (BK - 1)) / 32) + 1;  // size % 32 == 0 (checked)
         const int64_t cA = min64(2 * m2 + half, (p.na + 127) / 128 - 1);
         ti.sfa_chunk = cA * ct + kt0;
 #pragma unroll
@@ -919,12 +940,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sfb_t + 4 * j, smem_desc(smem_u32(smem + C::kOffSfb + cur * C::kSfbBytes + 512 * j), 0, 128, 0));
                     const uint32_t a_s = smem_u32(smem + cur * C::kABytes);
                     const uint32_t b_s = smem_u32(smem + C::kOffB + cur * C::kBBytes);
+                    if (kt + 1 < ti.k_tiles || ti.kb_last == BK / 32) {
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k) {
-                        const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
-                        const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
-                        tc_mma_pair_mxf8(tmem, ad, bd, idesc0 | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa_t, sfb_t,
-                                         (kt | k) != 0);
+                        for (int k = 0; k < BK / 32; ++k) {
+                            const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
+                            const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
+                            tc_mma_pair_mxf8(tmem, ad, bd, idesc0 | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa_t,
+                                             sfb_t, (kt | k) != 0);
+                        }
+                    } else {
+                        // K-grouped last k-tile: only the group's own 32-token blocks (the box's other
+                        // columns hold the next group's tokens, whose codes may be NaN)
+#pragma unroll 1
+                        for (int k = 0; k < ti.kb_last; ++k) {
+                            const uint64_t ad = smem_desc(a_s + 32 * k, 16, 1024, 2);
+                            const uint64_t bd = smem_desc(b_s + 32 * k, 16, 1024, 2);
+                            tc_mma_pair_mxf8(tmem, ad, bd, idesc0 | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa_t,
+                                             sfb_t, (kt | k) != 0);
+                        }
                     }
                     tc_commit_pair(&empty[cur], 0x3);
                 }

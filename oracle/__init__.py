@@ -263,6 +263,50 @@ def grouped_mm_wgrad(dq, ds, aq, as_, ends) -> np.ndarray:
     return out
 
 
+def _deq_rows(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Dequantized fp64 values of codes q[..., C] with compact scales s[..., C/32] (one per 32)."""
+    return dequant(np.ascontiguousarray(q, np.uint8), np.repeat(np.ascontiguousarray(s, np.uint8), 32, axis=-1))
+
+
+def grouped_mm_rows_blas(aq, as_, bq, bs, ends) -> np.ndarray:
+    """grouped_mm_rows with each group's contraction done by numpy's fp64 matmul (a library GEMM)
+    on the operands dequantized by the format definitions above: the same sum, another order, for
+    sizes where the scalar loops take minutes.  Pinned to grouped_mm_rows by the tests."""
+    aq = np.ascontiguousarray(aq, np.uint8)
+    M, K = aq.shape
+    G, Nb, K2 = bq.shape
+    assert K == K2
+    e = _ends(ends)
+    assert e.size == G and e[-1] == M
+    out = np.zeros((M, Nb), np.float64)
+    lo = 0
+    for g in range(G):
+        hi = int(e[g])
+        if hi > lo:
+            out[lo:hi] = _deq_rows(aq[lo:hi], as_[lo:hi]) @ _deq_rows(bq[g], bs[g]).T
+        lo = hi
+    return out
+
+
+def grouped_mm_wgrad_blas(dq, ds, aq, as_, ends) -> np.ndarray:
+    """grouped_mm_wgrad with numpy's fp64 matmul per group over the dequantized token-wise operands
+    (dOut^T codes dq[N, M], A^T codes aq[K, M], compact scales along M).  Pinned to grouped_mm_wgrad."""
+    N, M = dq.shape
+    K, M2 = aq.shape
+    assert M == M2
+    e = _ends(ends)
+    dd = _deq_rows(dq, ds)
+    ad = _deq_rows(aq, as_)
+    out = np.zeros((e.size, N, K), np.float64)
+    lo = 0
+    for g in range(e.size):
+        hi = int(e[g])
+        if hi > lo:
+            out[g] = dd[:, lo:hi] @ ad[:, lo:hi].T
+        lo = hi
+    return out
+
+
 # ---------------------------------------------------------------- SwiGLU stage of a routed expert
 def bf16_from_f64(x) -> np.ndarray:
     """fp64 values -> bf16 bit patterns (uint16), round to nearest even, one rounding."""
@@ -304,18 +348,20 @@ def swiglu_bwd_quantized(dh, h1, h3) -> dict:
     return out
 
 
-def swiglu_gate_up(x_u16, wg_u16, wu_u16, ends) -> dict:
+def swiglu_gate_up(x_u16, wg_u16, wu_u16, ends, blas: bool = False) -> dict:
     """The gate/up half of a SwiGLU routed expert, from bf16 inputs: x [M, D], Wg and Wu
     [G, H, D].  x and the weights are quantized along D, both GEMMs run in fp64, and
     h1, h3, h follow the bf16 rounding points of oracle_swiglu_bf16.  Returns the fp64
     GEMM results (h1_f64, h3_f64), the bf16 patterns (h1, h3, h), and h quantized along
-    H (h_q, h_s compact [M, H/32]) and along the tokens (hT_q [H, M], hT_s compact)."""
+    H (h_q, h_s compact [M, H/32]) and along the tokens (hT_q [H, M], hT_s compact).  blas: the
+    GEMMs by grouped_mm_rows_blas (large shapes)."""
     xq, xs = quantize_rows(x_u16)
     G = wg_u16.shape[0]
     wg = [quantize_rows(wg_u16[g]) for g in range(G)]
     wu = [quantize_rows(wu_u16[g]) for g in range(G)]
-    h1f = grouped_mm_rows(xq, xs, np.stack([q for q, _ in wg]), np.stack([s_ for _, s_ in wg]), ends)
-    h3f = grouped_mm_rows(xq, xs, np.stack([q for q, _ in wu]), np.stack([s_ for _, s_ in wu]), ends)
+    mm = grouped_mm_rows_blas if blas else grouped_mm_rows
+    h1f = mm(xq, xs, np.stack([q for q, _ in wg]), np.stack([s_ for _, s_ in wg]), ends)
+    h3f = mm(xq, xs, np.stack([q for q, _ in wu]), np.stack([s_ for _, s_ in wu]), ends)
     h1, h3 = bf16_from_f64(h1f), bf16_from_f64(h3f)
     h = swiglu_bf16(h1, h3)
     out = dict(h1_f64=h1f, h3_f64=h3f, h1=h1, h3=h3, h=h)

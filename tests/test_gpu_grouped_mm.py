@@ -398,3 +398,50 @@ def test_dgrad2_equals_the_sum_of_two_dgrads(mx):
     assert_gemm_close(f64(dA), ref, what="dgrad2")
     with pytest.raises(ValueError):
         mx.mxfp8_grouped_mm_dgrad2(*q[0], *wt[0], q[1][0][:, :128].contiguous(), q[1][1], *wt[1], offs)
+
+
+@pytest.mark.parametrize("N,K", [(256, 256), (160, 128)])
+def test_wgrad_next_group_nonfinite_does_not_leak(mx, N, K):
+    """A group whose size is a multiple of 32 but not of 128 ends inside a 128-token copy box; the
+    box's remaining columns hold the next group's tokens.  With Inf/NaN in the next group's first
+    tokens (their column blocks quantize to NaN codes), the group's own dW must stay finite and
+    equal the oracle's, which sums over the group's tokens only ("grouped result equals per-group
+    dense GEMMs").  K = 256: the CTA-pair kernel; K = 128: the single-CTA kernel."""
+    sizes = [96, 64, 160]
+    M = sum(sizes)
+    D = synth.randn_bf16((M, N), 1e-3, seed=401).float()
+    A = synth.randn_bf16((M, K), 1.0, seed=402).float()
+    D[96, 5], D[97, :] = float("nan"), float("inf")   # first tokens of group 1
+    A[96, 7], A[100, 3] = -float("inf"), float("nan")
+    D, A = D.to(torch.bfloat16), A.to(torch.bfloat16)
+    got = gpu_wgrad(mx, D, A, sizes)
+    ref = oracle_wgrad(D, A, sizes)
+    for g in (0, 2):
+        assert np.all(np.isfinite(got[g])), f"group {g}: non-finite values leaked from the next group"
+        assert_gemm_close(got[g], ref[g], what=f"wgrad group {g} beside a non-finite group")
+    assert not np.all(np.isfinite(got[1]))  # the group that holds them does see them
+
+
+def test_composite_op_rejects_bad_offsets(mx):
+    """Group sizes that are not multiples of 32 cannot be quantized along the tokens for the wgrad:
+    with W requiring a gradient the composite op raises instead of returning the outputs the
+    kernels skipped; with only A requiring one, the same offsets run (fwd and dgrad take any
+    size).  Offsets that do not end at M raise too."""
+    sizes = [48, 80]
+    M, N, K = sum(sizes), 128, 128
+    A = synth.randn_bf16((M, K), 1.0, seed=411)
+    W = synth.randn_bf16((2, N, K), 0.02, seed=412)
+    offs = offs_dev(sizes)
+    with pytest.raises(mx.Mxfp8Error, match="OFFSETS"):
+        mx.to_mxfp8_then_scaled_grouped_mm(A.cuda().requires_grad_(True), W.cuda().requires_grad_(True), offs)
+    a = A.cuda().requires_grad_(True)
+    out = mx.to_mxfp8_then_scaled_grouped_mm(a, W.cuda(), offs)
+    out.backward(synth.randn_bf16((M, N), 1e-3, seed=413).cuda())
+    torch.cuda.synchronize()
+    assert_gemm_close(f64(out), oracle_fwd(A, W, sizes), what="fwd with 48/80-token groups")
+    short = torch.tensor([48, 100], dtype=torch.int32, device="cuda")
+    with pytest.raises(mx.Mxfp8Error, match="OFFSETS"):
+        mx.to_mxfp8_then_scaled_grouped_mm(A.cuda(), W.cuda(), short)
+    # the context stays usable
+    x = torch.ones((32, 32), dtype=torch.bfloat16, device="cuda")
+    assert int(mx.mxfp8_quantize_2d(x, mx.ROW, mx.SCALES_COMPACT)[0][0, 0].item()) == 0x78

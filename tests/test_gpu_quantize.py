@@ -73,7 +73,7 @@ def test_hand_worked_blocks_on_gpu(mx):
 
 
 def test_nonfinite_block_reading_on_gpu(mx):
-    # parity unpinned: the NaN/Inf reading on one hand-made block, GPU == oracle
+    # the NaN/Inf reading (pinned in test_oracle_quantize.py) on hand-made blocks, GPU == oracle
     v = np.zeros((1, 64), dtype=np.float32)
     v[0, 0], v[0, 1], v[0, 2] = np.inf, -1.0, 2.0
     v[0, 32:] = np.linspace(-3, 3, 32)

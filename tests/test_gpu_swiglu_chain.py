@@ -37,6 +37,11 @@ def bf16_round(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
 
 
+def as_bf16(b: np.ndarray) -> torch.Tensor:
+    """bf16 bit patterns (uint16) as a bf16 tensor."""
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+
+
 def o_fwd(A, W, sizes):
     aq, as_ = oracle.quantize_rows(u16(A))
     wq, ws = zip(*[oracle.quantize_rows(u16(W[g])) for g in range(W.shape[0])])
@@ -79,23 +84,17 @@ def inputs():
 
 
 def oracle_chain(x, Wg, Wu, Wd, dY, sizes):
-    """The expert on the oracle: fp64 GEMMs of oracle-quantized operands, the SwiGLU glue in
-    fp64 with a bf16 rounding after each elementwise op (silu(h1), the product; in the
-    backward dh*silu(h1), dh*h3 and the silu-derivative product)."""
+    """The expert on the oracle: fp64 GEMMs of oracle-quantized operands, each rounded once to
+    bf16, and the oracle's SwiGLU stages (swiglu_bf16 and swiglu_bwd_bf16: fp64 with a bf16
+    rounding after each elementwise op, pinned in test_oracle_swiglu.py)."""
     o_h1 = bf16_round(o_fwd(x, Wg, sizes))
     o_h3 = bf16_round(o_fwd(x, Wu, sizes))
-    h1d, h3d = o_h1.double().numpy(), o_h3.double().numpy()
-    sig = 1.0 / (1.0 + np.exp(-h1d))
-    silu = bf16_round(h1d * sig).double().numpy()
-    o_h = bf16_round(silu * h3d)
+    o_h = as_bf16(oracle.swiglu_bf16(u16(o_h1), u16(o_h3)))               # the oracle's pinned SwiGLU stage
     o = dict(y=o_fwd(o_h, Wd, sizes))
-    # backward: dh = dY Wd (dgrad); dWd = dY^T h (wgrad); then the SwiGLU backward
+    # backward: dh = dY Wd (dgrad); dWd = dY^T h (wgrad); then the oracle's SwiGLU backward stage
     o_dh = bf16_round(o_dgrad(dY, Wd, sizes))
     o["dWd"] = o_wgrad(dY, o_h, sizes)
-    dhd = o_dh.double().numpy()
-    d_h3 = bf16_round(dhd * silu)                                          # d/dh3 of silu(h1) * h3
-    d_silu = bf16_round(dhd * h3d).double().numpy()
-    d_h1 = bf16_round(d_silu * sig * (1.0 + h1d * (1.0 - sig)))            # silu derivative
+    d_h1, d_h3 = (as_bf16(t) for t in oracle.swiglu_bwd_bf16(u16(o_dh), u16(o_h1), u16(o_h3)))
     o["dx"] = o_dgrad(d_h1, Wg, sizes) + o_dgrad(d_h3, Wu, sizes)
     o["dWg"] = o_wgrad(d_h1, x, sizes)
     o["dWu"] = o_wgrad(d_h3, x, sizes)
