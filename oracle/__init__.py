@@ -68,6 +68,7 @@ def lib():
         L.oracle_grouped_mm_rows.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P]
         L.oracle_grouped_mm_wgrad.argtypes = [P, P, P, P, P, I64, I64, I64, I64, P]
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         L.oracle_bf16_from_f64.argtypes = [ctypes.c_double]
         L.oracle_bf16_from_f64.restype = ctypes.c_uint16
         L.oracle_bf16_from_f64_array.argtypes = [P, I64, P]
@@ -102,6 +103,11 @@ def _u16(x) -> np.ndarray:
 
 def num_threads() -> int:
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's OpenMP GEMM loops (1 = single-threaded)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- scalars

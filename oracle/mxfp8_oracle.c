@@ -541,3 +541,14 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Thread count of the OpenMP loops above (the per-group GEMMs); no effect without OpenMP.  Lets
+ * a caller time the same oracle single-threaded and over all host cores. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}
