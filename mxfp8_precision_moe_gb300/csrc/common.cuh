@@ -265,6 +265,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Relaxed arrives, for handing a tensor-memory accumulator back to the MMA warp.  The epilogue's
+// reads of it are complete (tcgen05.wait::ld blocks until they are) and tcgen05.fence::before_thread_sync
+// orders them before the arrive; nothing in generic memory is handed over.  A release arrive would
+// also wait until every earlier global store of the thread is performed -- the previous tile's
+// output, tens of KB in flight -- and so hold the tensor pipe idle for thousands of cycles per tile.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // 2D TMA load into this CTA's shared memory, completing on an mbarrier of either CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
                                                  uint32_t cluster_bar) {

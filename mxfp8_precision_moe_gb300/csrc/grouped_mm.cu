@@ -119,12 +119,14 @@ struct TileInfo {
     int64_t col0;             // first output column
 };
 
-__device__ __forceinline__ int band_split(int64_t l, int64_t mt, int64_t nt, int64_t& m, int64_t& n) {
-    const int64_t band = l / (kBand * nt);
-    const int64_t bm = min64(kBand, mt - band * kBand);
-    const int64_t idx = l - band * kBand * nt;
+// Tile l of an mt x nt grid walked in bands of `bandw` m-tiles, each band n-tile by n-tile.
+__device__ __forceinline__ int band_split(int64_t l, int64_t mt, int64_t nt, int64_t& m, int64_t& n,
+                                          int64_t bandw = kBand) {
+    const int64_t band = l / (bandw * nt);
+    const int64_t bm = min64(bandw, mt - band * bandw);
+    const int64_t idx = l - band * bandw * nt;
     n = idx / bm;
-    m = band * kBand + (idx - n * bm);
+    m = band * bandw + (idx - n * bm);
     return 0;
 }
 
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[0]);
+                if (lane == 0) mbar_arrive_relaxed(&tempty[0]);
                 acc_phase ^= 1u;
 
                 const int vcols = ti.valid_cols;
@@ -596,7 +598,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (lane == 0) mbar_arrive_relaxed(&tempty[acc]);
                 // Coalesced stores: per 64-column chunk, each lane parks its row's eight 16-byte pieces in
                 // the warp's 32 x 128 B staging buffer (piece j of row r at slot j ^ (r & 7): no bank
                 // conflicts), then every store instruction writes 4 full 128-byte row segments.
@@ -646,6 +648,14 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
 // ============================================================================================
 constexpr int kPairStages = 5;
 constexpr int kSortGroups = 128;  // K-grouped schedules rank at most this many groups (O(G^2) per CTA)
+// Epilogue warps of the pair kernel: two per tensor-memory lane quarter, each draining one 128-column
+// half of the accumulator, so the single accumulator is handed back to the MMA warp in half the time
+// (a K-grouped tile of a small group contracts over few k-tiles, and the drain is per tile).
+constexpr int kPairEpiWarps = 8;
+constexpr int kThreadsPair = 64 + 32 * kPairEpiWarps;
+// K-grouped pair tiles run in bands of 8 row-tiles: the 76 tiles of a wave then share about
+// 8 A and 10 B operand slabs instead of 16 and 5 (a long group's slabs do not fit in L2 together).
+constexpr int kBandPairK = 8;
 
 struct CfgPair {
     static constexpr int BN = 256;
@@ -663,7 +673,7 @@ struct CfgPair {
     static constexpr int kOffSfa = kOffB + kStages * kBBytes;
     static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
     static constexpr int kOffStage = kOffSfb + kStages * kSfbBytes;
-    static constexpr int kStageBytes = 4 * 32 * 128;
+    static constexpr int kStageBytes = kPairEpiWarps * 32 * 128;
     static constexpr int kOffBar = kOffStage + kStageBytes;
     static constexpr int kBarBytes = (2 * kStages + 2 + 1) * 8 + 16;
     static constexpr int kSmem = kOffBar + kBarBytes + 1024;
@@ -724,7 +734,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
         const int gp = (int)(t / per_g);
         const int g = sorted ? gorder_s[gp] : gp;
         int64_t m2, n;
-        band_split(t - gp * per_g, nta2, ntb, m2, n);
+        band_split(t - gp * per_g, nta2, ntb, m2, n, kBandPairK);
         const int64_t start = g ? ends_s[g - 1] : 0, size = ends_s[g] - start;
         const int64_t ct = ptotal / 128, kt0 = pstart_s[g] / 128;
         const int64_t rows0 = m2 * 256 + half * 128;
@@ -746,7 +756,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
     return ti;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsPair, 1)
     grouped_mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                            const GemmParams p) {
@@ -833,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(&empty[s], 1);
             }
             mbar_init(tfull, 1);
-            mbar_init(tempty, 8);  // 4 epilogue warps in each CTA of the pair
+            mbar_init(tempty, 2 * kPairEpiWarps);  // every epilogue warp of both CTAs of the pair
             mbar_init(drain, 1);
             fence_barrier_init();
         }
@@ -970,7 +980,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
         } else if (warp >= 2) {
             // ------------------------------------------------ epilogue (both CTAs: own 128 rows)
+            // Warp w drains lane quarter w % 4 (the quarter its tensor-memory access is bound to) and
+            // column half (w - 2) / 4 of the accumulator.
+            constexpr int kHalfCols = BN / 2;
             const int quarter = warp & 3;
+            const int c_base = ((warp - 2) >> 2) * kHalfCols;
             uint8_t* stg = smem + C::kOffStage + (warp - 2) * (32 * 128);
             const uint32_t tempty_leader = cluster_addr(tempty, 0);
             uint32_t acc_phase = 0;
@@ -978,22 +992,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t t = tile_at(j);
                 if (t >= ntiles) continue;
                 const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
-                __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo;
+                __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo + c_base;
                 const int vrows = ti.valid_rows - quarter * 32;
+                const int vcols = ti.valid_cols - c_base;  // columns of this warp's half inside the output
                 if (ti.k_tiles == 0) {
                     for (int rl = 0; rl < 32; ++rl)
                         if (rl < vrows)
-                            for (int c = lane * 8; c < ti.valid_cols; c += 256)
+                            for (int c = lane * 8; c < kHalfCols && c < vcols; c += 256)
                                 *reinterpret_cast<uint4*>(wout + (int64_t)rl * ti.ldo + c) = make_uint4(0, 0, 0, 0);
                     continue;
                 }
                 if (!mbar_wait_bounded(tfull, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
                 acc_phase ^= 1u;
                 tc_fence_after();
-                uint32_t packed[BN / 2];
-                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+                uint32_t packed[kHalfCols / 2];
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + c_base;
 #pragma unroll
-                for (int c = 0; c < BN; c += 64) {
+                for (int c = 0; c < kHalfCols; c += 64) {
                     uint32_t v0[32], v1[32];
                     tmem_ld_32x32b_x32(taddr + c, v0);
                     tmem_ld_32x32b_x32(taddr + c + 32, v1);
@@ -1006,10 +1021,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(tempty_leader);
+                if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
 #pragma unroll
-                for (int ch = 0; ch < BN / 64; ++ch) {
-                    if (ch * 64 >= ti.valid_cols) break;
+                for (int ch = 0; ch < kHalfCols / 64; ++ch) {
+                    if (ch * 64 >= vcols) break;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) * 16),
@@ -1020,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 8; ++i) {
                         const int rl = (lane >> 3) + 4 * i, piece = lane & 7;
                         const uint4 val = ld_shared_v4(stg + rl * 128 + ((piece ^ (rl & 7)) * 16));
-                        if (rl < vrows && ch * 64 + piece * 8 < ti.valid_cols)
+                        if (rl < vrows && ch * 64 + piece * 8 < vcols)
                             *reinterpret_cast<uint4*>(wout + (int64_t)rl * ti.ldo + ch * 64 + piece * 8) = val;
                     }
                     __syncwarp();
@@ -1127,7 +1142,7 @@ static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols,
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreadsPair);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
     cfg.attrs = attr;
