@@ -60,9 +60,10 @@ struct QParams {
     uint8_t* s_col2;
 };
 
-// Kernel modes: plain MX quantization; the stability variants (fp32 values, Hadamard transform,
-// stochastic rounding); the fused SwiGLU backward (three inputs dh, h1, h3; two quantized outputs).
-enum QuantMode : int { kModePlain = 0, kModeExt = 1, kModeSwiBwd = 2 };
+// Kernel modes: plain MX quantization; the Hadamard variants (fp32 values, optionally with
+// stochastic rounding); the fused SwiGLU backward (three inputs dh, h1, h3; two quantized outputs);
+// stochastic rounding alone (the plain kernel's bf16 data path with stochastic codes).
+enum QuantMode : int { kModePlain = 0, kModeExt = 1, kModeSwiBwd = 2, kModeSR = 3 };
 
 // Warp 0 builds, for G groups over R rows, the clamped monotone end rows and
 // the padded start rows P[g] = sum_{h<g} ceil(size_h/128)*128 (also the scale
@@ -135,32 +136,84 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
-// The random words of the 4 elements n0..n0+3 (n0 % 4 == 0; element index r * C + c of the input)
-// for copy `dir` (0 row-wise, 1 column-wise): counter (n0 / 4, n0 / 2^34, dir, 0), key = seed.
-__device__ __forceinline__ uint4 sr_words4(uint64_t n0, uint32_t dir, uint64_t seed) {
-    return philox4x32_10(make_uint4((uint32_t)(n0 >> 2), (uint32_t)(n0 >> 34), dir, 0u), (uint32_t)seed,
-                         (uint32_t)(seed >> 32));
+// The random bytes of one 2 x 8 block: rows 2 rp, 2 rp + 1 and columns 8 cb .. 8 cb + 7 of an input
+// with C columns.  Counter (b mod 2^32, b / 2^32, 0, 0), b = rp * (C / 8) + cb, key = seed; byte
+// 8 (r mod 2) + (c mod 8) of the output (word k = bytes 4k .. 4k+3, least significant first) belongs
+// to element (r, c).  The row-wise and the column-wise copy of an element use the same byte.
+// Out of line: one copy of the ten unrolled rounds serves every call site (the kernel body stays small
+// enough for the instruction caches).
+__device__ __noinline__ uint4 sr_draw(uint64_t rp, uint64_t cb, uint64_t C, uint64_t seed) {
+    const uint64_t b = rp * (C >> 3) + cb;
+    return philox4x32_10(make_uint4((uint32_t)b, (uint32_t)(b >> 32), 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
-// E4M3 code of z rounded stochastically with the random word r.  Between consecutive finite
-// magnitudes lo <= |z| < hi the magnitude rounds up iff F + (r >> 12) >= 2^20, with F the part
-// of |z| above lo in units of 2^-20 of the step (truncated); |z| >= 448 gives 448.  On the normal
-// E4M3 range that is an integer add into the 20 fp32 mantissa bits E4M3 drops; below 2^-6 the step
-// is 2^-9.  The sign is applied last.
-__device__ __forceinline__ uint32_t e4m3_sr(float z, uint32_t r) {
-    const uint32_t bits = __float_as_uint(z), a = bits & 0x7FFFFFFFu;
-    float m;
-    if (a >= 0x43E00000u) {                 // 448 and beyond
-        m = 448.0f;
-    } else if (a >= 0x3C800000u) {          // 2^-6 <= |z| < 448
-        m = __uint_as_float((a + (r >> 12)) & ~0xFFFFFu);
+// E4M3 code of y rounded stochastically with the random byte u (0..255).  Between consecutive finite
+// magnitudes lo <= |y| < hi the magnitude rounds up iff F + u >= 256, with F the part of |y| above lo
+// in units of 1/256 of the step (truncated); |y| >= 448 gives 448; the sign is y's.
+//   |y| >= 2^-6: the step is the unit of fp32 mantissa bit 20, so F is the top 8 of the 20 bits E4M3
+//     drops: adding u at bit 12 carries into bit 20 exactly when F + u >= 256, and the E4M3 code is
+//     then the fp32 pattern's bits 20.. less 120 << 3 (the exponent bias difference), capped at 0x7E.
+//   |y| <  2^-6: the step is 2^-9; F_total = floor(|y| 2^17) holds the code below |y| in its bits
+//     8.. and F in its bits 0-7, computed from the fp32 mantissa M and exponent E as M >> (133 - E).
+__device__ __forceinline__ uint32_t sr_code_f32(float y, uint32_t u) {
+    const uint32_t bits = __float_as_uint(y), a = bits & 0x7FFFFFFFu;
+    uint32_t code;
+    if (a >= 0x3C800000u) {
+        code = min(((a + (u << 12)) >> 20) - 960u, 0x7Eu);
     } else {
-        const float n = __uint_as_float(a) * 512.0f;  // units of the subnormal step 2^-9 (exact)
-        const float lo = floorf(n);
-        const uint32_t F = (uint32_t)((n - lo) * 1048576.0f);
-        m = (lo + ((F + (r >> 12)) >= 0x100000u ? 1.0f : 0.0f)) * 0.001953125f;
+        const uint32_t E = a >> 23;
+        const uint32_t M = (a & 0x7FFFFFu) | (E ? 0x800000u : 0u);
+        const uint32_t sh = 133u - (E ? E : 1u);  // >= 13
+        const uint32_t F = sh >= 32u ? 0u : (M >> sh);
+        code = (F >> 8) + (((F & 0xFFu) + u) >> 8);
     }
-    return (cvt_e4m3x2(m, 0.0f) & 0xFFu) | ((bits >> 24) & 0x80u);  // m lies on the E4M3 grid: exact
+    return code | ((bits >> 24) & 0x80u);
+}
+
+// Exact stochastic codes (bytes 0 and 2, with signs) of the halves of a scaled bf16 pair yy that win
+// marks (bits 15 / 31), the others left as in c; ub holds the two random bytes in bits 0-7, 16-23.
+__device__ __noinline__ uint32_t sr_fix_pair(uint32_t yy, uint32_t ub, uint32_t c, uint32_t win) {
+    if (win & 0x8000u) c = (c & 0xFFFF0000u) | sr_code_f32(__uint_as_float(yy << 16), ub & 0xFFu);
+    if (win & 0x80000000u) c = (c & 0xFFFFu) | (sr_code_f32(__uint_as_float(yy & 0xFFFF0000u), (ub >> 16) & 0xFFu) << 16);
+    return c;
+}
+
+// Two E4M3 codes (bytes 0 and 2) of a scaled bf16 pair yy (exact: x times a power of two) rounded
+// stochastically; ub holds each element's random byte in bits 0-7 and 16-23.  A bf16 y has 8
+// significant bits, so on the normal E4M3 range its 4 mantissa bits below the E4M3 step are F / 16,
+// and F + u >= 256 is (those 4 bits) + (u >> 4) >= 16: one packed add carries into the E4M3 mantissa
+// (the sign bit is left alone), the code is the pattern's bits 4-14 less 120 << 3, clamped to 0 .. 0x7E
+// per half, and bit 15 moves to bit 7.  Below 2^-17 that also holds (F = 0: code 0 with the sign).
+// Magnitudes in [2^-17, 2^-6) (bf16 0x3700 .. 0x3C7F: E4M3 subnormals with F > 0) take the fp32 rule
+// out of line.  (A NaN half can carry into the other half; both then belong to a non-finite block,
+// whose codes are replaced.)
+__device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t sr_pair_bf16x2(uint32_t yy, uint32_t ub) {
+    const uint32_t t = yy + ((ub >> 4) & 0x000F000Fu);
+    uint32_t c = vmin_u16x2(vmax_u16x2((t >> 4) & 0x07FF07FFu, 0x03C003C0u) - 0x03C003C0u, 0x007E007Eu);
+    c |= (t >> 8) & 0x00800080u;
+    const uint32_t mag = yy & 0x7FFF7FFFu;
+    const uint32_t win = ~(mag + 0x43804380u) & (mag + 0x49004900u) & 0x80008000u;  // 0x3700 <= half < 0x3C80
+    if (win) c = sr_fix_pair(yy, ub, c, win);
+    return c;
+}
+
+// Bytes b and b + 1 (b = 0 or 2) of a random word into bits 0-7 and 16-23.
+__device__ __forceinline__ uint32_t sr_pick2(uint32_t w, int b) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(w), "r"(b ? 0x4342u : 0x4140u));
+    return d;
+}
+
+// bf16 x bf16 -> bf16 for both halves (round to nearest even; exact for x times a power of two).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 // E8M0 scale byte from the magnitude bits of an fp32 amax (same rule as for bf16: max(E - 8, 0)).
@@ -395,7 +448,7 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
         if constexpr (!kSwiBwd) {
             if (!mbar_wait_bounded(&full[stage], phase, kQTimeoutNs, abort_flag, p.dev_status)) break;
             src = tiles + stage * kStageBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
-            if constexpr (kMode == kModePlain) {
+            if constexpr (kMode == kModePlain || kMode == kModeSR) {
 #pragma unroll
                 for (int rr = 0; rr < 8; ++rr) {
                     const uint4 u = *reinterpret_cast<const uint4*>(src + rr * 256);
@@ -490,9 +543,11 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
             const bool sr = p.opts & MXFP8_OPT_STOCHASTIC;
             const uint32_t dsign = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)p.seed,
                                                  (uint32_t)(p.seed >> 32)).x;
-            auto code2 = [&](float z0, float z1, uint32_t r0, uint32_t r1) -> uint32_t {
-                return sr ? e4m3_sr(z0, r0) | (e4m3_sr(z1, r1) << 8) : cvt_e4m3x2(z0, z1);
+            // two codes from two fp32 values and (stochastic rounding) their random bytes
+            auto code2 = [&](float z0, float z1, uint32_t u0, uint32_t u1) -> uint32_t {
+                return sr ? sr_code_f32(z0, u0) | (sr_code_f32(z1, u1) << 8) : cvt_e4m3x2(z0, z1);
             };
+            const uint64_t rp0 = (uint64_t)((row0 + 8 * li) >> 1), cb = (uint64_t)(c8 >> 3);  // this lane's draws
             if constexpr (kRow) {
                 uint32_t s8[8];
                 uint8_t* qb = p.q_row + b * R * C;
@@ -552,19 +607,24 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
                         s8[4 * hr + i] = e8m0_from_f32bits(m);
                     }
+                    // rows 4hr .. 4hr+3 of the patch: draws 2hr and 2hr + 1 (rows 2d: words x, y; rows 2d+1: z, w)
+                    uint4 dr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+                    if (sr) {
+                        dr[0] = sr_draw(rp0 + 2 * hr, cb, (uint64_t)C, p.seed);
+                        dr[1] = sr_draw(rp0 + 2 * hr + 1, cb, (uint64_t)C, p.seed);
+                    }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const uint32_t sc = s8[4 * hr + i];
                         const int64_t row = row0 + 8 * li + 4 * hr + i;
                         const float f = inv_scale_from_e8m0(sc);
-                        uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
-                        if (sr && row < R) {
-                            w0 = sr_words4((uint64_t)(row * C + c8), 0u, p.seed);
-                            w1 = sr_words4((uint64_t)(row * C + c8 + 4), 0u, p.seed);
-                        }
+                        const uint32_t wa = (i & 1) ? dr[i >> 1].z : dr[i >> 1].x;  // columns 0-3
+                        const uint32_t wb = (i & 1) ? dr[i >> 1].w : dr[i >> 1].y;  // columns 4-7
                         uint2 q;
-                        q.x = code2(y[i][0] * f, y[i][1] * f, w0.x, w0.y) | (code2(y[i][2] * f, y[i][3] * f, w0.z, w0.w) << 16);
-                        q.y = code2(y[i][4] * f, y[i][5] * f, w1.x, w1.y) | (code2(y[i][6] * f, y[i][7] * f, w1.z, w1.w) << 16);
+                        q.x = code2(y[i][0] * f, y[i][1] * f, wa & 0xFFu, (wa >> 8) & 0xFFu) |
+                              (code2(y[i][2] * f, y[i][3] * f, (wa >> 16) & 0xFFu, wa >> 24) << 16);
+                        q.y = code2(y[i][4] * f, y[i][5] * f, wb & 0xFFu, (wb >> 8) & 0xFFu) |
+                              (code2(y[i][6] * f, y[i][7] * f, (wb >> 16) & 0xFFu, wb >> 24) << 16);
                         if (sc == 0xFFu) {
                             uint32_t sg[2] = {0u, 0u};
 #pragma unroll
@@ -641,16 +701,18 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                     uint32_t qc[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
 #pragma unroll
                     for (int rr = 0; rr < 8; rr += 2) {
-                        const int64_t row = row0 + 8 * li + rr;
-                        uint4 wa = make_uint4(0, 0, 0, 0), wb = wa;
-                        if (sr && row < R) {
-                            wa = sr_words4((uint64_t)(row * C + c8 + 4 * hc), 1u, p.seed);
-                            wb = sr_words4((uint64_t)((row + 1) * C + c8 + 4 * hc), 1u, p.seed);
+                        // rows rr, rr + 1 of the patch: draw rr / 2, words hc (row rr) and 2 + hc (row rr + 1),
+                        // byte j for column 4hc + j
+                        uint32_t wa = 0, wb = 0;
+                        if (sr) {
+                            const uint4 r4 = sr_draw(rp0 + (rr >> 1), cb, (uint64_t)C, p.seed);
+                            wa = hc ? r4.y : r4.x;
+                            wb = hc ? r4.w : r4.z;
                         }
-                        const uint32_t ra[4] = {wa.x, wa.y, wa.z, wa.w}, rb[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            qc[j][rr >> 2] |= code2(y[rr][j] * f[j], y[rr + 1][j] * f[j], ra[j], rb[j]) << (8 * (rr & 3));
+                            qc[j][rr >> 2] |= code2(y[rr][j] * f[j], y[rr + 1][j] * f[j], (wa >> (8 * j)) & 0xFFu,
+                                                    (wb >> (8 * j)) & 0xFFu) << (8 * (rr & 3));
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -674,6 +736,12 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
             continue;
         }
 
+        // Stochastic rounding: the random bytes of this lane's 8 x 8 patch; draw d covers its rows 2d,
+        // 2d + 1 (words x, y: row 2d, columns 0-3 / 4-7; words z, w: row 2d + 1).  Drawn where they are
+        // used, so that no more than one copy's draws are live at a time.
+        auto draw = [&](int d) -> uint4 {
+            return sr_draw((uint64_t)((row0 + 8 * li) >> 1) + d, (uint64_t)(c8 >> 3), (uint64_t)C, p.seed);
+        };
         // the plain MX quantization of one 8 x 8 patch per lane (bf16 pairs v) into one output set
         auto quant_rowcol = [&](const uint32_t (&v)[8][4], uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                                 uint8_t* s_col) {
@@ -720,7 +788,24 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t f2 = inv_scale_pair_bf16(s2[k]);
-                    uint2 q[2] = {quant8_bf16<0>(v[2 * k], f2), quant8_bf16<1>(v[2 * k + 1], f2)};
+                    uint2 q[2];
+                    if constexpr (kMode == kModeSR) {
+                        // rows 2k (scale in the low half of f2) and 2k + 1 (high half): draw k
+                        const uint4 rk = draw(k);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t fs = h ? (f2 & 0xFFFF0000u) | (f2 >> 16) : (f2 & 0xFFFFu) | (f2 << 16);
+                            const uint32_t w0 = h ? rk.z : rk.x, w1 = h ? rk.w : rk.y;  // columns 0-3 / 4-7
+                            uint32_t c[4];
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                c[kk] = sr_pair_bf16x2(mul_bf16x2(v[2 * k + h][kk], fs), sr_pick2(kk < 2 ? w0 : w1, (kk & 1) * 2));
+                            q[h] = make_uint2(__byte_perm(c[0], c[1], 0x6420), __byte_perm(c[2], c[3], 0x6420));
+                        }
+                    } else {
+                        q[0] = quant8_bf16<0>(v[2 * k], f2);
+                        q[1] = quant8_bf16<1>(v[2 * k + 1], f2);
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int rr = 2 * k + h;
@@ -766,13 +851,37 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                 for (int k = 0; k < 4; ++k) nf |= s2c[k] + kNonfiniteAdd;
                 const bool any_nonfinite = __any_sync(0xffffffffu, (nf & kNonfiniteBits) != 0u);
                 uint8_t* qb = q_col + b * R * C;
+                uint4 rnd[4];         // stochastic rounding: every column pair needs all four draws
+                if constexpr (kMode == kModeSR) {
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) rnd[d] = draw(d);
+                }
                 // codes of column 2k + h: elements (rr, half h of word k) times half h of the scale pair
                 auto col_codes = [&](auto hc, int k, uint32_t f2) -> uint2 {
                     constexpr int h = decltype(hc)::value;
                     uint32_t w[4];
+                    if constexpr (kMode == kModeSR) {
+                        // column j = 2k + h; rows rr, rr + 1 share draw rr / 2 (words j / 4 and 2 + j / 4,
+                        // byte j % 4 of each)
+                        const uint32_t fs = h ? (f2 & 0xFFFF0000u) | (f2 >> 16) : (f2 & 0xFFFFu) | (f2 << 16);
+                        constexpr uint32_t kPickH = h ? 0x7632u : 0x5410u;  // half h of two words -> one pair
+                        const int j = 2 * k + h, wsel = j >> 2, b = j & 3;
+                        const uint32_t sel = (uint32_t)b | ((uint32_t)(4 + b) << 8);  // byte b of each word
 #pragma unroll
-                    for (int rr = 0; rr < 8; rr += 2)
-                        w[rr >> 1] = cvt_e4m3x2(scale_bf16<h, h>(v[rr][k], f2), scale_bf16<h, h>(v[rr + 1][k], f2));
+                        for (int rr = 0; rr < 8; rr += 2) {
+                            const uint4 r4 = rnd[rr >> 1];
+                            const uint32_t wa = wsel ? r4.y : r4.x, wb = wsel ? r4.w : r4.z;
+                            uint32_t ub, xx;
+                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(ub) : "r"(wa), "r"(wb), "r"(sel));
+                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(xx) : "r"(v[rr][k]), "r"(v[rr + 1][k]), "r"(kPickH));
+                            const uint32_t c = sr_pair_bf16x2(mul_bf16x2(xx, fs), ub & 0x00FF00FFu);
+                            w[rr >> 1] = (c & 0xFFu) | ((c >> 8) & 0xFF00u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int rr = 0; rr < 8; rr += 2)
+                            w[rr >> 1] = cvt_e4m3x2(scale_bf16<h, h>(v[rr][k], f2), scale_bf16<h, h>(v[rr + 1][k], f2));
+                    }
                     return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
                 };
                 if (cval) {
@@ -794,7 +903,7 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                                 q[h].x = 0x7F7F7F7Fu | sg[0] | (sg[1] << 16);
                                 q[h].y = 0x7F7F7F7Fu | sg[2] | (sg[3] << 16);
                             }
-                            *reinterpret_cast<uint2*>(qb + (c8 + 2 * k + h) * R + row0 + 8 * li) = q[h];
+                            if (cval) *reinterpret_cast<uint2*>(qb + (c8 + 2 * k + h) * R + row0 + 8 * li) = q[h];
                         }
                     }
                 }
@@ -904,12 +1013,21 @@ static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t
     }
 }
 
-// The stability variants.
+// The stability variants: stochastic rounding alone on the plain kernel's bf16 path; any Hadamard
+// option on the fp32 kernel.
 static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStream_t st) {
     if (p.ntiles == 0) return MXFP8_OK;
     CUtensorMap m;
     if (!make_x_map(&m, p, p.x)) return MXFP8_ERR_DRIVER;
     const int64_t grid = std::min<int64_t>(p.ntiles, (int64_t)host::num_sms() * 2);
+    if (p.opts == MXFP8_OPT_STOCHASTIC) {
+        switch (dirs) {
+            case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeSR>(m, p, grid, st);
+            case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeSR>(m, p, grid, st);
+            case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeSR>(m, p, grid, st);
+            default: return MXFP8_ERR_LAYOUT;
+        }
+    }
     switch (dirs) {
         case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeExt>(m, p, grid, st);
         case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeExt>(m, p, grid, st);

@@ -75,14 +75,14 @@ def lib():
         L.oracle_swiglu_bf16.argtypes = [P, P, I64, P]
         L.oracle_swiglu_bwd_bf16.argtypes = [P, P, P, I64, P, P]
         L.oracle_philox4x32_10.argtypes = [P, P, P]
-        L.oracle_sr_word.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
-        L.oracle_sr_word.restype = ctypes.c_uint32
+        L.oracle_sr_byte.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
+        L.oracle_sr_byte.restype = ctypes.c_uint8
         L.oracle_e4m3_encode_sr.argtypes = [ctypes.c_double, ctypes.c_uint32]
         L.oracle_e4m3_encode_sr.restype = ctypes.c_uint8
         L.oracle_rht_signs.argtypes = [ctypes.c_uint64, P]
         L.oracle_rht32.argtypes = [P, P, P]
-        L.oracle_quantize_block_at.argtypes = [P, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint, ctypes.c_uint64,
-                                               ctypes.c_uint32, P]
+        L.oracle_quantize_block_at.argtypes = [P, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                               ctypes.c_uint64, ctypes.c_uint, ctypes.c_uint64, P]
         L.oracle_quantize_block_at.restype = ctypes.c_uint8
         L.oracle_quantize_rows_opts.argtypes = [P, I64, I64, ctypes.c_uint, ctypes.c_uint64, P, P]
         L.oracle_quantize_cols_opts.argtypes = [P, I64, I64, ctypes.c_uint, ctypes.c_uint64, P, P]
@@ -389,12 +389,14 @@ def philox4x32_10(ctr, key) -> list:
     return [int(v) for v in out]
 
 
-def sr_word(seed: int, n: int, direction: int) -> int:
-    return int(lib().oracle_sr_word(seed, n, direction))
+def sr_byte(seed: int, r: int, c: int, C: int) -> int:
+    """The random byte of element (r, c) of an input with C columns (both copies use it)."""
+    return int(lib().oracle_sr_byte(seed, r, c, C))
 
 
-def e4m3_encode_sr(y: float, r: int) -> int:
-    return int(lib().oracle_e4m3_encode_sr(float(y), int(r)))
+def e4m3_encode_sr(y: float, u: int) -> int:
+    """E4M3 code of y rounded stochastically with the random byte u."""
+    return int(lib().oracle_e4m3_encode_sr(float(y), int(u)))
 
 
 def rht_signs(seed: int) -> np.ndarray:
@@ -434,11 +436,13 @@ def quantize_cols_opts(x_u16, opts: int, seed: int):
     return qT, sT
 
 
-def quantize_block_at(x32_u16, n0: int, nstride: int, opts: int, seed: int, direction: int):
-    """One block of 32 bf16 values, element i at input index n0 + i * nstride, quantized with
-    options for copy `direction` (0 row-wise, 1 column-wise): (codes [32], scale byte)."""
+def quantize_block_at(x32_u16, r0: int, c0: int, along_rows: bool, C: int, opts: int, seed: int):
+    """One block of 32 bf16 values of an input with C columns, quantized with options: a row
+    block (element i at row r0, column c0 + i) or, with along_rows, a column block (element i at
+    row r0 + i, column c0).  Returns (codes [32], scale byte)."""
     x = _u16(x32_u16).reshape(-1)
     assert x.size == 32
     q = np.empty(32, np.uint8)
-    s_ = lib().oracle_quantize_block_at(_p(x), n0, nstride, opts, seed, direction, _p(q))
+    dr, dc = (1, 0) if along_rows else (0, 1)
+    s_ = lib().oracle_quantize_block_at(_p(x), r0, c0, dr, dc, C, opts, seed, _p(q))
     return q, int(s_)

@@ -40,10 +40,10 @@
  * SwiGLU stage: bf16 rounding pinned against torch's fp32->bf16 cast, hand
  * ties and a double-rounding case; silu against torch's fp64 silu.
  * Stability variants: Philox4x32-10 against its published known-answer
- * vectors; the Hadamard signs and the stochastic-rounding words (which output
- * word, which counter) against values written by an independent pure-Python
+ * vectors; the Hadamard signs and the stochastic-rounding bytes (which output
+ * byte, which counter) against values written by an independent pure-Python
  * Philox4x32-10 (tests/golden/stability_words.txt); stochastic rounding by hand
- * cases, exactness on the grid and its mean; the Hadamard butterflies against
+ * cases, an independent fp32 bit algorithm, exactness on the grid and its mean; the Hadamard butterflies against
  * scipy's Hadamard matrix on inputs where fp32 is exact, and orthogonality.
  */
 #include <math.h>
@@ -351,25 +351,29 @@ void oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* ou
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* The random word of element n (row-major index r*C + c of the input) for the
- * copy `dir` (0 = row-wise, 1 = column-wise): word n % 4 of Philox4x32-10 with
- * counter (n / 4 low 32 bits, n / 4 high bits, dir, 0) and key (seed low 32
- * bits, seed high 32 bits). */
-uint32_t oracle_sr_word(uint64_t seed, uint64_t n, uint32_t dir) {
-    uint32_t ctr[4] = {(uint32_t)(n >> 2), (uint32_t)(n >> 34), dir, 0u};
+/* The random byte of element (r, c) of an input with C columns (C % 8 == 0):
+ * byte 8 * (r mod 2) + (c mod 8) of the 16-byte Philox4x32-10 output (word k
+ * holds bytes 4k .. 4k+3, least significant first) for counter (b mod 2^32,
+ * b / 2^32, 0, 0), b = floor(r / 2) * (C / 8) + floor(c / 8), and key (seed
+ * low 32 bits, seed high 32 bits).  One draw serves a 2 x 8 block; the
+ * row-wise and the column-wise copy of an element use the same byte. */
+uint8_t oracle_sr_byte(uint64_t seed, uint64_t r, uint64_t c, uint64_t C) {
+    uint64_t b = (r / 2) * (C / 8) + c / 8;
+    uint32_t ctr[4] = {(uint32_t)b, (uint32_t)(b >> 32), 0u, 0u};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t o[4];
     oracle_philox4x32_10(ctr, key, o);
-    return o[n & 3];
+    unsigned k = 8u * (unsigned)(r % 2) + (unsigned)(c % 8);
+    return (uint8_t)((o[k / 4] >> (8 * (k % 4))) & 0xFFu);
 }
 
 /* Stochastic rounding of y to E4M3 (satfinite).  For |y| between the
  * consecutive finite magnitudes lo <= |y| < hi, let F = floor((|y| - lo) /
- * (hi - lo) * 2^20), the position inside the step in units of 2^-20 (the 20
- * fp32 mantissa bits E4M3 drops).  The magnitude rounds up to hi iff
- * F + (r >> 12) >= 2^20, so with r uniform it rounds up with probability
- * F / 2^20.  |y| >= 448 gives 448; the sign is applied afterwards; NaN -> 0x7F. */
-uint8_t oracle_e4m3_encode_sr(double y, uint32_t r) {
+ * (hi - lo) * 256), the position inside the step in units of 1/256 of it.  The
+ * magnitude rounds up to hi iff F + u >= 256, so with u a uniform byte it rounds
+ * up with probability F / 256.  |y| >= 448 gives 448; the sign is applied
+ * afterwards; NaN -> 0x7F. */
+uint8_t oracle_e4m3_encode_sr(double y, uint32_t u) {
     int neg = signbit(y) ? 1 : 0;
     if (isnan(y)) return (uint8_t)(0x7F | (neg << 7));
     double a = fabs(y);
@@ -381,8 +385,8 @@ uint8_t oracle_e4m3_encode_sr(double y, uint32_t r) {
         for (int c = 0; c <= 0x7E; ++c)
             if (oracle_e4m3_to_f64((uint8_t)c) <= a) lo = c;
         double vlo = oracle_e4m3_to_f64((uint8_t)lo), vhi = oracle_e4m3_to_f64((uint8_t)(lo + 1));
-        double F = floor((a - vlo) / (vhi - vlo) * 1048576.0);
-        code = (F + (double)(r >> 12) >= 1048576.0) ? lo + 1 : lo;
+        double F = floor((a - vlo) / (vhi - vlo) * 256.0);
+        code = (F + (double)(u & 0xFFu) >= 256.0) ? lo + 1 : lo;
     }
     return (uint8_t)(code | (neg << 7));
 }
@@ -417,11 +421,11 @@ void oracle_rht32(const float* x, const int8_t* d, float* y) {
     for (int i = 0; i < BLK; ++i) y[i] = t[i] * c;
 }
 
-/* One block of 32 bf16 values (element i at x[i * xstride], input index
- * n0 + i * nstride) quantized with options: bit 0 = stochastic rounding
- * (copy `dir`), bit 1 = Hadamard transform first. */
-static uint8_t quantize_block_opts(const uint16_t* x, int64_t xstride, uint64_t n0, uint64_t nstride, unsigned opts,
-                                   uint64_t seed, uint32_t dir, uint8_t* q, int64_t qstride) {
+/* One block of 32 bf16 values (element i at x[i * xstride], at row r0 + i * dr,
+ * column c0 + i * dc of an input with C columns) quantized with options:
+ * bit 0 = stochastic rounding (oracle_sr_byte), bit 1 = Hadamard transform first. */
+static uint8_t quantize_block_opts(const uint16_t* x, int64_t xstride, uint64_t r0, uint64_t c0, uint64_t dr,
+                                   uint64_t dc, uint64_t C, unsigned opts, uint64_t seed, uint8_t* q, int64_t qstride) {
     double v[BLK];
     uint32_t rw[BLK];
     if (opts & 2u) {
@@ -435,16 +439,17 @@ static uint8_t quantize_block_opts(const uint16_t* x, int64_t xstride, uint64_t 
         for (int i = 0; i < BLK; ++i) v[i] = oracle_bf16_to_f64(x[i * xstride]);
     }
     if (opts & 1u)
-        for (int i = 0; i < BLK; ++i) rw[i] = oracle_sr_word(seed, n0 + (uint64_t)i * nstride, dir);
+        for (int i = 0; i < BLK; ++i) rw[i] = oracle_sr_byte(seed, r0 + (uint64_t)i * dr, c0 + (uint64_t)i * dc, C);
     return quantize_block_f64_rw(v, BLK, q, qstride, (opts & 1u) ? rw : NULL);
 }
 
-/* One block of 32 contiguous bf16 values whose element i has input index n0 + i * nstride,
- * quantized with options for copy `dir`: 32 codes into q32, returns the scale byte (for
+/* One block of 32 contiguous bf16 values whose element i sits at row r0 + i * dr, column
+ * c0 + i * dc of an input with C columns (a row block: dr = 0, dc = 1; a column block:
+ * dr = 1, dc = 0), quantized with options: 32 codes into q32, returns the scale byte (for
  * checking single blocks of a large tensor). */
-uint8_t oracle_quantize_block_at(const uint16_t* x32, uint64_t n0, uint64_t nstride, unsigned opts, uint64_t seed,
-                                 uint32_t dir, uint8_t* q32) {
-    return quantize_block_opts(x32, 1, n0, nstride, opts, seed, dir, q32, 1);
+uint8_t oracle_quantize_block_at(const uint16_t* x32, uint64_t r0, uint64_t c0, uint64_t dr, uint64_t dc, uint64_t C,
+                                 unsigned opts, uint64_t seed, uint8_t* q32) {
+    return quantize_block_opts(x32, 1, r0, c0, dr, dc, C, opts, seed, q32, 1);
 }
 
 /* Row-wise quantization of x[R, C] with options (see quantize_block_opts). */
@@ -452,8 +457,8 @@ void oracle_quantize_rows_opts(const uint16_t* x, int64_t R, int64_t C, unsigned
                                uint8_t* s) {
     for (int64_t r = 0; r < R; ++r)
         for (int64_t b = 0; b < C / BLK; ++b)
-            s[r * (C / BLK) + b] = quantize_block_opts(x + r * C + b * BLK, 1, (uint64_t)(r * C + b * BLK), 1, opts,
-                                                       seed, 0u, q + r * C + b * BLK, 1);
+            s[r * (C / BLK) + b] = quantize_block_opts(x + r * C + b * BLK, 1, (uint64_t)r, (uint64_t)(b * BLK), 0, 1,
+                                                       (uint64_t)C, opts, seed, q + r * C + b * BLK, 1);
 }
 
 /* Column-wise quantization of x[R, C] with options, stored transposed. */
@@ -461,8 +466,8 @@ void oracle_quantize_cols_opts(const uint16_t* x, int64_t R, int64_t C, unsigned
                                uint8_t* sT) {
     for (int64_t c = 0; c < C; ++c)
         for (int64_t b = 0; b < R / BLK; ++b)
-            sT[c * (R / BLK) + b] = quantize_block_opts(x + b * BLK * C + c, C, (uint64_t)(b * BLK * C + c), (uint64_t)C,
-                                                        opts, seed, 1u, qT + c * R + b * BLK, 1);
+            sT[c * (R / BLK) + b] = quantize_block_opts(x + b * BLK * C + c, C, (uint64_t)(b * BLK), (uint64_t)c, 1, 0,
+                                                        (uint64_t)C, opts, seed, qT + c * R + b * BLK, 1);
 }
 
 /* ------------------------------------------------------------------ */

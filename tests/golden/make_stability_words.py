@@ -1,6 +1,6 @@
 #!/usr/bin/env python
 """Writes tests/golden/stability_words.txt: the random signs of the Hadamard transform and the
-stochastic-rounding words that the readings of "MXFP8 (Micro-scaling FP8)", "Numerical
+stochastic-rounding bytes that the readings of "MXFP8 (Micro-scaling FP8)", "Numerical
 stability" draw from Philox4x32-10.
 
 The generator here is a pure-Python Philox4x32-10 written from its definition in Salmon,
@@ -16,8 +16,10 @@ How each stored value is selected from the generator (the readings being pinned)
   signs  seed -> 32 characters; character i is '-' iff bit i (bit 0 = least significant) of
          output word 0 of Philox4x32-10 with counter (0, 0, 2, 0) and key
          (seed mod 2^32, seed >> 32) is set, else '+'.
-  sr     (seed, n, dir) -> output word (n mod 4) of Philox4x32-10 with counter
-         (floor(n / 4) mod 2^32, floor(n / 2^34), dir, 0) and the same key.
+  sr     (seed, r, c, C) -> the random byte of element (r, c) of an input with C columns:
+         byte 8 * (r mod 2) + (c mod 8) of the 16-byte output (output word k holds bytes
+         4k .. 4k+3, least significant first) for counter (b mod 2^32, floor(b / 2^32), 0, 0),
+         b = floor(r / 2) * (C / 8) + floor(c / 8), and the same key.
 
     python tests/golden/make_stability_words.py      # rewrites the golden file
 """
@@ -70,18 +72,24 @@ def signs(seed: int) -> str:
     return "".join("-" if (w0 >> i) & 1 else "+" for i in range(32))
 
 
-def sr_word(seed: int, n: int, direction: int) -> int:
-    out = philox4x32_10([(n >> 2) & MASK, (n >> 34) & MASK, direction, 0], key_of(seed))
-    return out[n & 3]
+def sr_block(r: int, c: int, C: int) -> int:
+    return (r // 2) * (C // 8) + c // 8
+
+
+def sr_byte(seed: int, r: int, c: int, C: int) -> int:
+    b = sr_block(r, c, C)
+    out = philox4x32_10([b & MASK, (b >> 32) & MASK, 0, 0], key_of(seed))
+    k = 8 * (r % 2) + c % 8
+    return (out[k // 4] >> (8 * (k % 4))) & 0xFF
 
 
 SIGN_SEEDS = [0, 1, 0x5EED, 0x0123456789ABCDEF, (1 << 40) + 3]
-SR_CASES = [
-    (0, 0, 0), (0, 1, 1), (0, 2, 0), (0, 3, 1),
-    (0x5EED, 12345, 0), (0x5EED, 12345, 1),
-    (0x0123456789ABCDEF, 7, 0), (0x0123456789ABCDEF, (1 << 32) + 6, 1),
-    (0x0123456789ABCDEF, (1 << 34) + 5, 0), (0x0123456789ABCDEF, (1 << 34) + 5, 1),
-    ((1 << 63) + 11, (3 << 34) + (1 << 33) + 2, 1), (42, 16384 * 5120 - 1, 0),
+SR_CASES = [  # (seed, r, c, C): both row parities, all byte positions of a word, blocks past 2^32
+    (0, 0, 0, 8), (0, 0, 5, 8), (0, 1, 2, 8), (0, 1, 7, 8),
+    (0x5EED, 12345, 4321, 5120), (0x5EED, 12344, 4321, 5120), (0x5EED, 12345, 4326, 5120),
+    (0x0123456789ABCDEF, 65599, 8191, 8192), (0x0123456789ABCDEF, 2, 9, 32),
+    (0x0123456789ABCDEF, (1 << 23) + 3, 1030, 8192), (0x0123456789ABCDEF, (3 << 24) + 2, 17, 8192),
+    ((1 << 63) + 11, 40001, 6, 5120), (42, 16383, 5119, 5120),
 ]
 
 
@@ -92,13 +100,14 @@ def main():
         "# pure-Python Philox4x32-10 (Salmon et al., SC 2011) checked against philox4x32_10_kat.txt.",
         "# sign <seed hex> <32 signs>: sign i is '-' iff bit i of output word 0 of Philox4x32-10 with",
         "#      counter (0, 0, 2, 0), key (seed mod 2^32, seed >> 32) is set ('+' otherwise).",
-        "# sr <seed hex> <n hex> <dir> <word hex>: output word (n mod 4) of Philox4x32-10 with counter",
-        "#      (floor(n/4) mod 2^32, floor(n/2^34), dir, 0) and the same key.",
+        "# sr <seed hex> <r> <c> <C> <byte hex>: byte 8(r mod 2) + (c mod 8) of the Philox4x32-10 output",
+        "#      (word k = bytes 4k..4k+3, least significant first) for counter (b mod 2^32, floor(b/2^32), 0, 0),",
+        "#      b = floor(r/2)(C/8) + floor(c/8), and the same key.",
     ]
     for s in SIGN_SEEDS:
         lines.append(f"sign {s:x} {signs(s)}")
-    for s, n, d in SR_CASES:
-        lines.append(f"sr {s:x} {n:x} {d} {sr_word(s, n, d):08x}")
+    for s, r, c, C in SR_CASES:
+        lines.append(f"sr {s:x} {r} {c} {C} {sr_byte(s, r, c, C):02x}")
     with open(OUT, "w") as f:
         f.write("\n".join(lines) + "\n")
     print(OUT)

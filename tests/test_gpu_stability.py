@@ -2,9 +2,10 @@
 random Hadamard transforms spread outliers before quantization; stochastic rounding removes the
 bias of deterministic rounding) against the oracle, byte for byte.
 
-Both sides draw the same Philox4x32-10 words (counter from the element index and the copy, key
-from the seed) and evaluate the Hadamard butterflies in fp32 in the same order, so codes and
-scales must agree exactly, padding of the blocked layouts included.  The composite op's GEMMs
+Both sides draw the same Philox4x32-10 bytes (counter from the element's 2 x 8 block, key from the
+seed; one byte per element, shared by its two copies) and evaluate the Hadamard butterflies in
+fp32 in the same order, so codes and scales must agree exactly, padding of the blocked layouts
+included.  The composite op's GEMMs
 with these options are compared with the oracle's fp64 GEMMs of the oracle's operands within
 the GEMM bound."""
 import numpy as np
@@ -163,7 +164,7 @@ def test_full_size_grouped_sampled(mx):
         g = group_of(int(r))
         pr = padded[g] + int(r) - starts[g]
         for b in rng.integers(0, K // 32, 3):
-            qo, so = oracle.quantize_block_at(u16(x[r, 32 * b:32 * b + 32]), int(r) * K + 32 * int(b), 1, o_opts, SEED, 0)
+            qo, so = oracle.quantize_block_at(u16(x[r, 32 * b:32 * b + 32]), int(r), 32 * int(b), False, K, o_opts, SEED)
             assert np.array_equal(u8(q[r, 32 * b:32 * b + 32]), qo)
             assert int(s[oracle.blocked_offset(int(pr), int(b), K // 128)].item()) == so
     ct = int(padded[-1]) // 128
@@ -172,8 +173,8 @@ def test_full_size_grouped_sampled(mx):
         if sizes[g] == 0:
             continue
         t0 = int(starts[g]) + 32 * int(rng.integers(0, sizes[g] // 32))
-        qo, so = oracle.quantize_block_at(np.ascontiguousarray(u16(x[t0:t0 + 32, c])), t0 * K + int(c), K, o_opts,
-                                          SEED, 1)
+        qo, so = oracle.quantize_block_at(np.ascontiguousarray(u16(x[t0:t0 + 32, c])), t0, int(c), True, K, o_opts,
+                                          SEED)
         assert np.array_equal(u8(qT[c, t0:t0 + 32]), qo)
         cq = padded[g] // 32 + (t0 - starts[g]) // 32
         assert int(sT[oracle.blocked_offset(int(c), int(cq), ct)].item()) == so
