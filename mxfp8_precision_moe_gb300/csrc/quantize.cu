@@ -140,73 +140,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // with C columns.  Counter (b mod 2^32, b / 2^32, 0, 0), b = rp * (C / 8) + cb, key = seed; byte
 // 8 (r mod 2) + (c mod 8) of the output (word k = bytes 4k .. 4k+3, least significant first) belongs
 // to element (r, c).  The row-wise and the column-wise copy of an element use the same byte.
-// Out of line: one copy of the ten unrolled rounds serves every call site (the kernel body stays small
-// enough for the instruction caches).
+// Out of line in the Hadamard kernel: one copy of the ten unrolled rounds serves its call sites (its
+// body stays small enough for the instruction caches).
 __device__ __noinline__ uint4 sr_draw(uint64_t rp, uint64_t cb, uint64_t C, uint64_t seed) {
     const uint64_t b = rp * (C >> 3) + cb;
     return philox4x32_10(make_uint4((uint32_t)b, (uint32_t)(b >> 32), 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
-}
-
-// E4M3 code of y rounded stochastically with the random byte u (0..255).  Between consecutive finite
-// magnitudes lo <= |y| < hi the magnitude rounds up iff F + u >= 256, with F the part of |y| above lo
-// in units of 1/256 of the step (truncated); |y| >= 448 gives 448; the sign is y's.
-//   |y| >= 2^-6: the step is the unit of fp32 mantissa bit 20, so F is the top 8 of the 20 bits E4M3
-//     drops: adding u at bit 12 carries into bit 20 exactly when F + u >= 256, and the E4M3 code is
-//     then the fp32 pattern's bits 20.. less 120 << 3 (the exponent bias difference), capped at 0x7E.
-//   |y| <  2^-6: the step is 2^-9; F_total = floor(|y| 2^17) holds the code below |y| in its bits
-//     8.. and F in its bits 0-7, computed from the fp32 mantissa M and exponent E as M >> (133 - E).
-__device__ __forceinline__ uint32_t sr_code_f32(float y, uint32_t u) {
-    const uint32_t bits = __float_as_uint(y), a = bits & 0x7FFFFFFFu;
-    uint32_t code;
-    if (a >= 0x3C800000u) {
-        code = min(((a + (u << 12)) >> 20) - 960u, 0x7Eu);
-    } else {
-        const uint32_t E = a >> 23;
-        const uint32_t M = (a & 0x7FFFFFu) | (E ? 0x800000u : 0u);
-        const uint32_t sh = 133u - (E ? E : 1u);  // >= 13
-        const uint32_t F = sh >= 32u ? 0u : (M >> sh);
-        code = (F >> 8) + (((F & 0xFFu) + u) >> 8);
-    }
-    return code | ((bits >> 24) & 0x80u);
-}
-
-// Exact stochastic codes (bytes 0 and 2, with signs) of the halves of a scaled bf16 pair yy that win
-// marks (bits 15 / 31), the others left as in c; ub holds the two random bytes in bits 0-7, 16-23.
-__device__ __noinline__ uint32_t sr_fix_pair(uint32_t yy, uint32_t ub, uint32_t c, uint32_t win) {
-    if (win & 0x8000u) c = (c & 0xFFFF0000u) | sr_code_f32(__uint_as_float(yy << 16), ub & 0xFFu);
-    if (win & 0x80000000u) c = (c & 0xFFFFu) | (sr_code_f32(__uint_as_float(yy & 0xFFFF0000u), (ub >> 16) & 0xFFu) << 16);
-    return c;
-}
-
-// Two E4M3 codes (bytes 0 and 2) of a scaled bf16 pair yy (exact: x times a power of two) rounded
-// stochastically; ub holds each element's random byte in bits 0-7 and 16-23.  A bf16 y has 8
-// significant bits, so on the normal E4M3 range its 4 mantissa bits below the E4M3 step are F / 16,
-// and F + u >= 256 is (those 4 bits) + (u >> 4) >= 16: one packed add carries into the E4M3 mantissa
-// (the sign bit is left alone), the code is the pattern's bits 4-14 less 120 << 3, clamped to 0 .. 0x7E
-// per half, and bit 15 moves to bit 7.  Below 2^-17 that also holds (F = 0: code 0 with the sign).
-// Magnitudes in [2^-17, 2^-6) (bf16 0x3700 .. 0x3C7F: E4M3 subnormals with F > 0) take the fp32 rule
-// out of line.  (A NaN half can carry into the other half; both then belong to a non-finite block,
-// whose codes are replaced.)
-__device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t sr_pair_bf16x2(uint32_t yy, uint32_t ub) {
-    const uint32_t t = yy + ((ub >> 4) & 0x000F000Fu);
-    uint32_t c = vmin_u16x2(vmax_u16x2((t >> 4) & 0x07FF07FFu, 0x03C003C0u) - 0x03C003C0u, 0x007E007Eu);
-    c |= (t >> 8) & 0x00800080u;
-    const uint32_t mag = yy & 0x7FFF7FFFu;
-    const uint32_t win = ~(mag + 0x43804380u) & (mag + 0x49004900u) & 0x80008000u;  // 0x3700 <= half < 0x3C80
-    if (win) c = sr_fix_pair(yy, ub, c, win);
-    return c;
-}
-
-// Bytes b and b + 1 (b = 0 or 2) of a random word into bits 0-7 and 16-23.
-__device__ __forceinline__ uint32_t sr_pick2(uint32_t w, int b) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(w), "r"(b ? 0x4342u : 0x4140u));
-    return d;
 }
 
 // bf16 x bf16 -> bf16 for both halves (round to nearest even; exact for x times a power of two).
@@ -214,6 +152,46 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
+}
+
+// Stochastic rounding on fp32 patterns.  E4M3 steps by 2^-9 below 2^-6 and keeps 3 mantissa bits above
+// it; fp32 steps by 2^-149 below 2^-126 and keeps 23 bits above it.  So the fp32 pattern of
+// z = |y| 2^-120, rounded toward zero, holds in bits 20.. the E4M3 code of |y| truncated (subnormal
+// or normal alike) and in bits 12-19 F = floor(256 (|y| - lo) / (hi - lo)).  Adding u << 12 carries
+// into bit 20 exactly when F + u >= 256; clearing bits 0-19 leaves the chosen E4M3 magnitude times
+// 2^-120 (with y's sign, which the add never reaches), and scaling back by 2^120 gives a value that
+// the round-to-nearest conversion returns unchanged, or saturates to 448 at and above 448.
+// One half of a bf16 pair times 2^-120 as an fp32, rounded toward zero.
+template <int H>
+__device__ __forceinline__ float bf16_times_2m120(uint32_t yy) {
+    float d;
+    if constexpr (H == 0)
+        asm("{\n\t.reg .b16 a0, a1, c;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b16 c, 0x0380;\n\t"
+            "fma.rz.f32.bf16 %0, a0, c, 0f80000000;\n\t}" : "=f"(d) : "r"(yy));
+    else
+        asm("{\n\t.reg .b16 a0, a1, c;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b16 c, 0x0380;\n\t"
+            "fma.rz.f32.bf16 %0, a1, c, 0f80000000;\n\t}" : "=f"(d) : "r"(yy));
+    return d;
+}
+__device__ __forceinline__ float f32_times_2m120(float y) {
+    float d;
+    asm("mul.rz.f32 %0, %1, 0f03800000;" : "=f"(d) : "f"(y));
+    return d;
+}
+// z = y 2^-120 (toward zero) and byte b of the random word w -> the E4M3 value stochastic rounding
+// picks, as an fp32.  (One asm block: the byte is moved to bits 12-19 and added in place, so that the
+// two copies' uses of a byte stay separate expressions, not one value held from copy to copy.)
+__device__ __forceinline__ float sr_pick_value(float z, uint32_t w, int b) {
+    float d;
+    asm("{\n\t.reg .b32 t;\n\tprmt.b32 t, %2, 0, %3;\n\tshl.b32 t, t, 4;\n\tadd.u32 t, t, %1;\n\t"
+        "and.b32 t, t, 0xFFF00000;\n\tmul.rn.f32 %0, t, 0f7B800000;\n\t}"
+        : "=f"(d) : "r"(__float_as_uint(z)), "r"(w), "r"(0x4404u | ((uint32_t)b << 4)));
+    return d;
+}
+// The stochastic codes (bytes 0 and 1) of a scaled bf16 pair yy (exact: x times a power of two); the
+// random byte of half h is byte b_h of word w_h.
+__device__ __forceinline__ uint32_t sr_pair_bf16x2(uint32_t yy, uint32_t w0, int b0, uint32_t w1, int b1) {
+    return cvt_e4m3x2(sr_pick_value(bf16_times_2m120<0>(yy), w0, b0), sr_pick_value(bf16_times_2m120<1>(yy), w1, b1));
 }
 
 // E8M0 scale byte from the magnitude bits of an fp32 amax (same rule as for bf16: max(E - 8, 0)).
@@ -538,14 +516,16 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
             // Stability variants: fp32 values; optionally a Hadamard transform of every block of 32
             // along the copy's axis, y = c * H * (D x) (signs D, butterflies h = 1, 2, 4 inside the
             // lane, h = 8, 16 across lanes, in that order); codes by round-to-nearest-even or by
-            // stochastic rounding with per-element Philox words.  Rows (row copy) and columns
+            // stochastic rounding with one random byte per element.  Rows (row copy) and columns
             // (column copy) are processed 4 at a time to keep the fp32 values in registers.
             const bool sr = p.opts & MXFP8_OPT_STOCHASTIC;
             const uint32_t dsign = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)p.seed,
                                                  (uint32_t)(p.seed >> 32)).x;
-            // two codes from two fp32 values and (stochastic rounding) their random bytes
-            auto code2 = [&](float z0, float z1, uint32_t u0, uint32_t u1) -> uint32_t {
-                return sr ? sr_code_f32(z0, u0) | (sr_code_f32(z1, u1) << 8) : cvt_e4m3x2(z0, z1);
+            // two codes from two scaled fp32 values and (stochastic rounding) their random bytes: byte b0
+            // of word w0, byte b1 of word w1
+            auto code2 = [&](float z0, float z1, uint32_t w0, int b0, uint32_t w1, int b1) -> uint32_t {
+                return sr ? cvt_e4m3x2(sr_pick_value(f32_times_2m120(z0), w0, b0), sr_pick_value(f32_times_2m120(z1), w1, b1))
+                          : cvt_e4m3x2(z0, z1);
             };
             const uint64_t rp0 = (uint64_t)((row0 + 8 * li) >> 1), cb = (uint64_t)(c8 >> 3);  // this lane's draws
             if constexpr (kRow) {
@@ -621,10 +601,8 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         const uint32_t wa = (i & 1) ? dr[i >> 1].z : dr[i >> 1].x;  // columns 0-3
                         const uint32_t wb = (i & 1) ? dr[i >> 1].w : dr[i >> 1].y;  // columns 4-7
                         uint2 q;
-                        q.x = code2(y[i][0] * f, y[i][1] * f, wa & 0xFFu, (wa >> 8) & 0xFFu) |
-                              (code2(y[i][2] * f, y[i][3] * f, (wa >> 16) & 0xFFu, wa >> 24) << 16);
-                        q.y = code2(y[i][4] * f, y[i][5] * f, wb & 0xFFu, (wb >> 8) & 0xFFu) |
-                              (code2(y[i][6] * f, y[i][7] * f, (wb >> 16) & 0xFFu, wb >> 24) << 16);
+                        q.x = code2(y[i][0] * f, y[i][1] * f, wa, 0, wa, 1) | (code2(y[i][2] * f, y[i][3] * f, wa, 2, wa, 3) << 16);
+                        q.y = code2(y[i][4] * f, y[i][5] * f, wb, 0, wb, 1) | (code2(y[i][6] * f, y[i][7] * f, wb, 2, wb, 3) << 16);
                         if (sc == 0xFFu) {
                             uint32_t sg[2] = {0u, 0u};
 #pragma unroll
@@ -711,8 +689,7 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            qc[j][rr >> 2] |= code2(y[rr][j] * f[j], y[rr + 1][j] * f[j], (wa >> (8 * j)) & 0xFFu,
-                                                    (wb >> (8 * j)) & 0xFFu) << (8 * (rr & 3));
+                            qc[j][rr >> 2] |= code2(y[rr][j] * f[j], y[rr + 1][j] * f[j], wa, j, wb, j) << (8 * (rr & 3));
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -736,12 +713,20 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
             continue;
         }
 
-        // Stochastic rounding: the random bytes of this lane's 8 x 8 patch; draw d covers its rows 2d,
-        // 2d + 1 (words x, y: row 2d, columns 0-3 / 4-7; words z, w: row 2d + 1).  Drawn where they are
-        // used, so that no more than one copy's draws are live at a time.
-        auto draw = [&](int d) -> uint4 {
-            return sr_draw((uint64_t)((row0 + 8 * li) >> 1) + d, (uint64_t)(c8 >> 3), (uint64_t)C, p.seed);
-        };
+        // Stochastic rounding: the random bytes of this lane's 8 x 8 patch, drawn once for both copies;
+        // draw d covers its rows 2d, 2d + 1 (words x, y: row 2d, columns 0-3 / 4-7; words z, w: row
+        // 2d + 1).
+        uint4 rnd[4];
+        if constexpr (kMode == kModeSR) {
+            const uint64_t cq = (uint64_t)C >> 3;
+            const uint64_t b0 = (uint64_t)((row0 + 8 * li) >> 1) * cq + (uint64_t)(c8 >> 3);
+#pragma unroll
+            for (int d = 0; d < 4; ++d) {
+                const uint64_t bd = b0 + (uint64_t)d * cq;
+                rnd[d] = philox4x32_10(make_uint4((uint32_t)bd, (uint32_t)(bd >> 32), 0u, 0u), (uint32_t)p.seed,
+                                       (uint32_t)(p.seed >> 32));
+            }
+        }
         // the plain MX quantization of one 8 x 8 patch per lane (bf16 pairs v) into one output set
         auto quant_rowcol = [&](const uint32_t (&v)[8][4], uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                                 uint8_t* s_col) {
@@ -791,16 +776,18 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                     uint2 q[2];
                     if constexpr (kMode == kModeSR) {
                         // rows 2k (scale in the low half of f2) and 2k + 1 (high half): draw k
-                        const uint4 rk = draw(k);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const uint32_t fs = h ? (f2 & 0xFFFF0000u) | (f2 >> 16) : (f2 & 0xFFFFu) | (f2 << 16);
-                            const uint32_t w0 = h ? rk.z : rk.x, w1 = h ? rk.w : rk.y;  // columns 0-3 / 4-7
+                            const uint32_t w0 = h ? rnd[k].z : rnd[k].x, w1 = h ? rnd[k].w : rnd[k].y;  // columns 0-3 / 4-7
                             uint32_t c[4];
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                c[kk] = sr_pair_bf16x2(mul_bf16x2(v[2 * k + h][kk], fs), sr_pick2(kk < 2 ? w0 : w1, (kk & 1) * 2));
-                            q[h] = make_uint2(__byte_perm(c[0], c[1], 0x6420), __byte_perm(c[2], c[3], 0x6420));
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t w = kk < 2 ? w0 : w1;  // columns 2kk, 2kk + 1: bytes 2 (kk % 2), + 1
+                                c[kk] = sr_pair_bf16x2(mul_bf16x2(v[2 * k + h][kk], fs), w, 2 * (kk & 1), w,
+                                                       2 * (kk & 1) + 1);
+                            }
+                            q[h] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
                         }
                     } else {
                         q[0] = quant8_bf16<0>(v[2 * k], f2);
@@ -851,11 +838,6 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                 for (int k = 0; k < 4; ++k) nf |= s2c[k] + kNonfiniteAdd;
                 const bool any_nonfinite = __any_sync(0xffffffffu, (nf & kNonfiniteBits) != 0u);
                 uint8_t* qb = q_col + b * R * C;
-                uint4 rnd[4];         // stochastic rounding: every column pair needs all four draws
-                if constexpr (kMode == kModeSR) {
-#pragma unroll
-                    for (int d = 0; d < 4; ++d) rnd[d] = draw(d);
-                }
                 // codes of column 2k + h: elements (rr, half h of word k) times half h of the scale pair
                 auto col_codes = [&](auto hc, int k, uint32_t f2) -> uint2 {
                     constexpr int h = decltype(hc)::value;
@@ -866,16 +848,13 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                         const uint32_t fs = h ? (f2 & 0xFFFF0000u) | (f2 >> 16) : (f2 & 0xFFFFu) | (f2 << 16);
                         constexpr uint32_t kPickH = h ? 0x7632u : 0x5410u;  // half h of two words -> one pair
                         const int j = 2 * k + h, wsel = j >> 2, b = j & 3;
-                        const uint32_t sel = (uint32_t)b | ((uint32_t)(4 + b) << 8);  // byte b of each word
 #pragma unroll
                         for (int rr = 0; rr < 8; rr += 2) {
                             const uint4 r4 = rnd[rr >> 1];
                             const uint32_t wa = wsel ? r4.y : r4.x, wb = wsel ? r4.w : r4.z;
-                            uint32_t ub, xx;
-                            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(ub) : "r"(wa), "r"(wb), "r"(sel));
+                            uint32_t xx;
                             asm("prmt.b32 %0, %1, %2, %3;" : "=r"(xx) : "r"(v[rr][k]), "r"(v[rr + 1][k]), "r"(kPickH));
-                            const uint32_t c = sr_pair_bf16x2(mul_bf16x2(xx, fs), ub & 0x00FF00FFu);
-                            w[rr >> 1] = (c & 0xFFu) | ((c >> 8) & 0xFF00u);
+                            w[rr >> 1] = sr_pair_bf16x2(mul_bf16x2(xx, fs), wa, b, wb, b);
                         }
                     } else {
 #pragma unroll

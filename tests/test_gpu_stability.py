@@ -88,6 +88,44 @@ def test_blocked_grouped(mx, opts):
     assert np.array_equal(sT[:n_col], oracle.blocked_colgroups(sTo, ends))
 
 
+def special_values_input(M, K, seed):
+    """mixed_input with blocks the stochastic-rounding paths treat apart: Inf / NaN (a non-finite
+    block keeps its replaced codes), whole blocks of bf16 subnormals (scale byte 0, codes from the
+    normal E4M3 range), signed zeros, and elements at 2^-17 .. 2^-6 after scaling (the E4M3
+    subnormal range, where the exact rule decides)."""
+    x = mixed_input(M, K, seed).float()
+    x[0, 5], x[3, 40], x[70, 64] = float("inf"), float("nan"), -float("inf")
+    x[100:132, 200] = float("nan")
+    i = torch.arange(32, dtype=torch.float32)
+    sub = torch.ldexp(1.0 + i / 32.0, -127.0 - (i % 7))                     # [2^-133, 2^-126): bf16 subnormals
+    x[10, :32] = sub * torch.where(i % 3 == 0, -1.0, 1.0)
+    x[32:64, 96] = sub
+    x[11, :] = 0.0
+    x[12, :32] = -0.0
+    # one element at 256 * 2^e (the block amax), the others at 2^-17 .. 2^-5 of it (scaled: 2^-9 .. 2^3)
+    x[13, 32:64] = torch.ldexp(torch.full((32,), 1.5), 8.0 - i)
+    x[14, 64:96] = -x[13, 32:64]
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("dirs", [1, 2, 3])
+def test_sr_special_values(mx, dirs):
+    """Stochastic rounding alone runs a packed bf16 path with an exact pass for the E4M3 subnormal
+    range: both against the oracle on special blocks, codes and scales byte for byte."""
+    M, K = 256, 384
+    x = special_values_input(M, K, seed=70 + dirs)
+    out = mx.mxfp8_quantize_2d(x.cuda(), dirs, mx.SCALES_COMPACT, opts=1, seed=SEED)
+    (qo, so), (qTo, sTo) = oracle_opts(x, 1, SEED)
+    if dirs & 1:
+        q, s = u8(out[0]), u8(out[1])
+        assert np.array_equal(s, so)
+        assert np.array_equal(q, qo), f"{int((q != qo).sum())} row codes differ"
+    if dirs & 2:
+        qT, sT = u8(out[2]), u8(out[3])
+        assert np.array_equal(sT, sTo)
+        assert np.array_equal(qT, qTo), f"{int((qT != qTo).sum())} column codes differ"
+
+
 def test_seed_changes_only_what_it_keys(mx):
     x = mixed_input(64, 128, seed=60).cuda()
     a = mx.mxfp8_quantize_2d(x, mx.ROW, mx.SCALES_COMPACT, opts=1, seed=1)
