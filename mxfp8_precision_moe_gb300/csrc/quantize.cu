@@ -60,10 +60,10 @@ struct QParams {
     uint8_t* s_col2;
 };
 
-// Kernel modes: plain MX quantization; the Hadamard variants (fp32 values, optionally with
-// stochastic rounding); the fused SwiGLU backward (three inputs dh, h1, h3; two quantized outputs);
+// Kernel modes: plain MX quantization; the Hadamard variants (fp32 values), without and with
+// stochastic rounding; the fused SwiGLU backward (three inputs dh, h1, h3; two quantized outputs);
 // stochastic rounding alone (the plain kernel's bf16 data path with stochastic codes).
-enum QuantMode : int { kModePlain = 0, kModeExt = 1, kModeSwiBwd = 2, kModeSR = 3 };
+enum QuantMode : int { kModePlain = 0, kModeExt = 1, kModeSwiBwd = 2, kModeSR = 3, kModeExtSR = 4 };
 
 // Warp 0 builds, for G groups over R rows, the clamped monotone end rows and
 // the padded start rows P[g] = sum_{h<g} ceil(size_h/128)*128 (also the scale
@@ -134,17 +134,6 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
         k1 += 0xBB67AE85u;
     }
     return c;
-}
-
-// The random bytes of one 2 x 8 block: rows 2 rp, 2 rp + 1 and columns 8 cb .. 8 cb + 7 of an input
-// with C columns.  Counter (b mod 2^32, b / 2^32, 0, 0), b = rp * (C / 8) + cb, key = seed; byte
-// 8 (r mod 2) + (c mod 8) of the output (word k = bytes 4k .. 4k+3, least significant first) belongs
-// to element (r, c).  The row-wise and the column-wise copy of an element use the same byte.
-// Out of line in the Hadamard kernel: one copy of the ten unrolled rounds serves its call sites (its
-// body stays small enough for the instruction caches).
-__device__ __noinline__ uint4 sr_draw(uint64_t rp, uint64_t cb, uint64_t C, uint64_t seed) {
-    const uint64_t b = rp * (C >> 3) + cb;
-    return philox4x32_10(make_uint4((uint32_t)b, (uint32_t)(b >> 32), 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
 // bf16 x bf16 -> bf16 for both halves (round to nearest even; exact for x times a power of two).
@@ -275,14 +264,15 @@ constexpr int kQThreads = 288;                 // 8 consumer warps + 1 TMA produ
 constexpr int kQSmem = kQStages * kQTileBytes + 128;
 constexpr int kQConsumerThreads = 256;           // 8 consumer warps (the producer warp is the ninth)
 
-// kModeExt: the stability variants of ROW / COL / ROW|COL (runtime options p.opts, seed p.seed);
-// fp32 working values.  kModeSwiBwd (ROW|COL only): 256 threads, no TMA ring: each warp loads its
+// kModeExt / kModeExtSR: the Hadamard variants of ROW / COL / ROW|COL (runtime options p.opts, seed
+// p.seed), without / with stochastic rounding; fp32 working values in the transformed copies.
+// kModeSR: stochastic rounding alone, on the bf16 data path.  kModeSwiBwd (ROW|COL only): 256 threads, no TMA ring: each warp loads its
 // patches of dh, h1 and h3 straight from global memory (three inputs a stage would leave room for
 // too few warps to hide the arithmetic's latency), computes dh1 and dh3 and quantizes each both ways.
 template <unsigned DIRS, int kMode = kModePlain>
 __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
-    constexpr bool kExt = kMode == kModeExt;
+    constexpr bool kExt = kMode == kModeExt || kMode == kModeExtSR;
     constexpr bool kSwiBwd = kMode == kModeSwiBwd;
     constexpr int kStages = kQStages;
     constexpr uint32_t kStageBytes = kQTileBytes;
@@ -512,212 +502,14 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
             w[16] = (uint8_t)(my >> 16);
         };
 
-        if constexpr (kExt) {
-            // Stability variants: fp32 values; optionally a Hadamard transform of every block of 32
-            // along the copy's axis, y = c * H * (D x) (signs D, butterflies h = 1, 2, 4 inside the
-            // lane, h = 8, 16 across lanes, in that order); codes by round-to-nearest-even or by
-            // stochastic rounding with one random byte per element.  Rows (row copy) and columns
-            // (column copy) are processed 4 at a time to keep the fp32 values in registers.
-            const bool sr = p.opts & MXFP8_OPT_STOCHASTIC;
-            const uint32_t dsign = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)p.seed,
-                                                 (uint32_t)(p.seed >> 32)).x;
-            // two codes from two scaled fp32 values and (stochastic rounding) their random bytes: byte b0
-            // of word w0, byte b1 of word w1
-            auto code2 = [&](float z0, float z1, uint32_t w0, int b0, uint32_t w1, int b1) -> uint32_t {
-                return sr ? cvt_e4m3x2(sr_pick_value(f32_times_2m120(z0), w0, b0), sr_pick_value(f32_times_2m120(z1), w1, b1))
-                          : cvt_e4m3x2(z0, z1);
-            };
-            const uint64_t rp0 = (uint64_t)((row0 + 8 * li) >> 1), cb = (uint64_t)(c8 >> 3);  // this lane's draws
-            if constexpr (kRow) {
-                uint32_t s8[8];
-                uint8_t* qb = p.q_row + b * R * C;
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    float y[4][8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(src + (4 * hr + i) * 256);
-                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            y[i][2 * k] = bf16lo(w[k]);
-                            y[i][2 * k + 1] = bf16hi(w[k]);
-                        }
-                    }
-                    if (p.opts & MXFP8_OPT_HADAMARD_ROW) {
-                        // block position of (row, c): 8 * (lj & 3) + c
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-#pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                if ((dsign >> (8 * (lj & 3) + c)) & 1u) y[i][c] = -y[i][c];
-#pragma unroll
-                        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                                for (int c = 0; c < 8; ++c)
-                                    if ((c & h) == 0) {
-                                        const float a = y[i][c], bb = y[i][c + h];
-                                        y[i][c] = a + bb;
-                                        y[i][c + h] = a - bb;
-                                    }
-#pragma unroll
-                        for (int m = 1; m <= 2; m <<= 1) {
-                            const bool upper = lane & m;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                                for (int c = 0; c < 8; ++c) {
-                                    const float o = __shfl_xor_sync(0xffffffffu, y[i][c], m);
-                                    y[i][c] = upper ? o - y[i][c] : y[i][c] + o;
-                                }
-                        }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) y[i][c] *= kRhtScale;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t m = 0;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) m = max(m, __float_as_uint(y[i][c]) & 0x7FFFFFFFu);
-                        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                        m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                        s8[4 * hr + i] = e8m0_from_f32bits(m);
-                    }
-                    // rows 4hr .. 4hr+3 of the patch: draws 2hr and 2hr + 1 (rows 2d: words x, y; rows 2d+1: z, w)
-                    uint4 dr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-                    if (sr) {
-                        dr[0] = sr_draw(rp0 + 2 * hr, cb, (uint64_t)C, p.seed);
-                        dr[1] = sr_draw(rp0 + 2 * hr + 1, cb, (uint64_t)C, p.seed);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t sc = s8[4 * hr + i];
-                        const int64_t row = row0 + 8 * li + 4 * hr + i;
-                        const float f = inv_scale_from_e8m0(sc);
-                        const uint32_t wa = (i & 1) ? dr[i >> 1].z : dr[i >> 1].x;  // columns 0-3
-                        const uint32_t wb = (i & 1) ? dr[i >> 1].w : dr[i >> 1].y;  // columns 4-7
-                        uint2 q;
-                        q.x = code2(y[i][0] * f, y[i][1] * f, wa, 0, wa, 1) | (code2(y[i][2] * f, y[i][3] * f, wa, 2, wa, 3) << 16);
-                        q.y = code2(y[i][4] * f, y[i][5] * f, wb, 0, wb, 1) | (code2(y[i][6] * f, y[i][7] * f, wb, 2, wb, 3) << 16);
-                        if (sc == 0xFFu) {
-                            uint32_t sg[2] = {0u, 0u};
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) sg[c >> 2] |= ((__float_as_uint(y[i][c]) >> 24) & 0x80u) << (8 * (c & 3));
-                            q.x = 0x7F7F7F7Fu | sg[0];
-                            q.y = 0x7F7F7F7Fu | sg[1];
-                        }
-                        if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
-                    }
-                }
-                store_row_scales(p.s_row, s8[0] | (s8[1] << 8) | (s8[2] << 16) | (s8[3] << 24),
-                                 s8[4] | (s8[5] << 8) | (s8[6] << 16) | (s8[7] << 24));
-            }
-            if constexpr (kCol) {
-                uint32_t sc[8];
-                uint8_t* qb = p.q_col + b * R * C;
-#pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {
-                    float y[8][4];  // columns 4hc .. 4hc+3 of the lane
-#pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) {
-                        const uint2 u = *reinterpret_cast<const uint2*>(src + rr * 256 + 8 * hc);
-                        y[rr][0] = bf16lo(u.x);
-                        y[rr][1] = bf16hi(u.x);
-                        y[rr][2] = bf16lo(u.y);
-                        y[rr][3] = bf16hi(u.y);
-                    }
-                    if (p.opts & MXFP8_OPT_HADAMARD_COL) {
-                        // block position of (rr, column): 8 * li + rr
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr)
-                            if ((dsign >> (8 * li + rr)) & 1u)
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) y[rr][j] = -y[rr][j];
-#pragma unroll
-                        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-                            for (int rr = 0; rr < 8; ++rr)
-                                if ((rr & h) == 0)
-#pragma unroll
-                                    for (int j = 0; j < 4; ++j) {
-                                        const float a = y[rr][j], bb = y[rr + h][j];
-                                        y[rr][j] = a + bb;
-                                        y[rr + h][j] = a - bb;
-                                    }
-#pragma unroll
-                        for (int m = 8; m <= 16; m <<= 1) {
-                            const bool upper = lane & m;
-#pragma unroll
-                            for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const float o = __shfl_xor_sync(0xffffffffu, y[rr][j], m);
-                                    y[rr][j] = upper ? o - y[rr][j] : y[rr][j] + o;
-                                }
-                        }
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) y[rr][j] *= kRhtScale;
-                    }
-                    float f[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t m = 0;
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr) m = max(m, __float_as_uint(y[rr][j]) & 0x7FFFFFFFu);
-                        m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                        m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                        sc[4 * hc + j] = e8m0_from_f32bits(m);
-                        f[j] = inv_scale_from_e8m0(sc[4 * hc + j]);
-                    }
-                    // codes of the 4 columns, two rows at a time (the words of a row cover its 4 columns)
-                    uint32_t qc[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
-#pragma unroll
-                    for (int rr = 0; rr < 8; rr += 2) {
-                        // rows rr, rr + 1 of the patch: draw rr / 2, words hc (row rr) and 2 + hc (row rr + 1),
-                        // byte j for column 4hc + j
-                        uint32_t wa = 0, wb = 0;
-                        if (sr) {
-                            const uint4 r4 = sr_draw(rp0 + (rr >> 1), cb, (uint64_t)C, p.seed);
-                            wa = hc ? r4.y : r4.x;
-                            wb = hc ? r4.w : r4.z;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            qc[j][rr >> 2] |= code2(y[rr][j] * f[j], y[rr + 1][j] * f[j], wa, j, wb, j) << (8 * (rr & 3));
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint2 q = make_uint2(qc[j][0], qc[j][1]);
-                        if (sc[4 * hc + j] == 0xFFu) {
-                            uint32_t sg[2] = {0u, 0u};
-#pragma unroll
-                            for (int rr = 0; rr < 8; ++rr)
-                                sg[rr >> 2] |= ((__float_as_uint(y[rr][j]) >> 24) & 0x80u) << (8 * (rr & 3));
-                            q.x = 0x7F7F7F7Fu | sg[0];
-                            q.y = 0x7F7F7F7Fu | sg[1];
-                        }
-                        if (cval) *reinterpret_cast<uint2*>(qb + (c8 + 4 * hc + j) * R + row0 + 8 * li) = q;
-                    }
-                }
-                const uint32_t s2c[4] = {sc[0] | (sc[1] << 16), sc[2] | (sc[3] << 16), sc[4] | (sc[5] << 16),
-                                         sc[6] | (sc[7] << 16)};
-                store_col_scales(p.s_col, s2c);
-            }
-            release_stage();
-            continue;
-        }
 
-        // Stochastic rounding: the random bytes of this lane's 8 x 8 patch, drawn once for both copies;
-        // draw d covers its rows 2d, 2d + 1 (words x, y: row 2d, columns 0-3 / 4-7; words z, w: row
-        // 2d + 1).
+        // Stochastic rounding: the random bytes of this lane's 8 x 8 patch, drawn once for both copies.
+        // Element (r, c) takes byte 8 (r mod 2) + (c mod 8) (word k = bytes 4k .. 4k+3, least significant
+        // first) of Philox4x32-10 with key = seed and counter (b mod 2^32, b / 2^32, 0, 0),
+        // b = floor(r / 2) (C / 8) + floor(c / 8): draw d covers the patch's rows 2d, 2d + 1 (words x, y:
+        // row 2d, columns 0-3 / 4-7; words z, w: row 2d + 1).
         uint4 rnd[4];
-        if constexpr (kMode == kModeSR) {
+        if constexpr (kMode == kModeSR || kMode == kModeExtSR) {
             const uint64_t cq = (uint64_t)C >> 3;
             const uint64_t b0 = (uint64_t)((row0 + 8 * li) >> 1) * cq + (uint64_t)(c8 >> 3);
 #pragma unroll
@@ -728,25 +520,8 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
             }
         }
         // the plain MX quantization of one 8 x 8 patch per lane (bf16 pairs v) into one output set
-        auto quant_rowcol = [&](const uint32_t (&v)[8][4], uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
-                                uint8_t* s_col) {
-            // amaxes are taken on the raw bf16 pairs (max of magnitudes; the sign bits they carry are
-            // ignored when the scale byte is read off the exponent field)
-            uint32_t sblk = 0;  // the 32x32 block's scale
-            if constexpr (kB32) {
-                // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1), 4 down (li)
-                uint32_t m = 0;
-#pragma unroll
-                for (int rr = 0; rr < 8; ++rr)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) m = amax_bf16x2(m, v[rr][k]);
-                m = shfl_xor_amax(m, 1);
-                m = shfl_xor_amax(m, 2);
-                m = shfl_xor_amax(m, 8);
-                m = shfl_xor_amax(m, 16);
-                sblk = e8m0_from_absbits(max(m & 0x7FFFu, (m >> 16) & 0x7FFFu));
-            }
-
+        // the row-wise half of it (sblk: the 32x32 block scale when 32x32 blocks are asked for)
+        auto quant_rows = [&](const uint32_t (&v)[8][4], uint32_t sblk, uint8_t* q_row, uint8_t* s_row, bool srq) {
             if constexpr (kRowOut) {
                 // s2[k]: scale bytes of rows 2k (low half) and 2k+1 (high half); 247 marks Inf/NaN
                 uint32_t s2[4];
@@ -774,7 +549,7 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t f2 = inv_scale_pair_bf16(s2[k]);
                     uint2 q[2];
-                    if constexpr (kMode == kModeSR) {
+                    if (kMode == kModeSR || (kMode == kModeExtSR && srq)) {
                         // rows 2k (scale in the low half of f2) and 2k + 1 (high half): draw k
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
@@ -816,7 +591,9 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                     store_row_scales(s_row, __byte_perm(s2[0], s2[1], 0x6420), __byte_perm(s2[2], s2[3], 0x6420));
                 }
             }
-
+        };
+        // the column-wise half of it
+        auto quant_cols = [&](const uint32_t (&v)[8][4], uint32_t sblk, uint8_t* q_col, uint8_t* s_col, bool srq) {
             if constexpr (kCol) {
                 // s2c[k]: scale bytes of this lane's columns 2k (low half) and 2k+1 (high half)
                 uint32_t s2c[4];
@@ -842,7 +619,7 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                 auto col_codes = [&](auto hc, int k, uint32_t f2) -> uint2 {
                     constexpr int h = decltype(hc)::value;
                     uint32_t w[4];
-                    if constexpr (kMode == kModeSR) {
+                    if (kMode == kModeSR || (kMode == kModeExtSR && srq)) {
                         // column j = 2k + h; rows rr, rr + 1 share draw rr / 2 (words j / 4 and 2 + j / 4,
                         // byte j % 4 of each)
                         const uint32_t fs = h ? (f2 & 0xFFFF0000u) | (f2 >> 16) : (f2 & 0xFFFFu) | (f2 << 16);
@@ -893,6 +670,238 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                 store_col_scales(s_col, s2c);
             }
         };
+        auto quant_rowcol = [&](const uint32_t (&v)[8][4], uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                                uint8_t* s_col) {
+            // amaxes are taken on the raw bf16 pairs (max of magnitudes; the sign bits they carry are
+            // ignored when the scale byte is read off the exponent field)
+            uint32_t sblk = 0;  // the 32x32 block's scale
+            if constexpr (kB32) {
+                // one amax over the 32x32 block: 8 rows here, 4 lanes across (lj bits 0-1), 4 down (li)
+                uint32_t m = 0;
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) m = amax_bf16x2(m, v[rr][k]);
+                m = shfl_xor_amax(m, 1);
+                m = shfl_xor_amax(m, 2);
+                m = shfl_xor_amax(m, 8);
+                m = shfl_xor_amax(m, 16);
+                sblk = e8m0_from_absbits(max(m & 0x7FFFu, (m >> 16) & 0x7FFFu));
+            }
+
+            quant_rows(v, sblk, q_row, s_row, kMode == kModeSR);
+            quant_cols(v, sblk, q_col, s_col, kMode == kModeSR);
+        };
+
+        if constexpr (kExt) {
+            // Stability variants: optionally a Hadamard transform of every block of 32 along the copy's
+            // axis, y = c * H * (D x) (signs D, butterflies h = 1, 2, 4 inside the lane, h = 8, 16 across
+            // lanes, in that order, in fp32); codes by round-to-nearest-even or by stochastic rounding
+            // with one random byte per element.  A copy with neither option takes the plain bf16 path.
+            // The fp32 copies take the block's amax before the factor c (the scale byte is read off
+            // fp32(amax * c), which equals the amax of the values fp32(c h): rounding is monotonic) and
+            // multiply each value once by c * 2^(127 - s), which gives fp32(c h) times that power of two
+            // exactly wherever the result is an fp32 normal; below that every code is a signed zero
+            // either way.  Signs are applied to the bf16 patterns; the cross-lane butterflies are one fma
+            // with -1 or 1 (exact in the product, one rounding as the sum or difference).  Rows (row
+            // copy) and columns (column copy) are processed 4 at a time to keep the fp32 values in
+            // registers.
+            constexpr bool sr = kMode == kModeExtSR;
+            const bool had_r = p.opts & MXFP8_OPT_HADAMARD_ROW, had_c = p.opts & MXFP8_OPT_HADAMARD_COL;
+            const uint32_t dsign = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)p.seed,
+                                                 (uint32_t)(p.seed >> 32)).x;
+            // two codes from two scaled fp32 values and (stochastic rounding) their random bytes: byte b0
+            // of word w0, byte b1 of word w1
+            auto code2 = [&](float z0, float z1, uint32_t w0, int b0, uint32_t w1, int b1) -> uint32_t {
+                return sr ? cvt_e4m3x2(sr_pick_value(f32_times_2m120(z0), w0, b0), sr_pick_value(f32_times_2m120(z1), w1, b1))
+                          : cvt_e4m3x2(z0, z1);
+            };
+            // the lane's 8 x 8 bf16 patch from the stage, for the plain path
+            auto load_patch = [&](uint32_t (&v)[8][4]) {
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(src + rr * 256);
+                    v[rr][0] = u.x; v[rr][1] = u.y; v[rr][2] = u.z; v[rr][3] = u.w;
+                }
+            };
+            if constexpr (kRow) {
+                if (!had_r) {
+                    uint32_t v[8][4];
+                    load_patch(v);
+                    quant_rows(v, 0u, p.q_row, p.s_row, sr);
+                } else {
+                    uint32_t s8[8];
+                    uint8_t* qb = p.q_row + b * R * C;
+                    const float cc = had_r ? kRhtScale : 1.0f;
+                    // sign masks of the row transform: columns 2k (bit 15) and 2k + 1 (bit 31) of the lane,
+                    // at block positions 8 (lj mod 4) + 2k, + 1
+                    uint32_t sm[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t d2 = had_r ? dsign >> (8 * (lj & 3) + 2 * k) : 0u;
+                        sm[k] = ((d2 & 1u) << 15) | ((d2 & 2u) << 30);
+                    }
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        float y[4][8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(src + (4 * hr + i) * 256);
+                            const uint32_t w[4] = {u.x ^ sm[0], u.y ^ sm[1], u.z ^ sm[2], u.w ^ sm[3]};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                y[i][2 * k] = bf16lo(w[k]);
+                                y[i][2 * k + 1] = bf16hi(w[k]);
+                            }
+                        }
+                        if (had_r) {
+#pragma unroll
+                            for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c)
+                                        if ((c & h) == 0) {
+                                            const float a = y[i][c], bb = y[i][c + h];
+                                            y[i][c] = a + bb;
+                                            y[i][c + h] = a - bb;
+                                        }
+#pragma unroll
+                            for (int m = 1; m <= 2; m <<= 1) {
+                                const float sg = (lane & m) ? -1.0f : 1.0f;  // upper lane: partner - own
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c)
+                                        y[i][c] = __fmaf_rn(y[i][c], sg, __shfl_xor_sync(0xffffffffu, y[i][c], m));
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t m = 0;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) m = max(m, __float_as_uint(y[i][c]) & 0x7FFFFFFFu);
+                            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                            s8[4 * hr + i] = e8m0_from_f32bits(__float_as_uint(__fmul_rn(__uint_as_float(m), cc)));
+                        }
+                        // rows 4hr .. 4hr+3 of the patch: draws 2hr and 2hr + 1 (rows 2d: words x, y; rows 2d+1: z, w)
+                        const uint4 dr[2] = {rnd[2 * hr], rnd[2 * hr + 1]};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t sc = s8[4 * hr + i];
+                            const int64_t row = row0 + 8 * li + 4 * hr + i;
+                            const float f = __fmul_rn(cc, inv_scale_from_e8m0(sc));
+                            const uint32_t wa = (i & 1) ? dr[i >> 1].z : dr[i >> 1].x;  // columns 0-3
+                            const uint32_t wb = (i & 1) ? dr[i >> 1].w : dr[i >> 1].y;  // columns 4-7
+                            uint2 q;
+                            q.x = code2(y[i][0] * f, y[i][1] * f, wa, 0, wa, 1) | (code2(y[i][2] * f, y[i][3] * f, wa, 2, wa, 3) << 16);
+                            q.y = code2(y[i][4] * f, y[i][5] * f, wb, 0, wb, 1) | (code2(y[i][6] * f, y[i][7] * f, wb, 2, wb, 3) << 16);
+                            if (sc == 0xFFu) {
+                                uint32_t sg[2] = {0u, 0u};
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) sg[c >> 2] |= ((__float_as_uint(y[i][c]) >> 24) & 0x80u) << (8 * (c & 3));
+                                q.x = 0x7F7F7F7Fu | sg[0];
+                                q.y = 0x7F7F7F7Fu | sg[1];
+                            }
+                            if (cval && row < R) *reinterpret_cast<uint2*>(qb + row * C + c8) = q;
+                        }
+                    }
+                    store_row_scales(p.s_row, s8[0] | (s8[1] << 8) | (s8[2] << 16) | (s8[3] << 24),
+                                     s8[4] | (s8[5] << 8) | (s8[6] << 16) | (s8[7] << 24));
+                }
+            }
+            if constexpr (kCol) {
+                if (!had_c) {
+                    uint32_t v[8][4];
+                    load_patch(v);
+                    quant_cols(v, 0u, p.q_col, p.s_col, sr);
+                } else {
+                    uint32_t sc[8];
+                    uint8_t* qb = p.q_col + b * R * C;
+                    const float cc = had_c ? kRhtScale : 1.0f;
+                    const uint32_t dl = had_c ? dsign >> (8 * li) : 0u;  // signs of the lane's rows: block positions 8 li + rr
+#pragma unroll
+                    for (int hc = 0; hc < 2; ++hc) {
+                        float y[8][4];  // columns 4hc .. 4hc+3 of the lane
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr) {
+                            uint2 u = *reinterpret_cast<const uint2*>(src + rr * 256 + 8 * hc);
+                            const uint32_t m = ((dl >> rr) & 1u) * 0x80008000u;
+                            u.x ^= m;
+                            u.y ^= m;
+                            y[rr][0] = bf16lo(u.x);
+                            y[rr][1] = bf16hi(u.x);
+                            y[rr][2] = bf16lo(u.y);
+                            y[rr][3] = bf16hi(u.y);
+                        }
+                        if (had_c) {
+#pragma unroll
+                            for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                                for (int rr = 0; rr < 8; ++rr)
+                                    if ((rr & h) == 0)
+#pragma unroll
+                                        for (int j = 0; j < 4; ++j) {
+                                            const float a = y[rr][j], bb = y[rr + h][j];
+                                            y[rr][j] = a + bb;
+                                            y[rr + h][j] = a - bb;
+                                        }
+#pragma unroll
+                            for (int m = 8; m <= 16; m <<= 1) {
+                                const float sg = (lane & m) ? -1.0f : 1.0f;  // upper lane: partner - own
+#pragma unroll
+                                for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j)
+                                        y[rr][j] = __fmaf_rn(y[rr][j], sg, __shfl_xor_sync(0xffffffffu, y[rr][j], m));
+                            }
+                        }
+                        float f[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t m = 0;
+#pragma unroll
+                            for (int rr = 0; rr < 8; ++rr) m = max(m, __float_as_uint(y[rr][j]) & 0x7FFFFFFFu);
+                            m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                            m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                            sc[4 * hc + j] = e8m0_from_f32bits(__float_as_uint(__fmul_rn(__uint_as_float(m), cc)));
+                            f[j] = __fmul_rn(cc, inv_scale_from_e8m0(sc[4 * hc + j]));
+                        }
+                        // codes of the 4 columns, two rows at a time (the words of a row cover its 4 columns)
+                        uint32_t qc[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+#pragma unroll
+                        for (int rr = 0; rr < 8; rr += 2) {
+                            // rows rr, rr + 1 of the patch: draw rr / 2, words hc (row rr) and 2 + hc (row rr + 1),
+                            // byte j for column 4hc + j
+                            const uint4 r4 = rnd[rr >> 1];
+                            const uint32_t wa = hc ? r4.y : r4.x, wb = hc ? r4.w : r4.z;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                qc[j][rr >> 2] |= code2(y[rr][j] * f[j], y[rr + 1][j] * f[j], wa, j, wb, j) << (8 * (rr & 3));
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint2 q = make_uint2(qc[j][0], qc[j][1]);
+                            if (sc[4 * hc + j] == 0xFFu) {
+                                uint32_t sg[2] = {0u, 0u};
+#pragma unroll
+                                for (int rr = 0; rr < 8; ++rr)
+                                    sg[rr >> 2] |= ((__float_as_uint(y[rr][j]) >> 24) & 0x80u) << (8 * (rr & 3));
+                                q.x = 0x7F7F7F7Fu | sg[0];
+                                q.y = 0x7F7F7F7Fu | sg[1];
+                            }
+                            if (cval) *reinterpret_cast<uint2*>(qb + (c8 + 4 * hc + j) * R + row0 + 8 * li) = q;
+                        }
+                    }
+                    const uint32_t s2c[4] = {sc[0] | (sc[1] << 16), sc[2] | (sc[3] << 16), sc[4] | (sc[5] << 16),
+                                             sc[6] | (sc[7] << 16)};
+                    store_col_scales(p.s_col, s2c);
+                }
+            }
+            release_stage();
+            continue;
+        }
 
         if constexpr (kSwiBwd) {
             // fused SwiGLU backward: dh1 and dh3 of h = silu(h1) * h3 at the rounding points of the
@@ -993,7 +1002,7 @@ static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t
 }
 
 // The stability variants: stochastic rounding alone on the plain kernel's bf16 path; any Hadamard
-// option on the fp32 kernel.
+// option on the fp32 kernel, built apart with and without stochastic rounding.
 static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStream_t st) {
     if (p.ntiles == 0) return MXFP8_OK;
     CUtensorMap m;
@@ -1004,6 +1013,14 @@ static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStre
             case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeSR>(m, p, grid, st);
             case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeSR>(m, p, grid, st);
             case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeSR>(m, p, grid, st);
+            default: return MXFP8_ERR_LAYOUT;
+        }
+    }
+    if (p.opts & MXFP8_OPT_STOCHASTIC) {
+        switch (dirs) {
+            case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeExtSR>(m, p, grid, st);
+            case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeExtSR>(m, p, grid, st);
+            case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeExtSR>(m, p, grid, st);
             default: return MXFP8_ERR_LAYOUT;
         }
     }
