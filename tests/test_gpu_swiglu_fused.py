@@ -14,7 +14,9 @@ Parity bars:
   crosses a rounding midpoint, and a one-ulp change of h moves its E4M3 code by at most one
   step (or its block scale by one).  So every dequantized element must lie within one E4M3
   step of the oracle's, every scale within one of the oracle's, and at least 99% of codes
-  and 99.9% of scales must be identical.
+  and 99.9% of scales must be identical.  The epilogue itself is then checked byte for byte:
+  the oracle's SwiGLU stage and quantizations applied to the kernel's own bf16 h1, h3 must
+  give h_q, h_s, hT_q, hT_s exactly, outside the silu rounding ties above.
 """
 import numpy as np
 import pytest
@@ -83,6 +85,17 @@ def test_fused_gate_up_random_inputs(mx, sizes, H, D):
     assert_gemm_close(f64(h3), o["h3_f64"], what="h3")
     compare_quantized(u8(hq), u8(hs), o["h_q"], o["h_s"], "rows", ends, exact=False, what="h (row-wise)")
     compare_quantized(u8(hTq), u8(hTs), o["hT_q"], o["hT_s"], "cols", ends, exact=False, what="h (token-wise)")
+    # the epilogue alone: the oracle's SwiGLU stage and quantizations applied to the kernel's own bf16
+    # h1, h3 (so the GEMMs' fp32-vs-fp64 rounding no longer enters), byte for byte outside the elements
+    # whose fp64 silu lies near a bf16 rounding midpoint
+    hb = oracle.swiglu_bf16(u16(h1), u16(h3))
+    ties = near_silu_ties(u16(h1))
+    assert ties.mean() < 1e-3
+    q_r, s_r = oracle.quantize_rows(hb)
+    compare_quantized(u8(hq), u8(hs), q_r, s_r, "rows", ends, exact=True, exclude=ties, what="h rows (own h1, h3)")
+    q_c, s_c = oracle.quantize_cols(hb)
+    compare_quantized(u8(hTq), u8(hTs), q_c, s_c, "cols", ends, exact=True, exclude=ties.T,
+                      what="h tokens (own h1, h3)")
 
 
 def exact_inputs(M, D, G, H, seed):
@@ -167,7 +180,8 @@ def test_full_size_sampled(mx):
     """The SwiGLU expert's full gate/up shape (G=2, M=65600 as 39360 + 26240, D=5120, H=8192) in
     the launch configuration the bench times, sampled: row blocks of h (including the first and
     last row of each group) and token blocks of h^T, against the oracle's stage computed from the
-    oracle's own dot products, with the random-input bars above."""
+    oracle's own dot products, with the random-input bars above; and byte for byte against the
+    oracle's SwiGLU stage applied to the kernel's own h1, h3 on blocks without a silu rounding tie."""
     s = synth.workload("swiglu", seed=0, device="cuda")
     x, Wg, Wu, sizes = s["x"], s["Wg"], s["Wu"], s["sizes"]
     M, D, H = s["M"], s["D"], s["H"]
@@ -197,6 +211,16 @@ def test_full_size_sampled(mx):
 
     ref13, got13 = [], []
     q_o, q_g, s_o, s_g = [], [], [], []
+    # the epilogue alone on the kernel's own bf16 h1, h3 of each sampled block (byte for byte on blocks
+    # with no silu rounding tie)
+    q_own, s_own, tie_own = [], [], []
+
+    def own(b1, b3):
+        qo, so = oracle.quantize_vec(oracle.swiglu_bf16(b1, b3))
+        q_own.append(qo)
+        s_own.append(so[0])
+        tie_own.append(near_silu_ties(b1))
+
     rows = np.unique(np.concatenate([rng.integers(0, M, 10), starts, ends - 1]))
     for r in rows:
         r = int(r)
@@ -210,6 +234,7 @@ def test_full_size_sampled(mx):
         q_o.append(qo)
         s_o.append(so[0])
         q_g.append(u8(hq[r, 32 * j:32 * j + 32]))
+        own(u16(h1[r, 32 * j:32 * j + 32]), u16(h3[r, 32 * j:32 * j + 32]))
         pr = int(padded[g]) + r - int(starts[g])
         s_g.append(int(hs[oracle.blocked_offset(pr, j, H // 128)].item()))
     # token blocks of h^T: column c, 32 tokens of one group
@@ -223,6 +248,7 @@ def test_full_size_sampled(mx):
         q_o.append(qo)
         s_o.append(so[0])
         q_g.append(u8(hTq[c, t0:t0 + 32]))
+        own(u16(h1[t0:t0 + 32, c]), u16(h3[t0:t0 + 32, c]))
         cq = int(padded[g]) // 32 + (t0 - int(starts[g])) // 32
         s_g.append(int(hTs[oracle.blocked_offset(c, cq, ct)].item()))
     assert_gemm_close(np.concatenate(got13), np.concatenate(ref13), what="h1/h3 sampled")
@@ -235,3 +261,7 @@ def test_full_size_sampled(mx):
     assert np.all(np.abs(s_g.astype(int) - s_o.astype(int)) <= 1)
     assert np.all(np.abs(dg - do) <= e4m3_step(np.maximum(np.abs(dg), np.abs(do)), smax))
     assert (q_g == q_o).mean() >= 0.99 and (s_g == s_o).mean() >= 0.95
+    clean = ~np.stack(tie_own).any(axis=1)
+    assert clean.mean() > 0.8
+    assert np.array_equal(np.array(s_own)[clean], s_g[clean]), "scales of tie-free blocks (own h1, h3)"
+    assert np.array_equal(np.stack(q_own)[clean], q_g[clean]), "codes of tie-free blocks (own h1, h3)"
