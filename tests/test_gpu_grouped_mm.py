@@ -153,6 +153,53 @@ def test_wgrad_many_groups(mx, G):
     assert_gemm_close(got, ref, what=f"wgrad G={G}")
 
 
+def test_max_groups(mx):
+    """MXFP8_MAX_GROUPS (1024) groups, a quarter of them empty: the group tables of the quantize and
+    GEMM kernels at full capacity.  fwd and dgrad take groups of any size; the wgrad and the
+    column-wise quantization groups of multiples of 32 (the token blocks).  GEMMs within the bound
+    (references by the oracle's matmul forms, pinned to its scalar loops on the CPU), quantization
+    byte for byte in both blocked layouts, empty groups zero dW."""
+    G, N, K = 1024, 32, 256   # K >= 256: the wgrad runs the CTA-pair kernel
+    rng = np.random.default_rng(1024)
+    W = synth.randn_bf16((G, N, K), 0.05, seed=1)
+    sizes = [int(x) for x in rng.integers(1, 48, G)]
+    sizes32 = [32] * G
+    for g in rng.choice(G, G // 4, replace=False):
+        sizes[int(g)] = 0
+        sizes32[int(g)] = 0
+    M, M32 = sum(sizes), sum(sizes32)
+    A = synth.randn_bf16((M, K), 1.0, seed=2)
+    D = synth.randn_bf16((M, N), 1e-2, seed=3)
+    ends_any = sizes_to_ends(sizes)
+    wq, ws = zip(*[oracle.quantize_rows(u16(W[g])) for g in range(G)])
+    wTq, wTs = zip(*[oracle.quantize_cols(u16(W[g])) for g in range(G)])
+    aq, as_ = oracle.quantize_rows(u16(A))
+    dq, ds = oracle.quantize_rows(u16(D))
+    ref_fwd = oracle.grouped_mm_rows_blas(aq, as_, np.stack(wq), np.stack(ws), ends_any)
+    ref_dgrad = oracle.grouped_mm_rows_blas(dq, ds, np.stack(wTq), np.stack(wTs), ends_any)
+    assert_gemm_close(gpu_fwd(mx, A, W, sizes), ref_fwd, what="fwd G=1024")
+    assert_gemm_close(gpu_dgrad(mx, D, W, sizes), ref_dgrad, what="dgrad G=1024")
+    A32 = synth.randn_bf16((M32, K), 1.0, seed=4)
+    D32 = synth.randn_bf16((M32, N), 1e-2, seed=5)
+    got = gpu_wgrad(mx, D32, A32, sizes32)
+    for g, m in enumerate(sizes32):
+        if m == 0:
+            assert np.all(got[g] == 0.0), f"empty group {g} must give zero dW"
+    dTq, dTs = oracle.quantize_cols(u16(D32))
+    aTq, aTs = oracle.quantize_cols(u16(A32))
+    ref_wgrad = oracle.grouped_mm_wgrad_blas(dTq, dTs, aTq, aTs, sizes_to_ends(sizes32))
+    assert_gemm_close(got, ref_wgrad, what="wgrad G=1024")
+    ends = sizes_to_ends(sizes32)
+    q, s, qT, sT = [u8(t) for t in mx.mxfp8_quantize_2d(A32.cuda(), mx.ROW | mx.COL, mx.SCALES_BLOCKED,
+                                                        offs_dev(sizes32))]
+    qo, so = oracle.quantize_rows(u16(A32))
+    qTo, sTo = oracle.quantize_cols(u16(A32))
+    assert np.array_equal(q, qo) and np.array_equal(qT, qTo)
+    n_row, n_col = oracle.blocked_rowgroups_bytes(ends, K // 32), oracle.blocked_colgroups_bytes(K, ends)
+    assert np.array_equal(s[:n_row], oracle.blocked_rowgroups(so, ends))
+    assert np.array_equal(sT[:n_col], oracle.blocked_colgroups(sTo, ends))
+
+
 def test_identity_weights_exact(mx):
     """W[g] = I: every weight scale is 2^-8 and every diagonal code 256, so the
     product is the dequantized activation, exact in fp32; bf16 rounding of that
