@@ -269,8 +269,18 @@ constexpr int kQConsumerThreads = 256;           // 8 consumer warps (the produc
 // kModeSR: stochastic rounding alone, on the bf16 data path.  kModeSwiBwd (ROW|COL only): 256 threads, no TMA ring: each warp loads its
 // patches of dh, h1 and h3 straight from global memory (three inputs a stage would leave room for
 // too few warps to hide the arithmetic's latency), computes dh1 and dh3 and quantizes each both ways.
+// The stochastic-rounding kernels have no producer warp: warp 0's lane 0 issues the ring's loads (the
+// first kQStages tiles up front, then each stage again once all 8 warps are done with it), so that 2
+// CTAs of 8 warps leave each thread 128 registers instead of 96 (their random words spilled at 96).
+// The Hadamard kernel without stochastic rounding fits in 96 and keeps the producer warp: there a
+// refill waits for the slowest warp's whole tile, which costs more than the registers give.
+template <int kMode>
+constexpr bool kFoldedProducer = kMode == kModeSR || kMode == kModeExtSR;
+template <int kMode>
+constexpr int kQThreadsOf = (kMode == kModeSwiBwd || kFoldedProducer<kMode>) ? kQConsumerThreads : kQThreads;
+
 template <unsigned DIRS, int kMode = kModePlain>
-__global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQThreads, 2)
+__global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
     constexpr bool kExt = kMode == kModeExt || kMode == kModeExtSR;
     constexpr bool kSwiBwd = kMode == kModeSwiBwd;
@@ -295,7 +305,8 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
 
     const bool grouped = p.offs != nullptr && p.G > 1;
     if (grouped && p.blocked && threadIdx.x < 32) build_group_table(p.offs, p.G, p.R, ends_s, pstart_s, &ptotal_s);
-    if (threadIdx.x == 256) {
+    constexpr bool kFolded = kFoldedProducer<kMode>;
+    if (threadIdx.x == (kFolded ? 0 : 256)) {
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 8);
@@ -314,6 +325,24 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
     const uint32_t per_b = (uint32_t)(p.tiles_r * p.tiles_c), tiles_c = (uint32_t)p.tiles_c;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the folded producer (warp 0, lane 0): tile t of this CTA into stage `stage`
+    uint32_t issued = 0, issued_phase = 0;  // stages with a load issued, and the phase it completes
+    auto issue_tile = [&](int64_t t, int stage, uint32_t phase) {
+        const uint32_t tt = (uint32_t)t, b = tt / per_b, rem = tt - b * per_b;
+        const uint32_t tr = rem / tiles_c, tc = rem - tr * tiles_c;
+        mbar_arrive_expect_tx(&full[stage], kStageBytes);
+        tma_load_3d(tiles + stage * kStageBytes, &xmap, (int32_t)(tc * 128), (int32_t)(tr * 128), (int32_t)b,
+                    &full[stage]);
+        issued |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+    };
+    if constexpr (kFolded) {
+        if (warp == 0 && lane == 0)
+            for (int s = 0; s < kStages; ++s) {
+                const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
+                if (t < p.ntiles) issue_tile(t, s, 0u);
+            }
+    }
     if (warp == 8) {
         // ------------------------------------------------ TMA producer: whole 128x128 tiles, OOB zero-filled
         if (lane == 0) {
@@ -413,6 +442,7 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
         const uint8_t* src = nullptr;
         uint32_t v[8][4];
         int cur_stage = 0;
+        uint32_t cur_phase = 0;
         if constexpr (!kSwiBwd) {
             if (!mbar_wait_bounded(&full[stage], phase, kQTimeoutNs, abort_flag, p.dev_status)) break;
             src = tiles + stage * kStageBytes + (32 * wi + 8 * li) * 256 + (64 * wj + 8 * lj) * 2;
@@ -424,14 +454,29 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
+                if constexpr (kFolded) {
+                    // refill: once all 8 warps have read this stage, the tile kStages rounds ahead
+                    const int64_t tn = t + (int64_t)kStages * gridDim.x;
+                    if (warp == 0 && lane == 0 && tn < p.ntiles &&
+                        mbar_wait_bounded(&empty[stage], phase, kQTimeoutNs, abort_flag, p.dev_status))
+                        issue_tile(tn, stage, phase ^ 1u);
+                }
             }
             cur_stage = stage;
+            cur_phase = phase;
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        // the stability variants read their values from the stage while they work and free it after
+        // the Hadamard variants read their values from the stage while they work and free it after
+        // (and warp 0 then refills it, once all 8 warps are done with it)
         auto release_stage = [&]() {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[cur_stage]);
+            if constexpr (kFolded) {
+                const int64_t tn = t + (int64_t)kStages * gridDim.x;
+                if (warp == 0 && lane == 0 && tn < p.ntiles &&
+                    mbar_wait_bounded(&empty[cur_stage], cur_phase, kQTimeoutNs, abort_flag, p.dev_status))
+                    issue_tile(tn, cur_stage, cur_phase ^ 1u);
+            }
         };
         if (row0 >= R || col0 >= C) {  // warp-uniform
             if constexpr (kExt) release_stage();
@@ -942,7 +987,17 @@ __global__ void __launch_bounds__(kMode == kModeSwiBwd ? kQConsumerThreads : kQT
             quant_rowcol(v, p.q_row, p.s_row, p.q_col, p.s_col);
         }
     }
-
+    if constexpr (kFolded) {
+        // Warp 0 waited for every tile it issued unless a wait ran out: then let every load this CTA
+        // issued land before its shared memory is released (bounded waits, no abort check).
+        if (warp == 0 && lane == 0 && *abort_flag) {
+            for (int s = 0; s < kStages; ++s)
+                if (issued & (1u << s)) {
+                    volatile int no_abort = 0;
+                    mbar_wait_bounded(&full[s], (issued_phase >> s) & 1u, kQTimeoutNs, &no_abort, nullptr);
+                }
+        }
+    }
 }
 
 __global__ void check_offsets_kernel(const int32_t* offs, int32_t G, int64_t M, int32_t align, int32_t* dev_status) {
@@ -979,7 +1034,7 @@ static mxfp8_status_t launch_dirs(const CUtensorMap& m, const QParams& p, int64_
     static std::atomic<int> attr_set[host::kMaxDevices];
     if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS, kMode>), smem, attr_set))
         return MXFP8_ERR_LAUNCH;
-    quant_tile_kernel<DIRS, kMode><<<(unsigned)grid, direct ? kQConsumerThreads : kQThreads, smem, st>>>(m, p);
+    quant_tile_kernel<DIRS, kMode><<<(unsigned)grid, kQThreadsOf<kMode>, smem, st>>>(m, p);
     return host::last_launch_status();
 }
 
