@@ -262,13 +262,14 @@ constexpr int kQStages = 3;                    // SMEM ring depth (tiles in flig
 constexpr int kQTileBytes = 128 * 128 * 2;     // one 128 x 128 bf16 tile
 constexpr int kQThreads = 288;                 // 8 consumer warps + 1 TMA producer warp
 constexpr int kQSmem = kQStages * kQTileBytes + 128;
-constexpr int kQConsumerThreads = 256;           // 8 consumer warps (the producer warp is the ninth)
+constexpr int kQConsumerThreads = 256;         // 8 consumer warps, no producer warp
 
 // kModeExt / kModeExtSR: the Hadamard variants of ROW / COL / ROW|COL (runtime options p.opts, seed
 // p.seed), without / with stochastic rounding; fp32 working values in the transformed copies.
-// kModeSR: stochastic rounding alone, on the bf16 data path.  kModeSwiBwd (ROW|COL only): 256 threads, no TMA ring: each warp loads its
-// patches of dh, h1 and h3 straight from global memory (three inputs a stage would leave room for
-// too few warps to hide the arithmetic's latency), computes dh1 and dh3 and quantizes each both ways.
+// kModeSR: stochastic rounding alone, on the bf16 data path.
+// kModeSwiBwd (ROW|COL only): 256 threads, no TMA ring: each warp loads its patches of dh, h1 and h3
+// straight from global memory (three inputs a stage would leave room for too few warps to hide the
+// arithmetic's latency), computes dh1 and dh3 and quantizes each both ways.
 // The stochastic-rounding kernels have no producer warp: warp 0's lane 0 issues the ring's loads (the
 // first kQStages tiles up front, then each stage again once all 8 warps are done with it), so that 2
 // CTAs of 8 warps leave each thread 128 registers instead of 96 (their random words spilled at 96).
