@@ -143,6 +143,13 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
+// max(a, b) of non-negative fp32 values, NaN if either is NaN (ordered as the bit patterns are).
+__device__ __forceinline__ float max_nan_f32(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
 // Stochastic rounding on fp32 patterns.  E4M3 steps by 2^-9 below 2^-6 and keeps 3 mantissa bits above
 // it; fp32 steps by 2^-149 below 2^-126 and keeps 23 bits above it.  So the fp32 pattern of
 // z = |y| 2^-120, rounded toward zero, holds in bits 20.. the E4M3 code of |y| truncated (subnormal
@@ -824,12 +831,12 @@ __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
                         }
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            uint32_t m = 0;
+                            float m = 0.0f;
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) m = max(m, __float_as_uint(y[i][c]) & 0x7FFFFFFFu);
-                            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                            s8[4 * hr + i] = e8m0_from_f32bits(__float_as_uint(__fmul_rn(__uint_as_float(m), cc)));
+                            for (int c = 0; c < 8; ++c) m = max_nan_f32(m, fabsf(y[i][c]));
+                            m = max_nan_f32(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                            m = max_nan_f32(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                            s8[4 * hr + i] = e8m0_from_f32bits(__float_as_uint(__fmul_rn(m, cc)));
                         }
                         // rows 4hr .. 4hr+3 of the patch: draws 2hr and 2hr + 1 (rows 2d: words x, y; rows 2d+1: z, w)
                         const uint4 dr[2] = {rnd[2 * hr], rnd[2 * hr + 1]};
@@ -906,12 +913,12 @@ __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
                         float f[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            uint32_t m = 0;
+                            float m = 0.0f;
 #pragma unroll
-                            for (int rr = 0; rr < 8; ++rr) m = max(m, __float_as_uint(y[rr][j]) & 0x7FFFFFFFu);
-                            m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                            m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                            sc[4 * hc + j] = e8m0_from_f32bits(__float_as_uint(__fmul_rn(__uint_as_float(m), cc)));
+                            for (int rr = 0; rr < 8; ++rr) m = max_nan_f32(m, fabsf(y[rr][j]));
+                            m = max_nan_f32(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                            m = max_nan_f32(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                            sc[4 * hc + j] = e8m0_from_f32bits(__float_as_uint(__fmul_rn(m, cc)));
                             f[j] = __fmul_rn(cc, inv_scale_from_e8m0(sc[4 * hc + j]));
                         }
                         // codes of the 4 columns, two rows at a time (the words of a row cover its 4 columns)
