@@ -287,7 +287,9 @@ constexpr bool kFoldedProducer = kMode == kModeSR || kMode == kModeExtSR;
 template <int kMode>
 constexpr int kQThreadsOf = (kMode == kModeSwiBwd || kFoldedProducer<kMode>) ? kQConsumerThreads : kQThreads;
 
-template <unsigned DIRS, int kMode = kModePlain>
+// kHad (the Hadamard kernels only): bit 0 = transform the row-wise copy, bit 1 = the column-wise copy,
+// fixed per instance so that each holds only the paths its options take.
+template <unsigned DIRS, int kMode = kModePlain, unsigned kHad = 0>
 __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap xmap, QParams p) {
     constexpr bool kExt = kMode == kModeExt || kMode == kModeExtSR;
@@ -760,7 +762,7 @@ __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
             // copy) and columns (column copy) are processed 4 at a time to keep the fp32 values in
             // registers.
             constexpr bool sr = kMode == kModeExtSR;
-            const bool had_r = p.opts & MXFP8_OPT_HADAMARD_ROW, had_c = p.opts & MXFP8_OPT_HADAMARD_COL;
+            constexpr bool had_r = (kHad & 1u) != 0, had_c = (kHad & 2u) != 0;
             const uint32_t dsign = philox4x32_10(make_uint4(0u, 0u, 2u, 0u), (uint32_t)p.seed,
                                                  (uint32_t)(p.seed >> 32)).x;
             // two codes from two scaled fp32 values and (stochastic rounding) their random bytes: byte b0
@@ -778,7 +780,7 @@ __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
                 }
             };
             if constexpr (kRow) {
-                if (!had_r) {
+                if constexpr (!had_r) {
                     uint32_t v[8][4];
                     load_patch(v);
                     quant_rows(v, 0u, p.q_row, p.s_row, sr);
@@ -807,7 +809,7 @@ __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
                                 y[i][2 * k + 1] = bf16hi(w[k]);
                             }
                         }
-                        if (had_r) {
+                        if constexpr (had_r) {
 #pragma unroll
                             for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
@@ -865,7 +867,7 @@ __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
                 }
             }
             if constexpr (kCol) {
-                if (!had_c) {
+                if constexpr (!had_c) {
                     uint32_t v[8][4];
                     load_patch(v);
                     quant_cols(v, 0u, p.q_col, p.s_col, sr);
@@ -888,7 +890,7 @@ __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
                             y[rr][2] = bf16lo(u.y);
                             y[rr][3] = bf16hi(u.y);
                         }
-                        if (had_c) {
+                        if constexpr (had_c) {
 #pragma unroll
                             for (int h = 1; h < 8; h <<= 1)
 #pragma unroll
@@ -1035,14 +1037,14 @@ static bool make_x_map(CUtensorMap* m, const QParams& p, const uint16_t* base) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <unsigned DIRS, int kMode = kModePlain>
+template <unsigned DIRS, int kMode = kModePlain, unsigned kHad = 0>
 static mxfp8_status_t launch_dirs(const CUtensorMap& m, const QParams& p, int64_t grid, cudaStream_t st) {
     constexpr bool direct = kMode == kModeSwiBwd;  // no TMA ring: no dynamic shared memory, no producer warp
     constexpr int smem = direct ? 0 : kQSmem;
     static std::atomic<int> attr_set[host::kMaxDevices];
-    if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS, kMode>), smem, attr_set))
+    if (!host::ensure_smem(reinterpret_cast<const void*>(quant_tile_kernel<DIRS, kMode, kHad>), smem, attr_set))
         return MXFP8_ERR_LAUNCH;
-    quant_tile_kernel<DIRS, kMode><<<(unsigned)grid, kQThreadsOf<kMode>, smem, st>>>(m, p);
+    quant_tile_kernel<DIRS, kMode, kHad><<<(unsigned)grid, kQThreadsOf<kMode>, smem, st>>>(m, p);
     return host::last_launch_status();
 }
 
@@ -1066,6 +1068,22 @@ static mxfp8_status_t launch_tiles(unsigned dirs, const QParams& p, cudaStream_t
 
 // The stability variants: stochastic rounding alone on the plain kernel's bf16 path; any Hadamard
 // option on the fp32 kernel, built apart with and without stochastic rounding.
+// The Hadamard kernels, one instance per direction set and transform set (kHad: bit 0 = the row-wise
+// copy, bit 1 = the column-wise copy; the host checks that each transformed copy is asked for).
+template <int kMode>
+static mxfp8_status_t launch_had(unsigned dirs, unsigned had, const CUtensorMap& m, const QParams& p, int64_t grid,
+                                 cudaStream_t st) {
+    constexpr unsigned RC = MXFP8_ROW | MXFP8_COL;
+    switch (dirs | (had << 4)) {
+        case MXFP8_ROW | (1u << 4): return launch_dirs<MXFP8_ROW, kMode, 1>(m, p, grid, st);
+        case MXFP8_COL | (2u << 4): return launch_dirs<MXFP8_COL, kMode, 2>(m, p, grid, st);
+        case RC | (1u << 4): return launch_dirs<RC, kMode, 1>(m, p, grid, st);
+        case RC | (2u << 4): return launch_dirs<RC, kMode, 2>(m, p, grid, st);
+        case RC | (3u << 4): return launch_dirs<RC, kMode, 3>(m, p, grid, st);
+        default: return MXFP8_ERR_LAYOUT;
+    }
+}
+
 static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStream_t st) {
     if (p.ntiles == 0) return MXFP8_OK;
     CUtensorMap m;
@@ -1079,20 +1097,9 @@ static mxfp8_status_t launch_tiles_ext(unsigned dirs, const QParams& p, cudaStre
             default: return MXFP8_ERR_LAYOUT;
         }
     }
-    if (p.opts & MXFP8_OPT_STOCHASTIC) {
-        switch (dirs) {
-            case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeExtSR>(m, p, grid, st);
-            case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeExtSR>(m, p, grid, st);
-            case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeExtSR>(m, p, grid, st);
-            default: return MXFP8_ERR_LAYOUT;
-        }
-    }
-    switch (dirs) {
-        case MXFP8_ROW: return launch_dirs<MXFP8_ROW, kModeExt>(m, p, grid, st);
-        case MXFP8_COL: return launch_dirs<MXFP8_COL, kModeExt>(m, p, grid, st);
-        case MXFP8_ROW | MXFP8_COL: return launch_dirs<MXFP8_ROW | MXFP8_COL, kModeExt>(m, p, grid, st);
-        default: return MXFP8_ERR_LAYOUT;
-    }
+    const unsigned had = ((p.opts & MXFP8_OPT_HADAMARD_ROW) ? 1u : 0u) | ((p.opts & MXFP8_OPT_HADAMARD_COL) ? 2u : 0u);
+    return (p.opts & MXFP8_OPT_STOCHASTIC) ? launch_had<kModeExtSR>(dirs, had, m, p, grid, st)
+                                           : launch_had<kModeExt>(dirs, had, m, p, grid, st);
 }
 
 // The fused SwiGLU backward: p.x = dh, p.x2 = h1, p.x3 = h3 (direct loads; the tensor map is unused).
