@@ -878,6 +878,38 @@ def cpu_baseline(s_cpu: dict) -> dict:
 
 
 # ---------------------------------------------------------------- end to end through host buffers
+def host_link(device, nbytes: int = 256 << 20, reps: int = 4) -> dict:
+    """Pinned-host <-> device copy rates of this box's link (GB/s): each direction alone, then both
+    directions at once on two streams; the e2e step's copies cannot run faster than these."""
+    h_src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_dst = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def timed(h2d: bool, d2h: bool) -> float:
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        s_out.wait_event(e0)
+        for _ in range(reps):
+            if h2d:
+                with torch.cuda.stream(s_in):
+                    d_a.copy_(h_src, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s_out):
+                    h_dst.copy_(d_b, non_blocking=True)
+        s_in.wait_stream(s_out)
+        e1.record(s_in)
+        torch.cuda.synchronize()
+        return reps * nbytes / (e0.elapsed_time(e1) * 1e6)
+
+    timed(True, True)  # first touch of the pinned pages
+    both = timed(True, True)
+    return {"h2d_gbs": round(timed(True, False), 1), "d2h_gbs": round(timed(False, True), 1),
+            "both_gbs_each": round(both, 1), "bytes_per_copy": nbytes}
+
+
 def run_e2e(make_step, step, stream, world, device, n_steps: int):
     """The step with its inputs copied in from pinned host memory and its outputs copied out, as a
     3-stream pipeline over two device buffer sets: the copy-in of step i+1 and the copy-out of step
@@ -923,9 +955,13 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
     xms = max_over_ranks(x0.elapsed_time(x1) / n_steps, world, device)
     bi = sum(t.numel() * t.element_size() for t in h_in)
     bo = sum(t.numel() * t.element_size() for t in h_out[0])
+    link = host_link(device)
+    # with both directions busy, each step's copies need at least this long on this machine's link
+    link["copy_ms_per_step"] = round(max(bi, bo) / (link["both_gbs_each"] * 1e6), 3)
     return {"value": round(world * step.flops / xms / 1e9, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_steps,
-            "pipeline": "copy-in, kernels and copy-out on 3 streams over 2 device buffer sets"}
+            "pipeline": "copy-in, kernels and copy-out on 3 streams over 2 device buffer sets",
+            "host_link": link}
 
 
 # ---------------------------------------------------------------- native (GPU) arm
