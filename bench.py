@@ -918,10 +918,11 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
     h_in = [t.cpu().pin_memory() for t in step.inputs()]
     h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in st.outputs()] for st in sets]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    mk = lambda: torch.cuda.Event(enable_timing=False)
+    mk = lambda: torch.cuda.Event(enable_timing=True)
     h2d_done = [mk() for _ in range(n_steps)]
     comp_done = [mk() for _ in range(n_steps)]
     d2h_done = [mk() for _ in range(n_steps)]
+    in_start, comp_start, out_start = ([mk() for _ in range(n_steps)] for _ in range(3))
     for st in sets:
         st.run(stream)  # warm both buffer sets once
     torch.cuda.synchronize()
@@ -934,16 +935,19 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(comp_done[i - 2])       # inputs of set i%2 no longer read
+            in_start[i].record(s_in)
             for d, h in zip(st.inputs(), h_in):
                 d.copy_(h, non_blocking=True)
             h2d_done[i].record(s_in)
         stream.wait_event(h2d_done[i])
         if i >= 2:
             stream.wait_event(d2h_done[i - 2])           # outputs of set i%2 already copied out
+        comp_start[i].record(stream)
         st.run(stream)
         comp_done[i].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[i])
+            out_start[i].record(s_out)
             for h, d in zip(h_out[i % 2], st.outputs()):
                 h.copy_(d, non_blocking=True)
             d2h_done[i].record(s_out)
@@ -955,13 +959,36 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
     xms = max_over_ranks(x0.elapsed_time(x1) / n_steps, world, device)
     bi = sum(t.numel() * t.element_size() for t in h_in)
     bo = sum(t.numel() * t.element_size() for t in h_out[0])
+
+    # each leg of the pipeline alone, on the step's own buffers
+    def alone(fn, s) -> float:
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        with torch.cuda.stream(s):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    legs = {"copy_in_ms": alone(lambda: [d.copy_(h, non_blocking=True) for d, h in zip(step.inputs(), h_in)], s_in),
+            "kernels_ms": alone(lambda: step.run(stream), stream),
+            "copy_out_ms": alone(lambda: [h.copy_(d, non_blocking=True) for h, d in zip(h_out[0], step.outputs())],
+                                 s_out)}
+    # the same legs inside the pipeline (median over the steps)
+    med = lambda a, b: float(np.median([a[i].elapsed_time(b[i]) for i in range(n_steps)]))
+    legs.update(piped_copy_in_ms=med(in_start, h2d_done), piped_kernels_ms=med(comp_start, comp_done),
+                piped_copy_out_ms=med(out_start, d2h_done))
+    legs = {k: round(v, 3) for k, v in legs.items()}
+    legs["copy_in_gbs"] = round(bi / (legs["copy_in_ms"] * 1e6), 1)
+    legs["copy_out_gbs"] = round(bo / (legs["copy_out_ms"] * 1e6), 1)
     link = host_link(device)
     # with both directions busy, each step's copies need at least this long on this machine's link
     link["copy_ms_per_step"] = round(max(bi, bo) / (link["both_gbs_each"] * 1e6), 3)
     return {"value": round(world * step.flops / xms / 1e9, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_steps,
             "pipeline": "copy-in, kernels and copy-out on 3 streams over 2 device buffer sets",
-            "host_link": link}
+            "alone": legs, "host_link": link}
 
 
 # ---------------------------------------------------------------- native (GPU) arm
