@@ -73,7 +73,7 @@ CONFIG_NAMES = {"tiny": "C1", "scout": "C2", "swiglu": "C3", "imbalanced": "C4"}
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernel of the
 # SwiGLU step, from a one-pass ncu capture of this command, valid only while the GEMM sources hash
 # to the recorded value (the kernel is then unchanged since the counters were taken).
-DOMINANT_TRAFFIC = {"kernel": "grouped_mm_pair_kernel", "bytes_per_launch": 3676352853, "src_sha": "75a542477b060c39"}
+DOMINANT_TRAFFIC = {"kernel": "grouped_mm_pair_kernel", "bytes_per_launch": 3042455962, "src_sha": "c93a6068c3a2f650"}
 
 
 def kernel_src_sha() -> str:
@@ -257,6 +257,11 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def gemm_kernel_of(out_width: int) -> str:
+    """The library's kernel for a plain fwd / dgrad / wgrad whose output is out_width columns wide."""
+    return "grouped_mm_pair_kernel" if out_width >= 256 else "grouped_mm_kernel<128>"
+
+
 def _blocked_expert_bytes(rows, cols):
     return ((rows + 127) // 128) * 128 * ((cols + 127) // 128) * 4
 
@@ -349,8 +354,8 @@ class Step(_CallList):
         self.bytes = {"quant_A": qb(M * K), "quant_W": qb(G * N * K), "quant_dOut": qb(M * N)}
         quant = "quant_tile_kernel<ROW|COL" + (", ext>" if stability else ">")
         self.kernel_of = {"quant_A": quant, "quant_W": "quant_tile_kernel<ROW|COL" + ("|32x32>" if w_block32 else ">"),
-                          "quant_dOut": quant, "fwd": "grouped_mm_kernel<256>", "dgrad": "grouped_mm_kernel<256>",
-                          "wgrad": "grouped_mm_pair_kernel" if K >= 256 else "grouped_mm_kernel<256>"}
+                          "quant_dOut": quant, "fwd": gemm_kernel_of(N), "dgrad": gemm_kernel_of(K),
+                          "wgrad": gemm_kernel_of(K)}
 
     def inputs(self):
         return [self.A, self.W, self.D, self.offs]
@@ -519,13 +524,13 @@ class SwiGLUStep(_CallList):
             if n.startswith("torch."):
                 ko[n] = n
             elif n.startswith("wgrad_"):
-                ko[n] = "grouped_mm_pair_kernel"
+                ko[n] = gemm_kernel_of(D if n in ("wgrad_gate", "wgrad_up") else H)
             elif n == "gateup_swiglu":
                 ko[n] = "grouped_mm_kernel<256, swiglu epilogue>"
             elif n == "dgrad_gate_up":
                 ko[n] = "grouped_mm_kernel<256, two-operand dgrad>"
             elif n.startswith(("fwd_", "dgrad_")):
-                ko[n] = "grouped_mm_kernel<256>"
+                ko[n] = gemm_kernel_of(D if n in ("fwd_down", "dgrad_gate", "dgrad_up") else H)
             elif n == "swiglu_bwd_quant":
                 ko[n] = "quant_tile_kernel<ROW|COL, swiglu backward>"
             else:
@@ -930,6 +935,7 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
         torch.distributed.barrier()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x0.record(s_in)
+    host0 = time.perf_counter()
     for i in range(n_steps):
         st = sets[i % 2]
         with torch.cuda.stream(s_in):
@@ -953,6 +959,7 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
             d2h_done[i].record(s_out)
     s_out.wait_event(d2h_done[n_steps - 1])
     x1.record(s_out)
+    host_ms = (time.perf_counter() - host0) * 1e3 / n_steps  # the host's enqueue time per step
     torch.cuda.synchronize()
     for st in sets:
         st.check_status()
@@ -988,7 +995,7 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
     return {"value": round(world * step.flops / xms / 1e9, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_steps,
             "pipeline": "copy-in, kernels and copy-out on 3 streams over 2 device buffer sets",
-            "alone": legs, "host_link": link}
+            "alone": legs, "host_enqueue_ms_per_step": round(host_ms, 3), "host_link": link}
 
 
 # ---------------------------------------------------------------- native (GPU) arm

@@ -23,13 +23,15 @@
 // Kernel structure (one CTA per SM, persistent over a static tile order):
 //   warp 0      TMA producer: 128B-swizzled A/B tiles (128 x 128 B and BN x 128 B)
 //               and the matching 512-byte scale tiles into a ring of SMEM stages.
-//   warp 1      MMA issuer: tcgen05.cp copies the scale tiles into tensor memory,
-//               then four tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each,
+//   warp 1      MMA issuer: four tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each,
 //               scale byte k of the 32-bit TMEM scale word) per stage into an fp32
 //               accumulator in tensor memory; tcgen05.commit frees stages.
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator (each warp its 32-lane
 //               quarter), fp32 -> bf16 round-to-nearest-even, masked 16-byte
 //               stores of the rows and columns that belong to the tile's group.
+//   warp 6      scale copies: as soon as a stage lands, tcgen05.cp moves its scale
+//               tiles into that stage's tensor-memory columns and signals the MMA
+//               issuer; off the issuer's thread, the copies do not hold its MMAs back.
 // Every mbarrier wait is bounded (MXFP8_ERR_TIMEOUT + orderly exit).
 
 #include "common.cuh"
@@ -39,11 +41,14 @@ namespace mx {
 
 constexpr int BM = 128;  // tile rows = tensor-memory lanes
 constexpr int BK = 128;  // contraction bytes (= e4m3 elements) per stage: one 128-byte swizzle row
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // producer, MMA issuer, 4 epilogue warps, scale-copy warp
 // SwiGLU variant: 16 epilogue warps (4 per tensor-memory lane quarter, one 32-column block each):
 // its per-element work (silu, two quantizations) needs the extra warps to keep pace with the MMAs.
 constexpr int kSwiEpiWarps = 16;
-constexpr int kThreadsSwi = 64 + 32 * kSwiEpiWarps;
+constexpr int kThreadsSwi = 96 + 32 * kSwiEpiWarps;
+// the warp that copies each stage's scale tiles into tensor memory: the one after the epilogue warps
+template <bool kSwi>
+constexpr int kSfWarpOf = kSwi ? 2 + kSwiEpiWarps : 6;
 constexpr int kBand = 16;  // m-tiles per raster band (tiles of a band share B tiles in L2)
 
 enum GemmMode : int { ROWGROUPED = 0, KGROUPED = 1 };
@@ -67,7 +72,7 @@ struct Cfg {
     static constexpr int kOffStage = kOffSfb + kStages * kSfbBytes;  // epilogue staging: 4 warps x 32 rows x 128 B
     static constexpr int kStageBytes = 4 * 32 * 128;
     static constexpr int kOffBar = kOffStage + kStageBytes;
-    static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
+    static constexpr int kBarBytes = (3 * kStages + 2 * kAcc + 2) * 8 + 16;
     static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
 };
 
@@ -238,6 +243,8 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
     uint64_t* tfull = empty + C::kStages;
     uint64_t* tempty = tfull + C::kAcc;
     uint64_t* drain = tempty + C::kAcc;
+    uint64_t* sfull = drain + 1;             // a stage's scale tiles are in tensor memory
+    uint64_t* sfdrain = sfull + C::kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -299,6 +306,8 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                 mbar_init(&tempty[a], kSwi ? kSwiEpiWarps : 4);
             }
             mbar_init(drain, 1);
+            for (int s = 0; s < C::kStages; ++s) mbar_init(&sfull[s], 1);
+            mbar_init(sfdrain, 1);
             fence_barrier_init();
         }
         __syncwarp();
@@ -381,24 +390,17 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + acc * BN;
-                // scale tiles of stage st: SMEM -> the stage's own tensor-memory columns
-                auto copy_scales = [&](int st) {
-                    const uint32_t sfa_t = tmem + C::kSfCol0 + st * C::kSfCols;
-                    const uint32_t sfa_s = smem_u32(smem + C::kOffSfa + st * C::kSfaBytes);
-                    const uint32_t sfb_s = smem_u32(smem + C::kOffSfb + st * C::kSfbBytes);
-                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sfa_s, 0, 128, 0));
-#pragma unroll
-                    for (int j = 0; j < BN / 128; ++j)
-                        tc_cp_32x128b_warpx4(sfa_t + 4 + 4 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
-                };
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     const int cur = stage;
                     if (!mbar_wait_bounded(&full[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
+                    if (!mbar_wait_bounded(&sfull[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    copy_scales(cur);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                     const uint32_t sfa_t = tmem + C::kSfCol0 + cur * C::kSfCols;
                     const uint32_t sfb_t = sfa_t + 4;
@@ -431,6 +433,40 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             tc_commit(drain);
             volatile int no_abort = 0;
             mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
+        } else if (warp == kSfWarpOf<kSwi>) {
+            // ------------------------------------------------ scale copies
+            // As soon as a stage lands, its scale tiles go to that stage's tensor-memory columns
+            // (tcgen05.cp, SMEM -> TMEM) and the copy's completion is signalled on sfull; the MMA
+            // thread waits for it before the stage's MMAs.  A stage's columns are rewritten only
+            // after the stage was refilled, i.e. after the MMAs that read them completed.
+            if (lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                    const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
+                    for (int kt = 0; kt < ti.k_tiles; ++kt) {
+                        if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sfa_t = tmem + C::kSfCol0 + stage * C::kSfCols;
+                        const uint32_t sfa_s = smem_u32(smem + C::kOffSfa + stage * C::kSfaBytes);
+                        const uint32_t sfb_s = smem_u32(smem + C::kOffSfb + stage * C::kSfbBytes);
+                        tc_cp_32x128b_warpx4(sfa_t, smem_desc(sfa_s, 0, 128, 0));
+#pragma unroll
+                        for (int j = 0; j < BN / 128; ++j)
+                            tc_cp_32x128b_warpx4(sfa_t + 4 + 4 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
+                        tc_commit(&sfull[stage]);
+                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    }
+                }
+                // this thread's copies complete before the columns are freed
+                tc_commit(sfdrain);
+                volatile int no_abort = 0;
+                mbar_wait_bounded(sfdrain, 0, p.timeout_ns, &no_abort, p.dev_status);
+            }
         } else if (warp >= 2) {
           if constexpr (kSwi) {
             // ------------------------------------------------ SwiGLU epilogue
@@ -643,8 +679,9 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
 // memory and writes rows 0-127 to its own tensor memory, rows 128-255 to the odd CTA's.
 // Every copy of the pair completes on the even CTA's stage barrier (TMA cta_group::2 form),
 // so the scale tiles are moved by TMA as well (tensor maps over the scale buffers, 512-byte
-// boxes).  Stage and accumulator release are multicast commits to both CTAs; the odd CTA's
-// epilogue reports a drained accumulator to the even CTA with a remote mbarrier arrive.
+// boxes); the even CTA's scale-copy warp moves them into both CTAs' tensor memory.  Stage and
+// accumulator release are multicast commits to both CTAs; the odd CTA's epilogue reports a
+// drained accumulator to the even CTA with a remote mbarrier arrive.
 // ============================================================================================
 constexpr int kPairStages = 5;
 constexpr int kSortGroups = 128;  // K-grouped schedules rank at most this many groups (O(G^2) per CTA)
@@ -652,7 +689,8 @@ constexpr int kSortGroups = 128;  // K-grouped schedules rank at most this many 
 // half of the accumulator, so the single accumulator is handed back to the MMA warp in half the time
 // (a K-grouped tile of a small group contracts over few k-tiles, and the drain is per tile).
 constexpr int kPairEpiWarps = 8;
-constexpr int kThreadsPair = 64 + 32 * kPairEpiWarps;
+constexpr int kPairSfWarp = 2 + kPairEpiWarps;  // the scale-copy warp
+constexpr int kThreadsPair = 96 + 32 * kPairEpiWarps;
 // K-grouped pair tiles run in bands of 8 row-tiles: the 76 tiles of a wave then share about
 // 8 A and 10 B operand slabs instead of 16 and 5 (a long group's slabs do not fit in L2 together).
 constexpr int kBandPairK = 8;
@@ -675,7 +713,7 @@ struct CfgPair {
     static constexpr int kOffStage = kOffSfb + kStages * kSfbBytes;
     static constexpr int kStageBytes = kPairEpiWarps * 32 * 128;
     static constexpr int kOffBar = kOffStage + kStageBytes;
-    static constexpr int kBarBytes = (2 * kStages + 2 + 1) * 8 + 16;
+    static constexpr int kBarBytes = (3 * kStages + 2 + 2) * 8 + 16;
     static constexpr int kSmem = kOffBar + kBarBytes + 1024;
 };
 
@@ -778,6 +816,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     uint64_t* tfull = empty + C::kStages;
     uint64_t* tempty = tfull + 1;
     uint64_t* drain = tempty + 1;
+    uint64_t* sfull = drain + 1;             // a stage's scale tiles are in tensor memory (even CTA)
+    uint64_t* sfdrain = sfull + C::kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
@@ -845,6 +885,8 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             mbar_init(tfull, 1);
             mbar_init(tempty, 2 * kPairEpiWarps);  // every epilogue warp of both CTAs of the pair
             mbar_init(drain, 1);
+            for (int s = 0; s < C::kStages; ++s) mbar_init(&sfull[s], 1);
+            mbar_init(sfdrain, 1);
             fence_barrier_init();
         }
         __syncwarp();
@@ -939,15 +981,14 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                         ok = false;
                         break;
                     }
+                    if (!mbar_wait_bounded(&sfull[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                     const uint32_t sfa_t = tmem + C::kSfCol0 + cur * C::kSfCols;
                     const uint32_t sfb_t = sfa_t + 4;
-                    tc_cp_pair_32x128b_warpx4(sfa_t, smem_desc(smem_u32(smem + C::kOffSfa + cur * C::kSfaBytes), 0, 128, 0));
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        tc_cp_pair_32x128b_warpx4(
-                            sfb_t + 4 * j, smem_desc(smem_u32(smem + C::kOffSfb + cur * C::kSfbBytes + 512 * j), 0, 128, 0));
                     const uint32_t a_s = smem_u32(smem + cur * C::kABytes);
                     const uint32_t b_s = smem_u32(smem + C::kOffB + cur * C::kBBytes);
                     if (kt + 1 < ti.k_tiles || ti.kb_last == BK / 32) {
@@ -978,6 +1019,39 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             tc_commit_pair(drain, 0x1);
             volatile int no_abort = 0;
             mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
+        } else if (warp == kPairSfWarp) {
+            // ------------------------------------------------ scale copies (even CTA only)
+            // Each landed stage's scale tiles go to its tensor-memory columns in both CTAs (the
+            // cta_group::2 copy), signalled on the even CTA's sfull; the MMA thread waits for it.
+            if (lane == 0 && leader) {
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                for (int64_t j = 0; j * ncl < ntiles && ok; ++j) {
+                    const int64_t t = tile_at(j);
+                    if (t >= ntiles) continue;
+                    const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                    for (int kt = 0; kt < ti.k_tiles; ++kt) {
+                        if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sfa_t = tmem + C::kSfCol0 + stage * C::kSfCols;
+                        tc_cp_pair_32x128b_warpx4(sfa_t, smem_desc(smem_u32(smem + C::kOffSfa + stage * C::kSfaBytes), 0, 128, 0));
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj)
+                            tc_cp_pair_32x128b_warpx4(
+                                sfa_t + 4 + 4 * jj,
+                                smem_desc(smem_u32(smem + C::kOffSfb + stage * C::kSfbBytes + 512 * jj), 0, 128, 0));
+                        tc_commit_pair(&sfull[stage], 0x1);
+                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    }
+                }
+                tc_commit_pair(sfdrain, 0x1);
+                volatile int no_abort = 0;
+                mbar_wait_bounded(sfdrain, 0, p.timeout_ns, &no_abort, p.dev_status);
+            }
         } else if (warp >= 2) {
             // ------------------------------------------------ epilogue (both CTAs: own 128 rows)
             // Warp w drains lane quarter w % 4 (the quarter its tensor-memory access is bound to) and
@@ -1090,12 +1164,12 @@ static mxfp8_status_t launch_gemm(const void* a, int64_t a_rows, int64_t a_cols,
 
 static uint64_t default_timeout_ns() { return 2000000000ull; }
 
-// Kernel choice (measured on the 8-expert Scout-like workload, TFLOP/s single / pair):
-// fwd 2890 / 2780, dgrad 2890 / 2890, wgrad 2468 / 2540.  The pair kernel pads ragged token
-// groups to 256 rows (vs 128), which costs the forward more than its smaller stages save; the
-// wgrad's groups own whole output matrices, so it takes the pair kernel.
-constexpr bool kPairForRowGrouped = false;
-constexpr bool kPairForKGrouped = true;
+// Kernel choice: the CTA-pair kernel wherever the output is at least 256 wide (fwd, dgrad and
+// wgrad alike); the single-CTA kernel for narrower outputs and for the SwiGLU and two-operand
+// variants.  Measured with the scale copies on their own warp (TFLOP/s, single-CTA with 256-wide
+// tiles / pair): forward of the 8-expert Scout-like workload 2533 / 2782, of the 2-expert SwiGLU
+// shapes 2694 / 3070 (N=16384, K=5120) and 2725 / 3057 (N=5120, K=8192).  Padding ragged token
+// groups to 256 rows instead of 128 costs less than the pair's halved B traffic per CTA saves.
 
 // A scale buffer as [bytes/256][256] uint8, 2 x 256 B boxes (= one 512-byte scale tile).
 static bool make_scale_map(CUtensorMap* m, const void* base, int64_t bytes) {
@@ -1200,15 +1274,11 @@ static mxfp8_status_t rowgrouped(const void* tok_q, const void* tok_s, const voi
         const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 127) / 128);
         return launch_gemm<128, false, true>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st, ex2_q, tok2_q);
     }
-    if (Nb >= 256 && kPairForRowGrouped) {
+    if (Nb >= 256) {
         const int64_t bound = ((M + 255) / 256 + G) * ((Nb + 255) / 256);
         const int64_t sfa_bytes = ((M + 127) / 128 + G) * 128 * p.sfa_ct * 4;
         return launch_pair(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, sfa_bytes, (int64_t)G * p.sfb_estride, p, bound,
                            st);
-    }
-    if (Nb >= 256) {
-        const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 255) / 256);
-        return launch_gemm<256>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st);
     }
     const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 127) / 128);
     return launch_gemm<128>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st);
@@ -1263,15 +1333,11 @@ extern "C" mxfp8_status_t mxfp8_grouped_mm_wgrad(const void* doutT_q, const void
     p.need32 = 1;
     p.dev_status = dev_status;
     p.timeout_ns = default_timeout_ns();
-    if (K >= 256 && kPairForKGrouped) {
+    if (K >= 256) {
         const int64_t bound = (int64_t)G * ((N + 255) / 256) * ((K + 255) / 256);
         const int64_t tiles_m = (M + 127) / 128 + G;
         return launch_pair(doutT_q, N, M, aT_q, K, M, ((N + 127) / 128) * 128 * tiles_m * 4,
                            ((K + 127) / 128) * 128 * tiles_m * 4, p, bound, st);
-    }
-    if (K >= 256) {
-        const int64_t bound = (int64_t)G * ((N + BM - 1) / BM) * ((K + 255) / 256);
-        return launch_gemm<256>(doutT_q, N, M, aT_q, K, M, p, bound, st);
     }
     const int64_t bound = (int64_t)G * ((N + BM - 1) / BM) * ((K + 127) / 128);
     return launch_gemm<128>(doutT_q, N, M, aT_q, K, M, p, bound, st);

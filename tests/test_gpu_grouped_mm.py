@@ -200,6 +200,30 @@ def test_max_groups(mx):
     assert np.array_equal(sT[:n_col], oracle.blocked_colgroups(sTo, ends))
 
 
+def test_max_groups_pair_rowgrouped(mx):
+    """1024 ragged groups (a quarter empty) through the CTA-pair fwd and dgrad: N = 288 is one
+    256-wide pair tile plus a 32-column tail whose B rows past N read TMA's zero fill; K = 160
+    ends in a partial k-tile."""
+    G, N, K = 1024, 288, 160
+    rng = np.random.default_rng(2048)
+    sizes = [int(x) for x in rng.integers(1, 40, G)]
+    for g in rng.choice(G, G // 4, replace=False):
+        sizes[int(g)] = 0
+    M = sum(sizes)
+    W = synth.randn_bf16((G, N, K), 0.05, seed=7)
+    A = synth.randn_bf16((M, K), 1.0, seed=8)
+    D = synth.randn_bf16((M, N), 1e-2, seed=9)
+    ends = sizes_to_ends(sizes)
+    wq, ws = zip(*[oracle.quantize_rows(u16(W[g])) for g in range(G)])
+    wTq, wTs = zip(*[oracle.quantize_cols(u16(W[g])) for g in range(G)])
+    aq, as_ = oracle.quantize_rows(u16(A))
+    dq, ds = oracle.quantize_rows(u16(D))
+    assert_gemm_close(gpu_fwd(mx, A, W, sizes), oracle.grouped_mm_rows_blas(aq, as_, np.stack(wq), np.stack(ws), ends),
+                      what="pair fwd G=1024")
+    assert_gemm_close(gpu_dgrad(mx, D, W, sizes),
+                      oracle.grouped_mm_rows_blas(dq, ds, np.stack(wTq), np.stack(wTs), ends), what="pair dgrad G=1024")
+
+
 def test_identity_weights_exact(mx):
     """W[g] = I: every weight scale is 2^-8 and every diagonal code 256, so the
     product is the dequantized activation, exact in fp32; bf16 rounding of that
