@@ -73,7 +73,7 @@ CONFIG_NAMES = {"tiny": "C1", "scout": "C2", "swiglu": "C3", "imbalanced": "C4"}
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernel of the
 # SwiGLU step, from a one-pass ncu capture of this command, valid only while the GEMM sources hash
 # to the recorded value (the kernel is then unchanged since the counters were taken).
-DOMINANT_TRAFFIC = {"kernel": "grouped_mm_pair_kernel", "bytes_per_launch": 3042455962, "src_sha": "c93a6068c3a2f650"}
+DOMINANT_TRAFFIC = {"kernel": "grouped_mm_pair_kernel", "bytes_per_launch": 3032201472, "src_sha": "f81fd28862cb108c"}
 
 
 def kernel_src_sha() -> str:
@@ -528,7 +528,8 @@ class SwiGLUStep(_CallList):
             elif n == "gateup_swiglu":
                 ko[n] = "grouped_mm_kernel<256, swiglu epilogue>"
             elif n == "dgrad_gate_up":
-                ko[n] = "grouped_mm_kernel<256, two-operand dgrad>"
+                ko[n] = ("grouped_mm_pair_kernel<two-operand dgrad>" if D >= 256
+                         else "grouped_mm_kernel<128, two-operand dgrad>")
             elif n.startswith(("fwd_", "dgrad_")):
                 ko[n] = gemm_kernel_of(D if n in ("fwd_down", "dgrad_gate", "dgrad_up") else H)
             elif n == "swiglu_bwd_quant":
@@ -987,6 +988,11 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
     legs.update(piped_copy_in_ms=med(in_start, h2d_done), piped_kernels_ms=med(comp_start, comp_done),
                 piped_copy_out_ms=med(out_start, d2h_done))
     legs = {k: round(v, 3) for k, v in legs.items()}
+    # when each leg of the first steps started and ended (ms after the pipeline's first event)
+    at = lambda e: round(x0.elapsed_time(e), 2)
+    timeline = [{"in": [at(in_start[i]), at(h2d_done[i])],
+                 "kernels": [at(comp_start[i]), at(comp_done[i])], "out": [at(out_start[i]), at(d2h_done[i])]}
+                for i in range(min(n_steps, 4))]
     legs["copy_in_gbs"] = round(bi / (legs["copy_in_ms"] * 1e6), 1)
     legs["copy_out_gbs"] = round(bo / (legs["copy_out_ms"] * 1e6), 1)
     link = host_link(device)
@@ -995,7 +1001,7 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
     return {"value": round(world * step.flops / xms / 1e9, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_steps,
             "pipeline": "copy-in, kernels and copy-out on 3 streams over 2 device buffer sets",
-            "alone": legs, "host_enqueue_ms_per_step": round(host_ms, 3), "host_link": link}
+            "alone": legs, "timeline_ms": timeline, "host_enqueue_ms_per_step": round(host_ms, 3), "host_link": link}
 
 
 # ---------------------------------------------------------------- native (GPU) arm

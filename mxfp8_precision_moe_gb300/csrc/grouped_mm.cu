@@ -730,6 +730,7 @@ struct PairTile {
 
 // Tile t of the pair schedule, seen from CTA `half` (0: rows 0-127 of the pair tile, 1: 128-255).
 // K-grouped: tile t belongs to the group at position t / per_g of gorder_s (or of the natural order).
+template <bool kDualK = false>
 __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, int half, const int32_t* ends_s,
                                               const int32_t* pstart_s, const int32_t* tstart_s, int64_t ptotal,
                                               const int32_t* gorder_s, bool sorted) {
@@ -753,7 +754,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
         ti.a_row = start + rows0;
         ti.b_row = (int64_t)g * p.nb + n * BN + half * 128;
         ti.a_x0 = 0;
-        ti.k_tiles = (int)((p.kc + BK - 1) / BK);
+        ti.k_tiles = (int)((p.kc + BK - 1) / BK) * (kDualK ? 2 : 1);
         ti.kb_last = BK / 32;
         const int64_t cA = min64(2 * m2 + half, (size + 127) / 128 - 1);  // clamp: rows past the group are masked
         ti.sfa_chunk = (pstart_s[g] / 128 + cA) * p.sfa_ct;
@@ -794,9 +795,14 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
     return ti;
 }
 
+// kDualK (row-grouped only): the contraction runs over two operand sets one after the other, k-tiles
+// 0 .. k/2-1 over (A, B) and k/2 .. k-1 over (A2, B2), into one accumulator.
+template <bool kDualK>
 __global__ void __launch_bounds__(kThreadsPair, 1)
     grouped_mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
+                           const __grid_constant__ CUtensorMap tmap_a2, const __grid_constant__ CUtensorMap tmap_b2,
+                           const __grid_constant__ CUtensorMap tmap_sfa2, const __grid_constant__ CUtensorMap tmap_sfb2,
                            const GemmParams p) {
     using C = CfgPair;
     constexpr int BN = 256;
@@ -875,6 +881,12 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             prefetch_tmap(&tmap_b);
             prefetch_tmap(&tmap_sfa);
             prefetch_tmap(&tmap_sfb);
+            if (kDualK) {
+                prefetch_tmap(&tmap_a2);
+                prefetch_tmap(&tmap_b2);
+                prefetch_tmap(&tmap_sfa2);
+                prefetch_tmap(&tmap_sfb2);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -940,7 +952,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             for (int64_t j = 0; j * ncl < ntiles; ++j) {
                 const int64_t t = tile_at(j);
                 if (t >= ntiles) continue;
-                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                const PairTile ti = pair_tile<kDualK>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 bool ok = true;
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
@@ -949,15 +961,19 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                     }
                     const uint32_t fb = cluster_addr(&full[stage], 0);  // the even CTA's stage barrier
                     if (leader) mbar_arrive_expect_tx(&full[stage], C::kTx);
-                    const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kt * BK);
-                    tma_load_2d_pair(smem + stage * C::kABytes, &tmap_a, kx, (int32_t)ti.a_row, fb);
-                    tma_load_2d_pair(smem + C::kOffB + stage * C::kBBytes, &tmap_b, kx, (int32_t)ti.b_row, fb);
-                    tma_load_2d_pair(smem + C::kOffSfa + stage * C::kSfaBytes, &tmap_sfa, 0,
-                                     (int32_t)(2 * (ti.sfa_chunk + kt)), fb);
+                    // second operand set of a two-operand tile: the same coordinates in the second maps
+                    const bool second = kDualK && kt >= ti.k_tiles / 2;
+                    const int kk = second ? kt - ti.k_tiles / 2 : kt;
+                    const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kk * BK);
+                    tma_load_2d_pair(smem + stage * C::kABytes, second ? &tmap_a2 : &tmap_a, kx, (int32_t)ti.a_row, fb);
+                    tma_load_2d_pair(smem + C::kOffB + stage * C::kBBytes, second ? &tmap_b2 : &tmap_b, kx,
+                                     (int32_t)ti.b_row, fb);
+                    tma_load_2d_pair(smem + C::kOffSfa + stage * C::kSfaBytes, second ? &tmap_sfa2 : &tmap_sfa, 0,
+                                     (int32_t)(2 * (ti.sfa_chunk + kk)), fb);
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
-                        tma_load_2d_pair(smem + C::kOffSfb + stage * C::kSfbBytes + 512 * j, &tmap_sfb, 0,
-                                         (int32_t)(2 * (ti.sfb_chunk[j] + kt)), fb);
+                        tma_load_2d_pair(smem + C::kOffSfb + stage * C::kSfbBytes + 512 * j, second ? &tmap_sfb2 : &tmap_sfb,
+                                         0, (int32_t)(2 * (ti.sfb_chunk[j] + kk)), fb);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -971,7 +987,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             for (int64_t j = 0; j * ncl < ntiles && ok; ++j) {
                 const int64_t t = tile_at(j);
                 if (t >= ntiles) continue;
-                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                const PairTile ti = pair_tile<kDualK>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 if (ti.k_tiles == 0) continue;
                 if (!mbar_wait_bounded(tempty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
@@ -1030,7 +1046,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 for (int64_t j = 0; j * ncl < ntiles && ok; ++j) {
                     const int64_t t = tile_at(j);
                     if (t >= ntiles) continue;
-                    const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                    const PairTile ti = pair_tile<kDualK>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                     for (int kt = 0; kt < ti.k_tiles; ++kt) {
                         if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                             ok = false;
@@ -1065,7 +1081,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             for (int64_t j = 0; j * ncl < ntiles; ++j) {
                 const int64_t t = tile_at(j);
                 if (t >= ntiles) continue;
-                const PairTile ti = pair_tile(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                const PairTile ti = pair_tile<kDualK>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo + c_base;
                 const int vrows = ti.valid_rows - quarter * 32;
                 const int vcols = ti.valid_cols - c_base;  // columns of this warp's half inside the output
@@ -1190,7 +1206,7 @@ static int max_pair_clusters(const cudaLaunchConfig_t& cfg) {
     if (d < 0 || d >= host::kMaxDevices) return 1;
     int v = cache[d].load(std::memory_order_relaxed);
     if (v == 0) {
-        if (cudaOccupancyMaxActiveClusters(&v, grouped_mm_pair_kernel, &cfg) != cudaSuccess || v <= 0)
+        if (cudaOccupancyMaxActiveClusters(&v, grouped_mm_pair_kernel<false>, &cfg) != cudaSuccess || v <= 0)
             v = host::num_sms() / 2;
         cudaGetLastError();
         cache[d].store(v, std::memory_order_relaxed);
@@ -1199,16 +1215,29 @@ static int max_pair_clusters(const cudaLaunchConfig_t& cfg) {
 }
 
 // sfa_bytes / sfb_bytes: extents of the scale buffers the maps may address (the ABI's sizing bounds).
+// kDualK: a2 / b2 (same shapes as a / b) with scales p.sfa2 / p.sfb2 are the second operand set.
+template <bool kDualK = false>
 static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
                                   int64_t b_cols, int64_t sfa_bytes, int64_t sfb_bytes, GemmParams& p,
-                                  int64_t pair_tiles_bound, cudaStream_t st) {
+                                  int64_t pair_tiles_bound, cudaStream_t st, const void* a2 = nullptr,
+                                  const void* b2 = nullptr) {
     using C = CfgPair;
-    CUtensorMap ma, mb, msa, msb;
+    CUtensorMap ma, mb, msa, msb, ma2, mb2, msa2, msb2;
     if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, 128) ||
         !make_scale_map(&msa, p.sfa, sfa_bytes) || !make_scale_map(&msb, p.sfb, sfb_bytes))
         return MXFP8_ERR_DRIVER;
+    if (kDualK) {
+        if (!make_map(&ma2, a2, a_rows, a_cols, BM) || !make_map(&mb2, b2, b_rows, b_cols, 128) ||
+            !make_scale_map(&msa2, p.sfa2, sfa_bytes) || !make_scale_map(&msb2, p.sfb2, sfb_bytes))
+            return MXFP8_ERR_DRIVER;
+    } else {
+        ma2 = ma;
+        mb2 = mb;
+        msa2 = msa;
+        msb2 = msb;
+    }
     static std::atomic<int> attr_set[host::kMaxDevices];
-    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_pair_kernel), C::kSmem, attr_set))
+    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_pair_kernel<kDualK>), C::kSmem, attr_set))
         return MXFP8_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -1224,7 +1253,9 @@ static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols,
     cfg.gridDim = dim3(2 * host::num_sms() / 2);
     const int clusters = (int)max64(1, min64(pair_tiles_bound, max_pair_clusters(cfg)));
     cfg.gridDim = dim3(2 * clusters);
-    if (cudaLaunchKernelEx(&cfg, grouped_mm_pair_kernel, ma, mb, msa, msb, p) != cudaSuccess) return MXFP8_ERR_LAUNCH;
+    if (cudaLaunchKernelEx(&cfg, grouped_mm_pair_kernel<kDualK>, ma, mb, msa, msb, ma2, mb2, msa2, msb2, p) !=
+        cudaSuccess)
+        return MXFP8_ERR_LAUNCH;
     return host::last_launch_status();
 }
 
@@ -1268,8 +1299,10 @@ static mxfp8_status_t rowgrouped(const void* tok_q, const void* tok_s, const voi
         p.sfa2 = static_cast<const uint8_t*>(tok2_s);
         p.sfb2 = static_cast<const uint8_t*>(ex2_s);
         if (Nb >= 256) {
-            const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 255) / 256);
-            return launch_gemm<256, false, true>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st, ex2_q, tok2_q);
+            const int64_t bound = ((M + 255) / 256 + G) * ((Nb + 255) / 256);
+            const int64_t sfa_bytes = ((M + 127) / 128 + G) * 128 * p.sfa_ct * 4;
+            return launch_pair<true>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, sfa_bytes, (int64_t)G * p.sfb_estride, p,
+                                     bound, st, tok2_q, ex2_q);
         }
         const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 127) / 128);
         return launch_gemm<128, false, true>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st, ex2_q, tok2_q);
