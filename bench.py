@@ -73,7 +73,7 @@ CONFIG_NAMES = {"tiny": "C1", "scout": "C2", "swiglu": "C3", "imbalanced": "C4"}
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernel of the
 # SwiGLU step, from a one-pass ncu capture of this command, valid only while the GEMM sources hash
 # to the recorded value (the kernel is then unchanged since the counters were taken).
-DOMINANT_TRAFFIC = {"kernel": "grouped_mm_pair_kernel", "bytes_per_launch": 3032201472, "src_sha": "f81fd28862cb108c"}
+DOMINANT_TRAFFIC = {"kernel": "grouped_mm_pair_kernel", "bytes_per_launch": 3090384794, "src_sha": "0a63957b1f38f08f"}
 
 
 def kernel_src_sha() -> str:
@@ -526,7 +526,7 @@ class SwiGLUStep(_CallList):
             elif n.startswith("wgrad_"):
                 ko[n] = gemm_kernel_of(D if n in ("wgrad_gate", "wgrad_up") else H)
             elif n == "gateup_swiglu":
-                ko[n] = "grouped_mm_kernel<256, swiglu epilogue>"
+                ko[n] = "grouped_mm_pair_kernel<swiglu epilogue>"
             elif n == "dgrad_gate_up":
                 ko[n] = ("grouped_mm_pair_kernel<two-operand dgrad>" if D >= 256
                          else "grouped_mm_kernel<128, two-operand dgrad>")
@@ -925,43 +925,49 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
     h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in st.outputs()] for st in sets]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     mk = lambda: torch.cuda.Event(enable_timing=True)
-    h2d_done = [mk() for _ in range(n_steps)]
-    comp_done = [mk() for _ in range(n_steps)]
-    d2h_done = [mk() for _ in range(n_steps)]
-    in_start, comp_start, out_start = ([mk() for _ in range(n_steps)] for _ in range(3))
-    for st in sets:
-        st.run(stream)  # warm both buffer sets once
+
+    def pipeline(n: int):
+        """n steps of the pipeline; returns its events (per step: copy-in, kernels, copy-out start/end)."""
+        ev = {k: [mk() for _ in range(n)] for k in ("in0", "in1", "k0", "k1", "out0", "out1")}
+        for i in range(n):
+            st = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev["k1"][i - 2])        # inputs of set i%2 no longer read
+                ev["in0"][i].record(s_in)
+                for d, h in zip(st.inputs(), h_in):
+                    d.copy_(h, non_blocking=True)
+                ev["in1"][i].record(s_in)
+            stream.wait_event(ev["in1"][i])
+            if i >= 2:
+                stream.wait_event(ev["out1"][i - 2])        # outputs of set i%2 already copied out
+            ev["k0"][i].record(stream)
+            st.run(stream)
+            ev["k1"][i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["k1"][i])
+                ev["out0"][i].record(s_out)
+                for h, d in zip(h_out[i % 2], st.outputs()):
+                    h.copy_(d, non_blocking=True)
+                ev["out1"][i].record(s_out)
+        s_in.wait_stream(s_out)
+        return ev
+
+    # untimed warm-up: both buffer sets through the whole pipeline, copies included (the first DMA to
+    # fresh pinned pages has been seen to run far below the link's rate)
+    pipeline(4)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x0.record(s_in)
     host0 = time.perf_counter()
-    for i in range(n_steps):
-        st = sets[i % 2]
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(comp_done[i - 2])       # inputs of set i%2 no longer read
-            in_start[i].record(s_in)
-            for d, h in zip(st.inputs(), h_in):
-                d.copy_(h, non_blocking=True)
-            h2d_done[i].record(s_in)
-        stream.wait_event(h2d_done[i])
-        if i >= 2:
-            stream.wait_event(d2h_done[i - 2])           # outputs of set i%2 already copied out
-        comp_start[i].record(stream)
-        st.run(stream)
-        comp_done[i].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[i])
-            out_start[i].record(s_out)
-            for h, d in zip(h_out[i % 2], st.outputs()):
-                h.copy_(d, non_blocking=True)
-            d2h_done[i].record(s_out)
-    s_out.wait_event(d2h_done[n_steps - 1])
-    x1.record(s_out)
+    ev = pipeline(n_steps)
+    x1.record(s_in)
     host_ms = (time.perf_counter() - host0) * 1e3 / n_steps  # the host's enqueue time per step
     torch.cuda.synchronize()
+    in_start, h2d_done, comp_start, comp_done, out_start, d2h_done = (
+        ev[k] for k in ("in0", "in1", "k0", "k1", "out0", "out1"))
     for st in sets:
         st.check_status()
     xms = max_over_ranks(x0.elapsed_time(x1) / n_steps, world, device)
@@ -999,7 +1005,7 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
     # with both directions busy, each step's copies need at least this long on this machine's link
     link["copy_ms_per_step"] = round(max(bi, bo) / (link["both_gbs_each"] * 1e6), 3)
     return {"value": round(world * step.flops / xms / 1e9, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_steps,
+            "d2h_bytes_per_step": bo, "ms_per_step": round(xms, 3), "steps": n_steps, "warmup_steps": 4,
             "pipeline": "copy-in, kernels and copy-out on 3 streams over 2 device buffer sets",
             "alone": legs, "timeline_ms": timeline, "host_enqueue_ms_per_step": round(host_ms, 3), "host_link": link}
 

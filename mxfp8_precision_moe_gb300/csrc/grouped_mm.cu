@@ -20,7 +20,11 @@
 //     blocks inside the group are multiplied, so another group's values
 //     (NaN included) never enter its sum.
 //
-// Kernel structure (one CTA per SM, persistent over a static tile order):
+// Two kernels: the CTA-pair kernel (below) runs every GEMM whose output is at least 256 wide,
+// including the SwiGLU gate/up and the two-operand dgrad variants; the single-CTA kernel runs
+// the narrower ones (tiles of 128 x 128).
+//
+// Single-CTA kernel structure (one CTA per SM, persistent over a static tile order):
 //   warp 0      TMA producer: 128B-swizzled A/B tiles (128 x 128 B and BN x 128 B)
 //               and the matching 512-byte scale tiles into a ring of SMEM stages.
 //   warp 1      MMA issuer: four tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each,
@@ -42,13 +46,7 @@ namespace mx {
 constexpr int BM = 128;  // tile rows = tensor-memory lanes
 constexpr int BK = 128;  // contraction bytes (= e4m3 elements) per stage: one 128-byte swizzle row
 constexpr int kThreads = 224;  // producer, MMA issuer, 4 epilogue warps, scale-copy warp
-// SwiGLU variant: 16 epilogue warps (4 per tensor-memory lane quarter, one 32-column block each):
-// its per-element work (silu, two quantizations) needs the extra warps to keep pace with the MMAs.
-constexpr int kSwiEpiWarps = 16;
-constexpr int kThreadsSwi = 96 + 32 * kSwiEpiWarps;
-// the warp that copies each stage's scale tiles into tensor memory: the one after the epilogue warps
-template <bool kSwi>
-constexpr int kSfWarpOf = kSwi ? 2 + kSwiEpiWarps : 6;
+constexpr int kSfWarp = 6;     // the warp that copies each stage's scale tiles into tensor memory
 constexpr int kBand = 16;  // m-tiles per raster band (tiles of a band share B tiles in L2)
 
 enum GemmMode : int { ROWGROUPED = 0, KGROUPED = 1 };
@@ -94,9 +92,10 @@ struct GemmParams {
     int need32;               // group sizes must be multiples of 32 (token-wise blocks or TMA coordinates)
     int32_t* dev_status;
     uint64_t timeout_ns;
-    // SwiGLU gate/up variant only: B rows 0-127 of a tile come from the gate weights (sfb), rows
-    // 128-255 from the up weights (sfb2); out = h1, out2 = h3; h = silu(h1) * h3 quantized along
-    // its row into hq/hs (blocked, row groups) and along the tokens into hTq/hTs (blocked, token groups).
+    // SwiGLU gate/up variant only (CTA-pair kernel): the even CTA's B rows come from the gate weights
+    // (sfb), the odd CTA's from the up weights (sfb2); out = h1, out2 = h3; h = silu(h1) * h3 quantized
+    // along its row into hq/hs (blocked, row groups) and along the tokens into hTq/hTs (blocked, token
+    // groups).
     const uint8_t* sfb2;      // also: second B operand's scales of the two-operand dgrad
     const uint8_t* sfa2;      // two-operand dgrad only: second A operand's scales
     __nv_bfloat16* out2;
@@ -135,14 +134,12 @@ __device__ __forceinline__ int band_split(int64_t l, int64_t mt, int64_t nt, int
     return 0;
 }
 
-// kSwi: a tile is 128 output columns wide and its 256 B rows are those 128 rows of the gate
-// weights followed by the same 128 rows of the up weights.
 // kDualK (ROWGROUPED): the contraction runs over two operand pairs one after the other, k-tiles
 // 0 .. k/2-1 over (A, B) and k/2 .. k-1 over (A2, B2), into one accumulator.
-template <int BN, bool kSwi = false, bool kDualK = false>
+template <int BN, bool kDualK = false>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, const int32_t* ends_s,
                                               const int32_t* pstart_s, int64_t ptotal) {
-    constexpr int TN = kSwi ? 128 : BN;  // output columns per tile
+    constexpr int TN = BN;  // output columns per tile
     TileInfo ti;
     const int64_t ntb = (p.nb + TN - 1) / TN;  // tiles along B rows
     if (p.mode == ROWGROUPED) {
@@ -168,7 +165,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int64_t t, co
         const int64_t last_chunk = (p.nb + 127) / 128 - 1;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int64_t ch = kSwi ? n : min64(n * (BN / 128) + j, last_chunk);
+            const int64_t ch = min64(n * (BN / 128) + j, last_chunk);
             ti.sfb_base[j] = (int64_t)g * p.sfb_estride + ch * p.sfb_ct * 512;
         }
         ti.out = p.out + ti.a_row * p.ldo + n * TN;
@@ -222,13 +219,135 @@ __device__ __forceinline__ uint32_t nonfinite_codes2(uint32_t v) {
 // One bf16 pair times f (a power of two, exact) -> two E4M3 codes (RNE, satfinite).
 __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float f) { return cvt_e4m3x2(bf16lo(v) * f, bf16hi(v) * f); }
 
-template <int BN, bool kSwi, bool kDualK = false>
-__global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
+// One tile of the SwiGLU epilogue, for one warp: TMEM lane quarter `quarter` (32 rows of the tile,
+// one per lane) and 32-column block jb of the tile's 128 h columns.  acc: tensor-memory address of the
+// warp's gate columns (the up columns sit 128 further).  h1 (gate) and h3 (up) are rounded to bf16 and
+// stored; h = bf16(bf16(silu(h1)) * h3) with silu(x) = x / (1 + e^-x) in fp32 (the bf16 rounding points
+// of an elementwise bf16 SwiGLU); h is quantized to MXFP8 along its row and, if p.hTq, along the tokens.
+// release() hands the accumulator back once it is in registers.  a_row: the tile's first token row;
+// valid_rows / valid_cols: rows inside the group and columns inside H; prow0: the padded (128-aligned per
+// group) row of the tile's first row; col0: its first column; ct_T: column tiles of the h^T scales.
+template <class Release>
+__device__ __forceinline__ void swiglu_tile_epilogue(const GemmParams& p, uint32_t acc, int quarter, int jb, int lane,
+                                                     uint8_t* stg, int64_t a_row, int valid_rows, int valid_cols,
+                                                     int64_t prow0, int64_t col0, int64_t ct_T, Release release) {
+    const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
+    const int64_t H = p.nb;
+    uint32_t hg[16], hu[16];  // bf16 pairs (columns 2i, 2i+1 of the block) of h1 and h3
+    {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(acc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hg[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        tmem_ld_32x32b_x32(acc + 128, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hu[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    }
+    tc_fence_before();
+    __syncwarp();
+    release();
+
+    const int vcols = valid_cols;
+    const bool bvalid = 32 * jb < vcols;            // this column block lies inside H
+    const bool rvalid = r < valid_rows;          // this row lies inside the group
+    const int64_t row = a_row + r;
+    const int64_t c0 = col0 + 32 * jb;           // first column of the block
+    // h1 and h3 through the warp's 1 KB staging buffer, 16 columns (32 bytes) of each of the
+    // 32 rows per pass, so every store instruction writes 16 whole 32-byte row segments
+    // instead of 32 scattered 16-byte pieces.  Chunk c of row l sits at l * 32 + 16 (c ^ s),
+    // s = (l >> 2) & 1, which spreads a pass's writes over all banks.
+    auto stage_store = [&](const uint32_t* w, __nv_bfloat16* dst_base, int h) {
+        const int sw = (lane >> 2) & 1;
+        st_shared_v4(stg + lane * 32 + 16 * (0 ^ sw), make_uint4(w[0], w[1], w[2], w[3]));
+        st_shared_v4(stg + lane * 32 + 16 * (1 ^ sw), make_uint4(w[4], w[5], w[6], w[7]));
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int rl = (lane >> 1) + 16 * k, ch = lane & 1;
+            const uint4 v = ld_shared_v4(stg + rl * 32 + 16 * (ch ^ ((rl >> 2) & 1)));
+            if (bvalid && quarter * 32 + rl < valid_rows)
+                *reinterpret_cast<uint4*>(dst_base + (a_row + quarter * 32 + rl) * H + c0 + 16 * h + 8 * ch) = v;
+        }
+        __syncwarp();
+    };
+    stage_store(hg, p.out, 0);
+    stage_store(hg + 8, p.out, 1);
+    stage_store(hu, p.out2, 0);
+    stage_store(hu + 8, p.out2, 1);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a = bf16lo(hg[i]), b = bf16hi(hg[i]);
+        const uint32_t sl = pack_bf16x2(a / (1.0f + expf(-a)), b / (1.0f + expf(-b)));
+        hg[i] = pack_bf16x2(bf16lo(sl) * bf16lo(hu[i]), bf16hi(sl) * bf16hi(hu[i]));
+    }
+    // row-wise: this thread's 32 elements are one block -> 32 codes and one scale byte
+    {
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = vmax_u16x2(m, hg[i] & 0x7FFF7FFFu);
+        const uint32_t sc = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
+        const float f = inv_scale_from_e8m0(sc);
+        uint32_t codes[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            codes[i] = sc == 0xFFu ? nonfinite_codes2(hg[2 * i]) | (nonfinite_codes2(hg[2 * i + 1]) << 16)
+                                   : quant_pair(hg[2 * i], f) | (quant_pair(hg[2 * i + 1], f) << 16);
+        if (bvalid && rvalid) {
+            uint4* gq = reinterpret_cast<uint4*>(p.hq + row * H + c0);
+            gq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            gq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        }
+        // the tile's row scales are one 512-byte blocked tile: row r -> (r%32)*16 + (r/32)*4,
+        // block jb -> byte jb; rows past the group and blocks past H are padding (0)
+        p.hs[((prow0 >> 7) * p.hs_ct + (col0 >> 7)) * 512 + lane * 16 + quarter * 4 + jb] =
+            (uint8_t)((bvalid && rvalid) ? sc : 0u);
+    }
+    if (p.hTq != nullptr) {
+        // group sizes are multiples of 32 here (device-checked), so the warp's 32 rows are
+        // either all inside the group or all padding
+        const int64_t cq = prow0 / 32 + quarter;  // scale column of this 32-token block
+        uint32_t my_s = 0;                          // scale of column c0 + lane
+        if (valid_rows > quarter * 32 && bvalid) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t w = hg[i];
+                const uint32_t slo = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, w & 0x7FFFu));
+                const uint32_t shi = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, (w >> 16) & 0x7FFFu));
+                uint32_t c2 = cvt_e4m3x2(bf16lo(w) * inv_scale_from_e8m0(slo),
+                                         bf16hi(w) * inv_scale_from_e8m0(shi));
+                if (slo == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu | ((w >> 8) & 0x80u);
+                if (shi == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u | ((w >> 16) & 0x8000u);
+                // transpose through shared memory: byte (column c, token lane) at c*32 + lane
+                st_shared_u8(stg + (2 * i) * 32 + lane, c2 & 0xFFu);
+                st_shared_u8(stg + (2 * i + 1) * 32 + lane, c2 >> 8);
+                my_s = lane == 2 * i ? slo : (lane == 2 * i + 1 ? shi : my_s);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int cc = 16 * h2 + (lane >> 1);  // column within the block
+                const uint4 val = ld_shared_v4(stg + cc * 32 + (lane & 1) * 16);
+                if (32 * jb + cc < vcols)
+                    *reinterpret_cast<uint4*>(p.hTq + (c0 + cc) * p.M + a_row + quarter * 32 +
+                                              (lane & 1) * 16) = val;
+            }
+            __syncwarp();
+            if (32 * jb + lane >= vcols) my_s = 0;
+        }
+        const int64_t cH = c0 + lane;  // row of h^T (columns past H: padding 0)
+        p.hTs[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] =
+            (uint8_t)my_s;
+    }
+}
+
+template <int BN, bool kDualK = false>
+__global__ void __launch_bounds__(kThreads, 1)
     grouped_mm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_b2, const __grid_constant__ CUtensorMap tmap_a2,
                       const GemmParams p) {
     using C = Cfg<BN>;
-    static_assert(!kSwi || BN == 256, "the SwiGLU variant pairs 128 gate with 128 up rows");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int32_t ends_s[kMaxGroups];
     __shared__ int32_t pstart_s[kMaxGroups];
@@ -292,7 +411,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             abort_s = 0;
             prefetch_tmap(&tmap_a);
             prefetch_tmap(&tmap_b);
-            if (kSwi || kDualK) prefetch_tmap(&tmap_b2);
+            if (kDualK) prefetch_tmap(&tmap_b2);
             if (kDualK) prefetch_tmap(&tmap_a2);
         }
     } else if (warp == 1) {
@@ -303,7 +422,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             }
             for (int a = 0; a < C::kAcc; ++a) {
                 mbar_init(&tfull[a], 1);
-                mbar_init(&tempty[a], kSwi ? kSwiEpiWarps : 4);
+                mbar_init(&tempty[a], 4);
             }
             mbar_init(drain, 1);
             for (int s = 0; s < C::kStages; ++s) mbar_init(&sfull[s], 1);
@@ -324,8 +443,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
     if (bad_s) {
         if (threadIdx.x == 0) report(p.dev_status, MXFP8_ERR_OFFSETS);
     } else {
-        constexpr int TN = kSwi ? 128 : BN;  // output columns per tile (as in tile_info)
-        const int64_t ntb = (p.nb + TN - 1) / TN;
+        const int64_t ntb = (p.nb + BN - 1) / BN;  // tiles along B rows (as in tile_info)
         const int64_t ntiles = p.mode == ROWGROUPED ? (ptotal / BM) * ntb
                                                     : (int64_t)p.G * ((p.na + BM - 1) / BM) * ntb;
 
@@ -336,7 +454,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             uint32_t issued_mask = 0, last_phase = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kDualK>(p, t, ends_s, pstart_s, ptotal);
                 const int kt_half = kDualK ? ti.k_tiles / 2 : ti.k_tiles;
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
@@ -353,19 +471,11 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                     const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kk * BK);
                     tma_load_2d(sa, second ? &tmap_a2 : &tmap_a, kx, (int32_t)ti.a_row, &full[stage]);
                     bulk_load(ssa, (second ? p.sfa2 : p.sfa) + ti.sfa_base + kk * ti.sf_kstep, 512, &full[stage]);
-                    if constexpr (kSwi) {
-                        // rows 0-127: gate weights, rows 128-255: the same rows of the up weights
-                        tma_load_2d(sb, &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
-                        tma_load_2d(sb + 128 * BK, &tmap_b2, kx, (int32_t)ti.b_row, &full[stage]);
-                        bulk_load(ssb, p.sfb + ti.sfb_base[0] + kt * ti.sf_kstep, 512, &full[stage]);
-                        bulk_load(ssb + 512, p.sfb2 + ti.sfb_base[1] + kt * ti.sf_kstep, 512, &full[stage]);
-                    } else {
-                        tma_load_2d(sb, second ? &tmap_b2 : &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
+                    tma_load_2d(sb, second ? &tmap_b2 : &tmap_b, kx, (int32_t)ti.b_row, &full[stage]);
 #pragma unroll
-                        for (int j = 0; j < BN / 128; ++j)
-                            bulk_load(ssb + j * 512, (second ? p.sfb2 : p.sfb) + ti.sfb_base[j] + kk * ti.sf_kstep, 512,
-                                      &full[stage]);
-                    }
+                    for (int j = 0; j < BN / 128; ++j)
+                        bulk_load(ssb + j * 512, (second ? p.sfb2 : p.sfb) + ti.sfb_base[j] + kk * ti.sf_kstep, 512,
+                                  &full[stage]);
                     issued_mask |= 1u << stage;
                     last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -385,7 +495,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kDualK>(p, t, ends_s, pstart_s, ptotal);
                 if (ti.k_tiles == 0) continue;
                 if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
@@ -433,7 +543,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             tc_commit(drain);
             volatile int no_abort = 0;
             mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
-        } else if (warp == kSfWarpOf<kSwi>) {
+        } else if (warp == kSfWarp) {
             // ------------------------------------------------ scale copies
             // As soon as a stage lands, its scale tiles go to that stage's tensor-memory columns
             // (tcgen05.cp, SMEM -> TMEM) and the copy's completion is signalled on sfull; the MMA
@@ -444,7 +554,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                 uint32_t phase = 0;
                 bool ok = true;
                 for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                    const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
+                    const TileInfo ti = tile_info<BN, kDualK>(p, t, ends_s, pstart_s, ptotal);
                     for (int kt = 0; kt < ti.k_tiles; ++kt) {
                         if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                             ok = false;
@@ -468,135 +578,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
                 mbar_wait_bounded(sfdrain, 0, p.timeout_ns, &no_abort, p.dev_status);
             }
         } else if (warp >= 2) {
-          if constexpr (kSwi) {
-            // ------------------------------------------------ SwiGLU epilogue
-            // Per tile: h1 (gate, accumulator columns 0-127) and h3 (up, 128-255) rounded to bf16 and
-            // stored; h = bf16(bf16(silu(h1)) * h3) with silu(x) = x / (1 + e^-x) in fp32 (the bf16
-            // rounding points of an elementwise bf16 SwiGLU); h quantized to MXFP8 along its row and,
-            // optionally, along the tokens.  Warp (quarter q, block j) owns rows 32q..32q+31 and the
-            // 32 columns 32j..32j+31: one row block of 32 per thread, one token block of 32 per column.
-            const int quarter = warp & 3;
-            const int jb = (warp - 2) >> 2;     // 32-column block of this warp
-            const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
-            uint8_t* stg = smem + C::kOffStage + (warp - 2) * 1024;
-            const int64_t H = p.nb;
-            const int64_t ct_T = ptotal / 128;  // column tiles of the token-grouped h^T scales
-            uint32_t acc_phase = 0;
-            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
-                if (!mbar_wait_bounded(&tfull[0], acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
-                tc_fence_after();
-                uint32_t hg[16], hu[16];  // bf16 pairs (columns 2i, 2i+1 of the block) of h1 and h3
-                {
-                    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + 32 * jb;
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) hg[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    tmem_ld_32x32b_x32(taddr + 128, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) hu[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_relaxed(&tempty[0]);
-                acc_phase ^= 1u;
-
-                const int vcols = ti.valid_cols;
-                const bool bvalid = 32 * jb < vcols;            // this column block lies inside H
-                const bool rvalid = r < ti.valid_rows;          // this row lies inside the group
-                const int64_t row = ti.a_row + r;
-                const int64_t c0 = ti.col0 + 32 * jb;           // first column of the block
-                // h1 and h3 through the warp's 1 KB staging buffer, 16 columns (32 bytes) of each of the
-                // 32 rows per pass, so every store instruction writes 16 whole 32-byte row segments
-                // instead of 32 scattered 16-byte pieces.  Chunk c of row l sits at l * 32 + 16 (c ^ s),
-                // s = (l >> 2) & 1, which spreads a pass's writes over all banks.
-                auto stage_store = [&](const uint32_t* w, __nv_bfloat16* dst_base, int h) {
-                    const int sw = (lane >> 2) & 1;
-                    st_shared_v4(stg + lane * 32 + 16 * (0 ^ sw), make_uint4(w[0], w[1], w[2], w[3]));
-                    st_shared_v4(stg + lane * 32 + 16 * (1 ^ sw), make_uint4(w[4], w[5], w[6], w[7]));
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int rl = (lane >> 1) + 16 * k, ch = lane & 1;
-                        const uint4 v = ld_shared_v4(stg + rl * 32 + 16 * (ch ^ ((rl >> 2) & 1)));
-                        if (bvalid && quarter * 32 + rl < ti.valid_rows)
-                            *reinterpret_cast<uint4*>(dst_base + (ti.a_row + quarter * 32 + rl) * H + c0 + 16 * h + 8 * ch) = v;
-                    }
-                    __syncwarp();
-                };
-                stage_store(hg, p.out, 0);
-                stage_store(hg + 8, p.out, 1);
-                stage_store(hu, p.out2, 0);
-                stage_store(hu + 8, p.out2, 1);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float a = bf16lo(hg[i]), b = bf16hi(hg[i]);
-                    const uint32_t sl = pack_bf16x2(a / (1.0f + expf(-a)), b / (1.0f + expf(-b)));
-                    hg[i] = pack_bf16x2(bf16lo(sl) * bf16lo(hu[i]), bf16hi(sl) * bf16hi(hu[i]));
-                }
-                // row-wise: this thread's 32 elements are one block -> 32 codes and one scale byte
-                {
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) m = vmax_u16x2(m, hg[i] & 0x7FFF7FFFu);
-                    const uint32_t sc = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
-                    const float f = inv_scale_from_e8m0(sc);
-                    uint32_t codes[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        codes[i] = sc == 0xFFu ? nonfinite_codes2(hg[2 * i]) | (nonfinite_codes2(hg[2 * i + 1]) << 16)
-                                               : quant_pair(hg[2 * i], f) | (quant_pair(hg[2 * i + 1], f) << 16);
-                    if (bvalid && rvalid) {
-                        uint4* gq = reinterpret_cast<uint4*>(p.hq + row * H + c0);
-                        gq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-                        gq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-                    }
-                    // the tile's row scales are one 512-byte blocked tile: row r -> (r%32)*16 + (r/32)*4,
-                    // block jb -> byte jb; rows past the group and blocks past H are padding (0)
-                    p.hs[((ti.prow0 >> 7) * p.hs_ct + (ti.col0 >> 7)) * 512 + lane * 16 + quarter * 4 + jb] =
-                        (uint8_t)((bvalid && rvalid) ? sc : 0u);
-                }
-                if (p.hTq != nullptr) {
-                    // group sizes are multiples of 32 here (device-checked), so the warp's 32 rows are
-                    // either all inside the group or all padding
-                    const int64_t cq = ti.prow0 / 32 + quarter;  // scale column of this 32-token block
-                    uint32_t my_s = 0;                          // scale of column c0 + lane
-                    if (ti.valid_rows > quarter * 32 && bvalid) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const uint32_t w = hg[i];
-                            const uint32_t slo = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, w & 0x7FFFu));
-                            const uint32_t shi = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, (w >> 16) & 0x7FFFu));
-                            uint32_t c2 = cvt_e4m3x2(bf16lo(w) * inv_scale_from_e8m0(slo),
-                                                     bf16hi(w) * inv_scale_from_e8m0(shi));
-                            if (slo == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu | ((w >> 8) & 0x80u);
-                            if (shi == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u | ((w >> 16) & 0x8000u);
-                            // transpose through shared memory: byte (column c, token lane) at c*32 + lane
-                            st_shared_u8(stg + (2 * i) * 32 + lane, c2 & 0xFFu);
-                            st_shared_u8(stg + (2 * i + 1) * 32 + lane, c2 >> 8);
-                            my_s = lane == 2 * i ? slo : (lane == 2 * i + 1 ? shi : my_s);
-                        }
-                        __syncwarp();
-#pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int cc = 16 * h2 + (lane >> 1);  // column within the block
-                            const uint4 val = ld_shared_v4(stg + cc * 32 + (lane & 1) * 16);
-                            if (32 * jb + cc < vcols)
-                                *reinterpret_cast<uint4*>(p.hTq + (c0 + cc) * p.M + ti.a_row + quarter * 32 +
-                                                          (lane & 1) * 16) = val;
-                        }
-                        __syncwarp();
-                        if (32 * jb + lane >= vcols) my_s = 0;
-                    }
-                    const int64_t cH = c0 + lane;  // row of h^T (columns past H: padding 0)
-                    p.hTs[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] =
-                        (uint8_t)my_s;
-                }
-            }
-          } else {
+          {
             // ------------------------------------------------ epilogue
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
@@ -604,7 +586,7 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                const TileInfo ti = tile_info<BN, kSwi, kDualK>(p, t, ends_s, pstart_s, ptotal);
+                const TileInfo ti = tile_info<BN, kDualK>(p, t, ends_s, pstart_s, ptotal);
                 const bool row_ok = r < ti.valid_rows;
                 __nv_bfloat16* orow = ti.out + (int64_t)r * ti.ldo;
                 __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo;  // first row of this warp
@@ -682,6 +664,9 @@ __global__ void __launch_bounds__(kSwi ? kThreadsSwi : kThreads, 1)
 // boxes); the even CTA's scale-copy warp moves them into both CTAs' tensor memory.  Stage and
 // accumulator release are multicast commits to both CTAs; the odd CTA's epilogue reports a
 // drained accumulator to the even CTA with a remote mbarrier arrive.
+// Variants: two-operand (a second (A2, B2) contraction into the same accumulator) and SwiGLU
+// gate/up (a 128-column tile of h; the even CTA stages gate rows, the odd CTA the same up rows,
+// and each CTA's 16 epilogue warps turn its own 128 token rows into h1, h3 and quantized h).
 // ============================================================================================
 constexpr int kPairStages = 5;
 constexpr int kSortGroups = 128;  // K-grouped schedules rank at most this many groups (O(G^2) per CTA)
@@ -689,8 +674,15 @@ constexpr int kSortGroups = 128;  // K-grouped schedules rank at most this many 
 // half of the accumulator, so the single accumulator is handed back to the MMA warp in half the time
 // (a K-grouped tile of a small group contracts over few k-tiles, and the drain is per tile).
 constexpr int kPairEpiWarps = 8;
-constexpr int kPairSfWarp = 2 + kPairEpiWarps;  // the scale-copy warp
-constexpr int kThreadsPair = 96 + 32 * kPairEpiWarps;
+// The SwiGLU variant's epilogue (silu, two quantizations per element) runs 16 warps per CTA, four per
+// lane quarter, one 32-column block of h each (swiglu_tile_epilogue).
+constexpr int kPairSwiEpiWarps = 16;
+template <bool kSwi>
+constexpr int kPairEpiOf = kSwi ? kPairSwiEpiWarps : kPairEpiWarps;
+template <bool kSwi>
+constexpr int kPairSfWarpOf = 2 + kPairEpiOf<kSwi>;  // the scale-copy warp, after the epilogue warps
+template <bool kSwi>
+constexpr int kThreadsPairOf = 96 + 32 * kPairEpiOf<kSwi>;
 // K-grouped pair tiles run in bands of 8 row-tiles: the 76 tiles of a wave then share about
 // 8 A and 10 B operand slabs instead of 16 and 5 (a long group's slabs do not fit in L2 together).
 constexpr int kBandPairK = 8;
@@ -724,19 +716,24 @@ struct PairTile {
     int kb_last;                      // 32-wide K blocks of the last k-tile inside the tile's contraction
     int64_t sfa_chunk, sfb_chunk[2];  // 512-byte scale tiles of k-tile 0 (index = byte offset / 512)
     __nv_bfloat16* out;               // first element of this CTA's 128 rows
+    int64_t prow0, col0;              // ROWGROUPED: padded (128-aligned per group) first row; first column
     int64_t ldo;
     int valid_rows, valid_cols;
 };
 
 // Tile t of the pair schedule, seen from CTA `half` (0: rows 0-127 of the pair tile, 1: 128-255).
 // K-grouped: tile t belongs to the group at position t / per_g of gorder_s (or of the natural order).
-template <bool kDualK = false>
+// kSwi (ROWGROUPED): a pair tile is 128 output columns of h; the even CTA stages those 128 rows of the
+// gate weights, the odd CTA the same rows of the up weights, so accumulator columns 0-127 of either
+// CTA hold h1 for its own 128 token rows and columns 128-255 hold h3.
+template <bool kDualK = false, bool kSwi = false>
 __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, int half, const int32_t* ends_s,
                                               const int32_t* pstart_s, const int32_t* tstart_s, int64_t ptotal,
                                               const int32_t* gorder_s, bool sorted) {
     constexpr int BN = 256;
+    constexpr int TN = kSwi ? 128 : BN;  // output columns per tile
     PairTile ti;
-    const int64_t ntb = (p.nb + BN - 1) / BN;
+    const int64_t ntb = (p.nb + TN - 1) / TN;
     const int64_t last_chunk = (p.nb + 127) / 128 - 1;
     if (p.mode == ROWGROUPED) {
         int lo = 0, hi = p.G;
@@ -752,21 +749,23 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
         const int64_t rows0 = m2 * 256 + half * 128;
         ti.g = g;
         ti.a_row = start + rows0;
-        ti.b_row = (int64_t)g * p.nb + n * BN + half * 128;
+        ti.b_row = (int64_t)g * p.nb + n * TN + (kSwi ? 0 : half * 128);
         ti.a_x0 = 0;
         ti.k_tiles = (int)((p.kc + BK - 1) / BK) * (kDualK ? 2 : 1);
         ti.kb_last = BK / 32;
         const int64_t cA = min64(2 * m2 + half, (size + 127) / 128 - 1);  // clamp: rows past the group are masked
         ti.sfa_chunk = (pstart_s[g] / 128 + cA) * p.sfa_ct;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int64_t ch = min64(n * 2 + j, last_chunk);
+        for (int j = 0; j < 2; ++j) {  // kSwi: chunk n of the gate scales (j = 0) and of the up scales (j = 1)
+            const int64_t ch = kSwi ? n : min64(n * 2 + j, last_chunk);
             ti.sfb_chunk[j] = (int64_t)g * (p.sfb_estride / 512) + ch * p.sfb_ct;
         }
-        ti.out = p.out + ti.a_row * p.ldo + n * BN;
+        ti.out = p.out + ti.a_row * p.ldo + n * TN;
         ti.ldo = p.ldo;
-        ti.valid_rows = (int)max64(-1, min64(128, size - rows0));
-        ti.valid_cols = (int)min64(BN, p.nb - n * BN);
+        ti.valid_rows = (int)max64(-1, min64(128, size - rows0));  // <= 0: past the group's padded rows
+        ti.valid_cols = (int)min64(TN, p.nb - n * TN);
+        ti.prow0 = (int64_t)pstart_s[g] + rows0;
+        ti.col0 = n * TN;
     } else {
         const int64_t nta2 = (p.na + 255) / 256;
         const int64_t per_g = nta2 * ntb;
@@ -797,8 +796,10 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int64_t t, in
 
 // kDualK (row-grouped only): the contraction runs over two operand sets one after the other, k-tiles
 // 0 .. k/2-1 over (A, B) and k/2 .. k-1 over (A2, B2), into one accumulator.
-template <bool kDualK>
-__global__ void __launch_bounds__(kThreadsPair, 1)
+// kSwi: the SwiGLU gate/up variant (pair_tile, swiglu_tile_epilogue); tmap_b2 / tmap_sfb2 are the up
+// weights and their scales.
+template <bool kDualK, bool kSwi = false>
+__global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
     grouped_mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                            const __grid_constant__ CUtensorMap tmap_a2, const __grid_constant__ CUtensorMap tmap_b2,
@@ -848,7 +849,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
         for (int g = g0; g < g1; ++g) {
             const int32_t e = max(prev, min(max(p.offs[g], 0), Mc));
             ends_s[g] = e;
-            if (p.mode == KGROUPED && (e - prev) % 32 != 0) bad = 1;
+            if ((p.mode == KGROUPED || p.need32) && (e - prev) % 32 != 0) bad = 1;  // token blocks of 32
             psum += ((e - prev + 127) / 128) * 128;
             tsum += (e - prev + 255) / 256;
             prev = e;
@@ -895,7 +896,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 mbar_init(&empty[s], 1);
             }
             mbar_init(tfull, 1);
-            mbar_init(tempty, 2 * kPairEpiWarps);  // every epilogue warp of both CTAs of the pair
+            mbar_init(tempty, 2 * kPairEpiOf<kSwi>);  // every epilogue warp of both CTAs of the pair
             mbar_init(drain, 1);
             for (int s = 0; s < C::kStages; ++s) mbar_init(&sfull[s], 1);
             mbar_init(sfdrain, 1);
@@ -916,7 +917,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     if (bad_s) {
         if (threadIdx.x == 0 && leader) report(p.dev_status, MXFP8_ERR_OFFSETS);
     } else {
-        const int64_t ntb = (p.nb + BN - 1) / BN;
+        const int64_t ntb = (p.nb + (kSwi ? 128 : BN) - 1) / (kSwi ? 128 : BN);
         int64_t ntiles;
         if (p.mode == ROWGROUPED) {
             ntiles = (int64_t)tstart_s[p.G - 1] + (ends_s[p.G - 1] - (p.G > 1 ? ends_s[p.G - 2] : 0) + 255) / 256;
@@ -952,7 +953,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             for (int64_t j = 0; j * ncl < ntiles; ++j) {
                 const int64_t t = tile_at(j);
                 if (t >= ntiles) continue;
-                const PairTile ti = pair_tile<kDualK>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 bool ok = true;
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
@@ -966,14 +967,16 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                     const int kk = second ? kt - ti.k_tiles / 2 : kt;
                     const int32_t kx = (int32_t)(ti.a_x0 + (int64_t)kk * BK);
                     tma_load_2d_pair(smem + stage * C::kABytes, second ? &tmap_a2 : &tmap_a, kx, (int32_t)ti.a_row, fb);
-                    tma_load_2d_pair(smem + C::kOffB + stage * C::kBBytes, second ? &tmap_b2 : &tmap_b, kx,
-                                     (int32_t)ti.b_row, fb);
+                    // kSwi: the even CTA's B rows are the gate weights', the odd CTA's the up weights'
+                    tma_load_2d_pair(smem + C::kOffB + stage * C::kBBytes,
+                                     (second || (kSwi && half)) ? &tmap_b2 : &tmap_b, kx, (int32_t)ti.b_row, fb);
                     tma_load_2d_pair(smem + C::kOffSfa + stage * C::kSfaBytes, second ? &tmap_sfa2 : &tmap_sfa, 0,
                                      (int32_t)(2 * (ti.sfa_chunk + kk)), fb);
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
-                        tma_load_2d_pair(smem + C::kOffSfb + stage * C::kSfbBytes + 512 * j, second ? &tmap_sfb2 : &tmap_sfb,
-                                         0, (int32_t)(2 * (ti.sfb_chunk[j] + kk)), fb);
+                        tma_load_2d_pair(smem + C::kOffSfb + stage * C::kSfbBytes + 512 * j,
+                                         (second || (kSwi && j == 1)) ? &tmap_sfb2 : &tmap_sfb, 0,
+                                         (int32_t)(2 * (ti.sfb_chunk[j] + kk)), fb);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -987,7 +990,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             for (int64_t j = 0; j * ncl < ntiles && ok; ++j) {
                 const int64_t t = tile_at(j);
                 if (t >= ntiles) continue;
-                const PairTile ti = pair_tile<kDualK>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 if (ti.k_tiles == 0) continue;
                 if (!mbar_wait_bounded(tempty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
@@ -1035,7 +1038,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             tc_commit_pair(drain, 0x1);
             volatile int no_abort = 0;
             mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
-        } else if (warp == kPairSfWarp) {
+        } else if (warp == kPairSfWarpOf<kSwi>) {
             // ------------------------------------------------ scale copies (even CTA only)
             // Each landed stage's scale tiles go to its tensor-memory columns in both CTAs (the
             // cta_group::2 copy), signalled on the even CTA's sfull; the MMA thread waits for it.
@@ -1046,7 +1049,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 for (int64_t j = 0; j * ncl < ntiles && ok; ++j) {
                     const int64_t t = tile_at(j);
                     if (t >= ntiles) continue;
-                    const PairTile ti = pair_tile<kDualK>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                    const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                     for (int kt = 0; kt < ti.k_tiles; ++kt) {
                         if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                             ok = false;
@@ -1068,6 +1071,32 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
                 volatile int no_abort = 0;
                 mbar_wait_bounded(sfdrain, 0, p.timeout_ns, &no_abort, p.dev_status);
             }
+        } else if (warp >= 2 && kSwi) {
+            // ------------------------------------------------ SwiGLU epilogue (both CTAs: own 128 rows)
+            const int quarter = warp & 3;
+            const int jb = (warp - 2) >> 2;  // 32-column block of h of this warp
+            uint8_t* stg = smem + C::kOffStage + (warp - 2) * 1024;
+            const int64_t ct_T = ptotal / 128;
+            const uint32_t tempty_leader = cluster_addr(tempty, 0);
+            uint32_t acc_phase = 0;
+            for (int64_t j = 0; j * ncl < ntiles; ++j) {
+                const int64_t t = tile_at(j);
+                if (t >= ntiles) continue;
+                const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                if (!mbar_wait_bounded(tfull, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+                acc_phase ^= 1u;
+                tc_fence_after();
+                auto release = [&] { if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader); };
+                if (ti.valid_rows > 0) {
+                    swiglu_tile_epilogue(p, tmem + ((uint32_t)(quarter * 32) << 16) + 32 * jb, quarter, jb, lane, stg,
+                                         ti.a_row, ti.valid_rows, ti.valid_cols, ti.prow0, ti.col0, ct_T, release);
+                } else {
+                    // this CTA's half lies past the group's padded rows: it owns no output, not even padding
+                    tc_fence_before();
+                    __syncwarp();
+                    release();
+                }
+            }
         } else if (warp >= 2) {
             // ------------------------------------------------ epilogue (both CTAs: own 128 rows)
             // Warp w drains lane quarter w % 4 (the quarter its tensor-memory access is bound to) and
@@ -1081,7 +1110,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
             for (int64_t j = 0; j * ncl < ntiles; ++j) {
                 const int64_t t = tile_at(j);
                 if (t >= ntiles) continue;
-                const PairTile ti = pair_tile<kDualK>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
+                const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 __nv_bfloat16* wout = ti.out + (int64_t)(quarter * 32) * ti.ldo + c_base;
                 const int vrows = ti.valid_rows - quarter * 32;
                 const int vcols = ti.valid_cols - c_base;  // columns of this warp's half inside the output
@@ -1158,23 +1187,24 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 
 // b2: SwiGLU variant: the up weights, same shape as b (each B map then has 128-row boxes); two-operand
 // dgrad (kDualK): the second B operand.  a2: two-operand dgrad only, the second A operand.
-template <int BN, bool kSwi = false, bool kDualK = false>
+template <int BN, bool kDualK = false>
 static mxfp8_status_t launch_gemm(const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
                                   int64_t b_cols, GemmParams& p, int64_t tiles_bound, cudaStream_t st,
                                   const void* b2 = nullptr, const void* a2 = nullptr) {
     using C = Cfg<BN>;
     CUtensorMap ma, mb, mb2, ma2;
-    const int b_box = kSwi ? 128 : BN;
-    if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, b_box)) return MXFP8_ERR_DRIVER;
-    if ((kSwi || kDualK) ? !make_map(&mb2, b2, b_rows, b_cols, b_box) : false) return MXFP8_ERR_DRIVER;
+    if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, BN)) return MXFP8_ERR_DRIVER;
+    if (kDualK ? !make_map(&mb2, b2, b_rows, b_cols, BN) : false) return MXFP8_ERR_DRIVER;
     if (kDualK ? !make_map(&ma2, a2, a_rows, a_cols, BM) : false) return MXFP8_ERR_DRIVER;
-    if (!kSwi && !kDualK) mb2 = mb;
-    if (!kDualK) ma2 = ma;
+    if (!kDualK) {
+        mb2 = mb;
+        ma2 = ma;
+    }
     static std::atomic<int> attr_set[host::kMaxDevices];
-    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_kernel<BN, kSwi, kDualK>), C::kSmem, attr_set))
+    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_kernel<BN, kDualK>), C::kSmem, attr_set))
         return MXFP8_ERR_LAUNCH;
     const int grid = (int)max64(1, min64(tiles_bound, host::num_sms()));
-    grouped_mm_kernel<BN, kSwi, kDualK><<<grid, kSwi ? kThreadsSwi : kThreads, C::kSmem, st>>>(ma, mb, mb2, ma2, p);
+    grouped_mm_kernel<BN, kDualK><<<grid, kThreads, C::kSmem, st>>>(ma, mb, mb2, ma2, p);
     return host::last_launch_status();
 }
 
@@ -1200,13 +1230,14 @@ static bool make_scale_map(CUtensorMap* m, const void* base, int64_t bytes) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <bool kDualK, bool kSwi>
 static int max_pair_clusters(const cudaLaunchConfig_t& cfg) {
     static std::atomic<int> cache[host::kMaxDevices];
     const int d = host::current_device();
     if (d < 0 || d >= host::kMaxDevices) return 1;
     int v = cache[d].load(std::memory_order_relaxed);
     if (v == 0) {
-        if (cudaOccupancyMaxActiveClusters(&v, grouped_mm_pair_kernel<false>, &cfg) != cudaSuccess || v <= 0)
+        if (cudaOccupancyMaxActiveClusters(&v, grouped_mm_pair_kernel<kDualK, kSwi>, &cfg) != cudaSuccess || v <= 0)
             v = host::num_sms() / 2;
         cudaGetLastError();
         cache[d].store(v, std::memory_order_relaxed);
@@ -1216,7 +1247,8 @@ static int max_pair_clusters(const cudaLaunchConfig_t& cfg) {
 
 // sfa_bytes / sfb_bytes: extents of the scale buffers the maps may address (the ABI's sizing bounds).
 // kDualK: a2 / b2 (same shapes as a / b) with scales p.sfa2 / p.sfb2 are the second operand set.
-template <bool kDualK = false>
+// kSwi: b2 with scales p.sfb2 are the up weights (b the gate weights).
+template <bool kDualK = false, bool kSwi = false>
 static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols, const void* b, int64_t b_rows,
                                   int64_t b_cols, int64_t sfa_bytes, int64_t sfb_bytes, GemmParams& p,
                                   int64_t pair_tiles_bound, cudaStream_t st, const void* a2 = nullptr,
@@ -1230,6 +1262,11 @@ static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols,
         if (!make_map(&ma2, a2, a_rows, a_cols, BM) || !make_map(&mb2, b2, b_rows, b_cols, 128) ||
             !make_scale_map(&msa2, p.sfa2, sfa_bytes) || !make_scale_map(&msb2, p.sfb2, sfb_bytes))
             return MXFP8_ERR_DRIVER;
+    } else if (kSwi) {
+        if (!make_map(&mb2, b2, b_rows, b_cols, 128) || !make_scale_map(&msb2, p.sfb2, sfb_bytes))
+            return MXFP8_ERR_DRIVER;
+        ma2 = ma;
+        msa2 = msa;
     } else {
         ma2 = ma;
         mb2 = mb;
@@ -1237,7 +1274,7 @@ static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols,
         msb2 = msb;
     }
     static std::atomic<int> attr_set[host::kMaxDevices];
-    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_pair_kernel<kDualK>), C::kSmem, attr_set))
+    if (!host::ensure_smem(reinterpret_cast<const void*>(grouped_mm_pair_kernel<kDualK, kSwi>), C::kSmem, attr_set))
         return MXFP8_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -1245,15 +1282,15 @@ static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols,
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreadsPair);
+    cfg.blockDim = dim3(kThreadsPairOf<kSwi>);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(2 * host::num_sms() / 2);
-    const int clusters = (int)max64(1, min64(pair_tiles_bound, max_pair_clusters(cfg)));
+    const int clusters = (int)max64(1, min64(pair_tiles_bound, max_pair_clusters<kDualK, kSwi>(cfg)));
     cfg.gridDim = dim3(2 * clusters);
-    if (cudaLaunchKernelEx(&cfg, grouped_mm_pair_kernel<kDualK>, ma, mb, msa, msb, ma2, mb2, msa2, msb2, p) !=
+    if (cudaLaunchKernelEx(&cfg, grouped_mm_pair_kernel<kDualK, kSwi>, ma, mb, msa, msb, ma2, mb2, msa2, msb2, p) !=
         cudaSuccess)
         return MXFP8_ERR_LAUNCH;
     return host::last_launch_status();
@@ -1305,7 +1342,7 @@ static mxfp8_status_t rowgrouped(const void* tok_q, const void* tok_s, const voi
                                      bound, st, tok2_q, ex2_q);
         }
         const int64_t bound = ((M + BM - 1) / BM + G) * ((Nb + 127) / 128);
-        return launch_gemm<128, false, true>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st, ex2_q, tok2_q);
+        return launch_gemm<128, true>(tok_q, M, Kc, ex_q, (int64_t)G * Nb, Kc, p, bound, st, ex2_q, tok2_q);
     }
     if (Nb >= 256) {
         const int64_t bound = ((M + 255) / 256 + G) * ((Nb + 255) / 256);
@@ -1419,8 +1456,10 @@ extern "C" mxfp8_status_t mxfp8_grouped_mm_swiglu_fwd(const void* x_q, const voi
     p.need32 = hT_q != nullptr;
     p.dev_status = dev_status;
     p.timeout_ns = default_timeout_ns();
-    const int64_t bound = ((M + BM - 1) / BM + G) * ((H + 127) / 128);
-    return launch_gemm<256, true>(x_q, M, D, wg_q, (int64_t)G * H, D, p, bound, st, wu_q);
+    const int64_t bound = ((M + 255) / 256 + G) * ((H + 127) / 128);
+    const int64_t sfa_bytes = ((M + 127) / 128 + G) * 128 * p.sfa_ct * 4;
+    return launch_pair<false, true>(x_q, M, D, wg_q, (int64_t)G * H, D, sfa_bytes, (int64_t)G * p.sfb_estride, p, bound,
+                                    st, nullptr, wu_q);
 }
 
 extern "C" mxfp8_status_t mxfp8_grouped_mm_dgrad2(const void* dout1_q, const void* dout1_s, const void* wt1_q,
