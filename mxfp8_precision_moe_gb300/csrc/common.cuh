@@ -62,6 +62,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// SwiGLU backward of one bf16 pair, elementwise at the rounding points of the bf16 autograd ops, fp32
+// inside: g = dh, x = h1, u = h3 of h = silu(h1) * h3 with sig = 1 / (1 + e^-h1):
+//   dh3 = bf16(dh * bf16(silu(h1))),  dh1 = bf16(bf16(dh * h3) * sig * (1 + h1 * (1 - sig))).
+__device__ __forceinline__ void swiglu_bwd_pair(uint32_t g, uint32_t x, uint32_t u, uint32_t& dh1, uint32_t& dh3) {
+    const float g0 = bf16lo(g), g1 = bf16hi(g);
+    const float x0 = bf16lo(x), x1 = bf16hi(x);
+    const float sg0 = 1.0f / (1.0f + expf(-x0)), sg1 = 1.0f / (1.0f + expf(-x1));
+    const uint32_t sl = pack_bf16x2(x0 * sg0, x1 * sg1);              // bf16(silu(h1))
+    const uint32_t ds = pack_bf16x2(g0 * bf16lo(u), g1 * bf16hi(u));  // bf16(dh * h3)
+    dh3 = pack_bf16x2(g0 * bf16lo(sl), g1 * bf16hi(sl));
+    dh1 = pack_bf16x2(bf16lo(ds) * sg0 * (1.0f + x0 * (1.0f - sg0)), bf16hi(ds) * sg1 * (1.0f + x1 * (1.0f - sg1)));
+}
+
 // max over the two 16-bit halves (unsigned), one instruction on sm_90+.
 __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
     uint32_t d;

@@ -227,11 +227,87 @@ __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float f) { return cvt
 // release() hands the accumulator back once it is in registers.  a_row: the tile's first token row;
 // valid_rows / valid_cols: rows inside the group and columns inside H; prow0: the padded (128-aligned per
 // group) row of the tile's first row; col0: its first column; ct_T: column tiles of the h^T scales.
+// Row-wise and (if qT) token-wise MXFP8 quantization of one 32 x 32 bf16 block held by a warp: lane l owns
+// row 32 * quarter + l of a 128-row tile, w[i] its columns c0 + 2i, c0 + 2i + 1.  Row-wise: codes into
+// q [rows, H], scale bytes into the blocked row-group layout s (s_ct column tiles of 128); token-wise: the
+// block's 32 tokens of each column are one block, codes into qT [H, M] (transposed through the warp's 1 KB
+// stg), scale bytes into the blocked token-group layout sT (ct_T column tiles).  a_row: the tile's first
+// token row; valid_rows: its rows inside the group (group sizes are multiples of 32 where qT is given);
+// prow0: the padded (128-aligned per group) row of its first row.  Blocks past H write padding (0) up to
+// the layouts' 128-column round-up and nothing beyond it.
+__device__ __forceinline__ void quant_block_rowcol(const uint32_t (&w)[16], uint8_t* q, uint8_t* s, int64_t s_ct,
+                                                   uint8_t* qT, uint8_t* sT, int64_t H, int64_t M, int64_t ct_T,
+                                                   int quarter, int lane, uint8_t* stg, int64_t a_row, int valid_rows,
+                                                   int64_t prow0, int64_t c0) {
+    if ((c0 >> 7) >= s_ct) return;
+    const int r = quarter * 32 + lane;
+    const bool bvalid = c0 < H;          // this column block lies inside H
+    const bool rvalid = r < valid_rows;  // this row lies inside the group
+    const int64_t row = a_row + r;
+    // row-wise: this thread's 32 elements are one block -> 32 codes and one scale byte
+    {
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = vmax_u16x2(m, w[i] & 0x7FFF7FFFu);
+        const uint32_t sc = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
+        const float f = inv_scale_from_e8m0(sc);
+        uint32_t codes[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            codes[i] = sc == 0xFFu ? nonfinite_codes2(w[2 * i]) | (nonfinite_codes2(w[2 * i + 1]) << 16)
+                                   : quant_pair(w[2 * i], f) | (quant_pair(w[2 * i + 1], f) << 16);
+        if (bvalid && rvalid) {
+            uint4* gq = reinterpret_cast<uint4*>(q + row * H + c0);
+            gq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            gq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        }
+        // the tile's row scales are one 512-byte blocked tile: row r -> (r%32)*16 + (r/32)*4,
+        // block (c0 / 32) % 4 -> that byte; rows past the group and blocks past H are padding (0)
+        s[((prow0 >> 7) * s_ct + (c0 >> 7)) * 512 + lane * 16 + quarter * 4 + ((c0 >> 5) & 3)] =
+            (uint8_t)((bvalid && rvalid) ? sc : 0u);
+    }
+    if (qT != nullptr) {
+        // group sizes are multiples of 32 here (device-checked), so the warp's 32 rows are
+        // either all inside the group or all padding
+        const int64_t cq = prow0 / 32 + quarter;  // scale column of this 32-token block
+        uint32_t my_s = 0;                          // scale of column c0 + lane
+        if (valid_rows > quarter * 32 && bvalid) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t x = w[i];
+                const uint32_t slo = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, x & 0x7FFFu));
+                const uint32_t shi = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, (x >> 16) & 0x7FFFu));
+                uint32_t c2 = cvt_e4m3x2(bf16lo(x) * inv_scale_from_e8m0(slo),
+                                         bf16hi(x) * inv_scale_from_e8m0(shi));
+                if (slo == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu | ((x >> 8) & 0x80u);
+                if (shi == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u | ((x >> 16) & 0x8000u);
+                // transpose through shared memory: byte (column c, token lane) at c*32 + lane
+                st_shared_u8(stg + (2 * i) * 32 + lane, c2 & 0xFFu);
+                st_shared_u8(stg + (2 * i + 1) * 32 + lane, c2 >> 8);
+                my_s = lane == 2 * i ? slo : (lane == 2 * i + 1 ? shi : my_s);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int cc = 16 * h2 + (lane >> 1);  // column within the block
+                const uint4 val = ld_shared_v4(stg + cc * 32 + (lane & 1) * 16);
+                if (c0 + cc < H)
+                    *reinterpret_cast<uint4*>(qT + (c0 + cc) * M + a_row + quarter * 32 +
+                                              (lane & 1) * 16) = val;
+            }
+            __syncwarp();
+            if (c0 + lane >= H) my_s = 0;
+        }
+        const int64_t cH = c0 + lane;  // row of h^T (columns past H: padding 0)
+        sT[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] =
+            (uint8_t)my_s;
+    }
+}
+
 template <class Release>
 __device__ __forceinline__ void swiglu_tile_epilogue(const GemmParams& p, uint32_t acc, int quarter, int jb, int lane,
                                                      uint8_t* stg, int64_t a_row, int valid_rows, int valid_cols,
                                                      int64_t prow0, int64_t col0, int64_t ct_T, Release release) {
-    const int r = quarter * 32 + lane;  // accumulator row (= tensor-memory lane) of this thread
     const int64_t H = p.nb;
     uint32_t hg[16], hu[16];  // bf16 pairs (columns 2i, 2i+1 of the block) of h1 and h3
     {
@@ -249,11 +325,8 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const GemmParams& p, uint32
     __syncwarp();
     release();
 
-    const int vcols = valid_cols;
-    const bool bvalid = 32 * jb < vcols;            // this column block lies inside H
-    const bool rvalid = r < valid_rows;          // this row lies inside the group
-    const int64_t row = a_row + r;
-    const int64_t c0 = col0 + 32 * jb;           // first column of the block
+    const bool bvalid = 32 * jb < valid_cols;  // this column block lies inside H
+    const int64_t c0 = col0 + 32 * jb;         // first column of the block
     // h1 and h3 through the warp's 1 KB staging buffer, 16 columns (32 bytes) of each of the
     // 32 rows per pass, so every store instruction writes 16 whole 32-byte row segments
     // instead of 32 scattered 16-byte pieces.  Chunk c of row l sits at l * 32 + 16 (c ^ s),
@@ -282,64 +355,8 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const GemmParams& p, uint32
         const uint32_t sl = pack_bf16x2(a / (1.0f + expf(-a)), b / (1.0f + expf(-b)));
         hg[i] = pack_bf16x2(bf16lo(sl) * bf16lo(hu[i]), bf16hi(sl) * bf16hi(hu[i]));
     }
-    // row-wise: this thread's 32 elements are one block -> 32 codes and one scale byte
-    {
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = vmax_u16x2(m, hg[i] & 0x7FFF7FFFu);
-        const uint32_t sc = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
-        const float f = inv_scale_from_e8m0(sc);
-        uint32_t codes[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            codes[i] = sc == 0xFFu ? nonfinite_codes2(hg[2 * i]) | (nonfinite_codes2(hg[2 * i + 1]) << 16)
-                                   : quant_pair(hg[2 * i], f) | (quant_pair(hg[2 * i + 1], f) << 16);
-        if (bvalid && rvalid) {
-            uint4* gq = reinterpret_cast<uint4*>(p.hq + row * H + c0);
-            gq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-            gq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-        }
-        // the tile's row scales are one 512-byte blocked tile: row r -> (r%32)*16 + (r/32)*4,
-        // block jb -> byte jb; rows past the group and blocks past H are padding (0)
-        p.hs[((prow0 >> 7) * p.hs_ct + (col0 >> 7)) * 512 + lane * 16 + quarter * 4 + jb] =
-            (uint8_t)((bvalid && rvalid) ? sc : 0u);
-    }
-    if (p.hTq != nullptr) {
-        // group sizes are multiples of 32 here (device-checked), so the warp's 32 rows are
-        // either all inside the group or all padding
-        const int64_t cq = prow0 / 32 + quarter;  // scale column of this 32-token block
-        uint32_t my_s = 0;                          // scale of column c0 + lane
-        if (valid_rows > quarter * 32 && bvalid) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t w = hg[i];
-                const uint32_t slo = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, w & 0x7FFFu));
-                const uint32_t shi = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, (w >> 16) & 0x7FFFu));
-                uint32_t c2 = cvt_e4m3x2(bf16lo(w) * inv_scale_from_e8m0(slo),
-                                         bf16hi(w) * inv_scale_from_e8m0(shi));
-                if (slo == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu | ((w >> 8) & 0x80u);
-                if (shi == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u | ((w >> 16) & 0x8000u);
-                // transpose through shared memory: byte (column c, token lane) at c*32 + lane
-                st_shared_u8(stg + (2 * i) * 32 + lane, c2 & 0xFFu);
-                st_shared_u8(stg + (2 * i + 1) * 32 + lane, c2 >> 8);
-                my_s = lane == 2 * i ? slo : (lane == 2 * i + 1 ? shi : my_s);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int cc = 16 * h2 + (lane >> 1);  // column within the block
-                const uint4 val = ld_shared_v4(stg + cc * 32 + (lane & 1) * 16);
-                if (32 * jb + cc < vcols)
-                    *reinterpret_cast<uint4*>(p.hTq + (c0 + cc) * p.M + a_row + quarter * 32 +
-                                              (lane & 1) * 16) = val;
-            }
-            __syncwarp();
-            if (32 * jb + lane >= vcols) my_s = 0;
-        }
-        const int64_t cH = c0 + lane;  // row of h^T (columns past H: padding 0)
-        p.hTs[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] =
-            (uint8_t)my_s;
-    }
+    quant_block_rowcol(hg, p.hq, p.hs, p.hs_ct, p.hTq, p.hTs, H, p.M, ct_T, quarter, lane, stg, a_row, valid_rows,
+                       prow0, c0);
 }
 
 template <int BN, bool kDualK = false>

@@ -981,14 +981,9 @@ __global__ void __launch_bounds__(kQThreadsOf<kMode>, 2)
             for (int rr = 0; rr < 8; ++rr)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float g0 = bf16lo(v[rr][k]), g1 = bf16hi(v[rr][k]);
-                    const float x0 = bf16lo(a[rr][k]), x1 = bf16hi(a[rr][k]);
-                    const float sg0 = 1.0f / (1.0f + expf(-x0)), sg1 = 1.0f / (1.0f + expf(-x1));
-                    const uint32_t sl = pack_bf16x2(x0 * sg0, x1 * sg1);                 // bf16(silu(h1))
-                    const uint32_t d3 = pack_bf16x2(g0 * bf16lo(sl), g1 * bf16hi(sl));   // dh3
-                    const uint32_t ds = pack_bf16x2(g0 * bf16lo(u3[rr][k]), g1 * bf16hi(u3[rr][k]));  // dh * h3
-                    a[rr][k] = pack_bf16x2(bf16lo(ds) * sg0 * (1.0f + x0 * (1.0f - sg0)),
-                                           bf16hi(ds) * sg1 * (1.0f + x1 * (1.0f - sg1)));     // dh1
+                    uint32_t d1, d3;
+                    swiglu_bwd_pair(v[rr][k], a[rr][k], u3[rr][k], d1, d3);
+                    a[rr][k] = d1;
                     u3[rr][k] = d3;
                 }
             quant_rowcol(a, p.q_row, p.s_row, p.q_col, p.s_col);
