@@ -73,7 +73,7 @@ CONFIG_NAMES = {"tiny": "C1", "scout": "C2", "swiglu": "C3", "imbalanced": "C4"}
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernel of the
 # SwiGLU step, from a one-pass ncu capture of this command, valid only while the GEMM sources hash
 # to the recorded value (the kernel is then unchanged since the counters were taken).
-DOMINANT_TRAFFIC = {"kernel": "grouped_mm_pair_kernel", "bytes_per_launch": 3090384794, "src_sha": "0a63957b1f38f08f"}
+DOMINANT_TRAFFIC = {"kernel": "grouped_mm_pair_kernel", "bytes_per_launch": 3084558387, "src_sha": "ba849a9615cf1fdb"}
 
 
 def kernel_src_sha() -> str:
@@ -953,13 +953,17 @@ def run_e2e(make_step, step, stream, world, device, n_steps: int):
         s_in.wait_stream(s_out)
         return ev
 
-    # untimed warm-up: both buffer sets through the whole pipeline, copies included (the first DMA to
-    # fresh pinned pages has been seen to run far below the link's rate)
+    # untimed warm-up: both buffer sets through the whole pipeline, copies included (the first copies of
+    # a run, after the device had gone idle, have been seen at a tenth of the link's rate)
     pipeline(4)
-    torch.cuda.synchronize()
     if world > 1:
+        torch.cuda.synchronize()
         torch.distributed.barrier()
+    # one GPU: the timed steps follow the warm-up with no idle gap; x0 marks the end of every warm-up
+    # operation in stream order, and the timed copies start after it
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_in.wait_stream(stream)
+    s_in.wait_stream(s_out)
     x0.record(s_in)
     host0 = time.perf_counter()
     ev = pipeline(n_steps)

@@ -18,7 +18,7 @@ __global__ void wait_timeout_probe_kernel(int32_t* dev_status, uint64_t limit_ns
         fence_barrier_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, limit_ns, &abort_flag, dev_status);
+    if (threadIdx.x == 0) mbar_wait_bounded<true>(&bar, 0, limit_ns, &abort_flag, dev_status);
     __syncthreads();
 }
 

@@ -126,6 +126,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same with a suspend-time hint: a thread whose phase has not completed sleeps until it completes
+// or kSuspendNs pass, instead of re-polling.  In the GEMM kernels the waiting epilogue warps then leave
+// the issue slots to the producer, MMA and scale-copy threads (3-6% faster GEMMs, identical outputs).
+// The quantize kernels keep the default wait: their stages turn over every few microseconds, and the
+// folded-producer stability kernels ran up to 28% slower with the hint.
+constexpr uint32_t kSuspendNs = 1000000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -135,14 +154,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Bounded wait on an mbarrier phase.  Returns false (after recording
 // MXFP8_ERR_TIMEOUT) once `limit_ns` of wall time has passed, or at once when
 // another role of the CTA has already given up (*abort != 0).  Never traps.
+// kSleep: wait with the suspend-time hint (mbar_try_wait_sleep).
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                                   volatile int* abort, int32_t* dev_status) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_wait = [&] { return kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity); };
+    if (try_wait()) return true;
     const uint64_t t0 = globaltimer_ns();
     uint32_t spins = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (((++spins) & 63u) == 0) {
+        if (try_wait()) return true;
+        // a failed sleeping wait has already slept up to kSuspendNs: check on every one of those
+        if (kSleep || ((++spins) & 63u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;

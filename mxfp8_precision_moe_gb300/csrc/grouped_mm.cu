@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const TileInfo ti = tile_info<BN, kDualK>(p, t, ends_s, pstart_s, ptotal);
                 const int kt_half = kDualK ? ti.k_tiles / 2 : ti.k_tiles;
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
+                    if (!mbar_wait_bounded<true>(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int s = 0; s < C::kStages; ++s)
                     if (issued_mask & (1u << s)) {
                         volatile int no_abort = 0;
-                        mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, p.timeout_ns, &no_abort, nullptr);
+                        mbar_wait_bounded<true>(&full[s], (last_phase >> s) & 1u, p.timeout_ns, &no_abort, nullptr);
                     }
             }
         } else if (warp == 1 && lane == 0) {
@@ -514,16 +514,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const TileInfo ti = tile_info<BN, kDualK>(p, t, ends_s, pstart_s, ptotal);
                 if (ti.k_tiles == 0) continue;
-                if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
+                if (!mbar_wait_bounded<true>(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + acc * BN;
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     const int cur = stage;
-                    if (!mbar_wait_bounded(&full[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    if (!mbar_wait_bounded<true>(&full[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
-                    if (!mbar_wait_bounded(&sfull[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    if (!mbar_wait_bounded<true>(&sfull[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // all tensor-core work of this CTA must be done before the columns are freed
             tc_commit(drain);
             volatile int no_abort = 0;
-            mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
+            mbar_wait_bounded<true>(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
         } else if (warp == kSfWarp) {
             // ------------------------------------------------ scale copies
             // As soon as a stage lands, its scale tiles go to that stage's tensor-memory columns
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                     const TileInfo ti = tile_info<BN, kDualK>(p, t, ends_s, pstart_s, ptotal);
                     for (int kt = 0; kt < ti.k_tiles; ++kt) {
-                        if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                        if (!mbar_wait_bounded<true>(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                             ok = false;
                             break;
                         }
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this thread's copies complete before the columns are freed
                 tc_commit(sfdrain);
                 volatile int no_abort = 0;
-                mbar_wait_bounded(sfdrain, 0, p.timeout_ns, &no_abort, p.dev_status);
+                mbar_wait_bounded<true>(sfdrain, 0, p.timeout_ns, &no_abort, p.dev_status);
             }
         } else if (warp >= 2) {
           {
@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
                     continue;
                 }
-                if (!mbar_wait_bounded(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+                if (!mbar_wait_bounded<true>(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
                 // Drain the whole accumulator row into registers as bf16 pairs, then hand the
                 // columns back to the MMA warp before any global store is issued.
@@ -973,7 +973,7 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
                 const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 bool ok = true;
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
+                    if (!mbar_wait_bounded<true>(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
@@ -1009,15 +1009,15 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
                 if (t >= ntiles) continue;
                 const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                 if (ti.k_tiles == 0) continue;
-                if (!mbar_wait_bounded(tempty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
+                if (!mbar_wait_bounded<true>(tempty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) break;
                 tc_fence_after();
                 for (int kt = 0; kt < ti.k_tiles; ++kt) {
                     const int cur = stage;
-                    if (!mbar_wait_bounded(&full[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    if (!mbar_wait_bounded<true>(&full[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
-                    if (!mbar_wait_bounded(&sfull[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    if (!mbar_wait_bounded<true>(&sfull[cur], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
                     }
@@ -1054,7 +1054,7 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
             }
             tc_commit_pair(drain, 0x1);
             volatile int no_abort = 0;
-            mbar_wait_bounded(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
+            mbar_wait_bounded<true>(drain, 0, p.timeout_ns, &no_abort, p.dev_status);
         } else if (warp == kPairSfWarpOf<kSwi>) {
             // ------------------------------------------------ scale copies (even CTA only)
             // Each landed stage's scale tiles go to its tensor-memory columns in both CTAs (the
@@ -1068,7 +1068,7 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
                     if (t >= ntiles) continue;
                     const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
                     for (int kt = 0; kt < ti.k_tiles; ++kt) {
-                        if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                        if (!mbar_wait_bounded<true>(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                             ok = false;
                             break;
                         }
@@ -1086,7 +1086,7 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
                 }
                 tc_commit_pair(sfdrain, 0x1);
                 volatile int no_abort = 0;
-                mbar_wait_bounded(sfdrain, 0, p.timeout_ns, &no_abort, p.dev_status);
+                mbar_wait_bounded<true>(sfdrain, 0, p.timeout_ns, &no_abort, p.dev_status);
             }
         } else if (warp >= 2 && kSwi) {
             // ------------------------------------------------ SwiGLU epilogue (both CTAs: own 128 rows)
@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
                 const int64_t t = tile_at(j);
                 if (t >= ntiles) continue;
                 const PairTile ti = pair_tile<kDualK, kSwi>(p, t, half, ends_s, pstart_s, tstart_s, ptotal, gorder_s, sorted);
-                if (!mbar_wait_bounded(tfull, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+                if (!mbar_wait_bounded<true>(tfull, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
                 acc_phase ^= 1u;
                 tc_fence_after();
                 auto release = [&] { if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader); };
@@ -1138,7 +1138,7 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
                                 *reinterpret_cast<uint4*>(wout + (int64_t)rl * ti.ldo + c) = make_uint4(0, 0, 0, 0);
                     continue;
                 }
-                if (!mbar_wait_bounded(tfull, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+                if (!mbar_wait_bounded<true>(tfull, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
                 acc_phase ^= 1u;
                 tc_fence_after();
                 uint32_t packed[kHalfCols / 2];
