@@ -227,14 +227,62 @@ __device__ __forceinline__ uint32_t quant_pair(uint32_t v, float f) { return cvt
 // release() hands the accumulator back once it is in registers.  a_row: the tile's first token row;
 // valid_rows / valid_cols: rows inside the group and columns inside H; prow0: the padded (128-aligned per
 // group) row of the tile's first row; col0: its first column; ct_T: column tiles of the h^T scales.
+__device__ __forceinline__ void st_shared_u32(void* p, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// Largest magnitude of each half of two bf16 pairs, NaN winning (the sign bits left are not used).
+__device__ __forceinline__ uint32_t amax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// 32 bf16 values (16 pairs) -> their MXFP8 block: the E8M0 scale byte s from the amax's exponent field
+// and, in c[8], the 32 E4M3 codes (RNE, satfinite) of x * 2^(127 - s).  The products come from one
+// mixed-precision fma per element with the scale as a bf16 (exact, and zero keeps its sign); a block
+// whose amax is Inf or NaN gets scale 0xFF and the codes 0x7F with each element's sign.
+__device__ __forceinline__ uint32_t mx_block32(const uint32_t (&w)[16], uint32_t (&c)[8]) {
+    uint32_t m = w[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) m = amax_bf16x2(m, w[i]);
+    const uint32_t sc = e8m0_from_absbits(max(m & 0x7FFFu, (m >> 16) & 0x7FFFu));
+    const uint32_t f2 = (254u - sc) << 7;  // 2^(127 - sc) as a bf16 (sc <= 246 for a finite amax)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t pr[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float lo, hi;
+            asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+                "fma.rn.f32.bf16 %0, a0, b0, 0f80000000;\n\tfma.rn.f32.bf16 %1, a1, b0, 0f80000000;\n\t}"
+                : "=f"(lo), "=f"(hi)
+                : "r"(w[2 * i + h]), "r"(f2));
+            pr[h] = cvt_e4m3x2(lo, hi);
+        }
+        c[i] = pr[0] | (pr[1] << 16);
+    }
+    if (sc == 0xFFu) {  // a non-finite block (rare): the codes are 0x7F with each element's sign
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = nonfinite_codes2(w[2 * i]) | (nonfinite_codes2(w[2 * i + 1]) << 16);
+    }
+    return sc;
+}
+
 // Row-wise and (if qT) token-wise MXFP8 quantization of one 32 x 32 bf16 block held by a warp: lane l owns
 // row 32 * quarter + l of a 128-row tile, w[i] its columns c0 + 2i, c0 + 2i + 1.  Row-wise: codes into
 // q [rows, H], scale bytes into the blocked row-group layout s (s_ct column tiles of 128); token-wise: the
-// block's 32 tokens of each column are one block, codes into qT [H, M] (transposed through the warp's 1 KB
-// stg), scale bytes into the blocked token-group layout sT (ct_T column tiles).  a_row: the tile's first
-// token row; valid_rows: its rows inside the group (group sizes are multiples of 32 where qT is given);
-// prow0: the padded (128-aligned per group) row of its first row.  Blocks past H write padding (0) up to
-// the layouts' 128-column round-up and nothing beyond it.
+// block's 32 tokens of each column are one block, codes into qT [H, M], scale bytes into the blocked
+// token-group layout sT (ct_T column tiles).  stg: the warp's 2 KB of shared memory, through which the
+// block is transposed (word (pair p, row r) at p * 32 + (r ^ p): conflict-free both ways).  a_row: the
+// tile's first token row; valid_rows: its rows inside the group (group sizes are multiples of 32 where
+// qT is given); prow0: the padded (128-aligned per group) row of its first row.  Blocks past H write
+// padding (0) up to the layouts' 128-column round-up and nothing beyond it.
 __device__ __forceinline__ void quant_block_rowcol(const uint32_t (&w)[16], uint8_t* q, uint8_t* s, int64_t s_ct,
                                                    uint8_t* qT, uint8_t* sT, int64_t H, int64_t M, int64_t ct_T,
                                                    int quarter, int lane, uint8_t* stg, int64_t a_row, int valid_rows,
@@ -243,21 +291,12 @@ __device__ __forceinline__ void quant_block_rowcol(const uint32_t (&w)[16], uint
     const int r = quarter * 32 + lane;
     const bool bvalid = c0 < H;          // this column block lies inside H
     const bool rvalid = r < valid_rows;  // this row lies inside the group
-    const int64_t row = a_row + r;
     // row-wise: this thread's 32 elements are one block -> 32 codes and one scale byte
     {
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = vmax_u16x2(m, w[i] & 0x7FFF7FFFu);
-        const uint32_t sc = e8m0_from_absbits(max(m & 0xFFFFu, m >> 16));
-        const float f = inv_scale_from_e8m0(sc);
         uint32_t codes[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            codes[i] = sc == 0xFFu ? nonfinite_codes2(w[2 * i]) | (nonfinite_codes2(w[2 * i + 1]) << 16)
-                                   : quant_pair(w[2 * i], f) | (quant_pair(w[2 * i + 1], f) << 16);
+        const uint32_t sc = mx_block32(w, codes);
         if (bvalid && rvalid) {
-            uint4* gq = reinterpret_cast<uint4*>(q + row * H + c0);
+            uint4* gq = reinterpret_cast<uint4*>(q + (a_row + r) * H + c0);
             gq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
             gq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
         }
@@ -267,40 +306,37 @@ __device__ __forceinline__ void quant_block_rowcol(const uint32_t (&w)[16], uint
             (uint8_t)((bvalid && rvalid) ? sc : 0u);
     }
     if (qT != nullptr) {
-        // group sizes are multiples of 32 here (device-checked), so the warp's 32 rows are
-        // either all inside the group or all padding
-        const int64_t cq = prow0 / 32 + quarter;  // scale column of this 32-token block
-        uint32_t my_s = 0;                          // scale of column c0 + lane
-        if (valid_rows > quarter * 32 && bvalid) {
+        // token-wise: lane t takes column c0 + t, whose 32 tokens (the warp's rows) are one block.
+        // Group sizes are multiples of 32 here (device-checked), so the warp's rows are all inside the
+        // group or all padding.
+        const bool cvalid = c0 + lane < H && valid_rows > quarter * 32;
+        uint32_t sc = 0;
+        if (bvalid && valid_rows > quarter * 32) {
+#pragma unroll
+            for (int p2 = 0; p2 < 16; ++p2) st_shared_u32(stg + 4 * (p2 * 32 + (lane ^ p2)), w[p2]);
+            __syncwarp();
+            const int pc = lane >> 1;  // the pair that holds column c0 + lane
+            uint32_t tw[16];           // its tokens 2i, 2i + 1 as bf16 pairs
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const uint32_t x = w[i];
-                const uint32_t slo = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, x & 0x7FFFu));
-                const uint32_t shi = e8m0_from_absbits(__reduce_max_sync(0xffffffffu, (x >> 16) & 0x7FFFu));
-                uint32_t c2 = cvt_e4m3x2(bf16lo(x) * inv_scale_from_e8m0(slo),
-                                         bf16hi(x) * inv_scale_from_e8m0(shi));
-                if (slo == 0xFFu) c2 = (c2 & 0xFF00u) | 0x7Fu | ((x >> 8) & 0x80u);
-                if (shi == 0xFFu) c2 = (c2 & 0x00FFu) | 0x7F00u | ((x >> 16) & 0x8000u);
-                // transpose through shared memory: byte (column c, token lane) at c*32 + lane
-                st_shared_u8(stg + (2 * i) * 32 + lane, c2 & 0xFFu);
-                st_shared_u8(stg + (2 * i + 1) * 32 + lane, c2 >> 8);
-                my_s = lane == 2 * i ? slo : (lane == 2 * i + 1 ? shi : my_s);
+                const uint32_t x0 = ld_shared_u32(stg + 4 * (pc * 32 + ((2 * i) ^ pc)));
+                const uint32_t x1 = ld_shared_u32(stg + 4 * (pc * 32 + ((2 * i + 1) ^ pc)));
+                tw[i] = __byte_perm(x0, x1, (lane & 1) ? 0x7632u : 0x5410u);
             }
             __syncwarp();
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int cc = 16 * h2 + (lane >> 1);  // column within the block
-                const uint4 val = ld_shared_v4(stg + cc * 32 + (lane & 1) * 16);
-                if (c0 + cc < H)
-                    *reinterpret_cast<uint4*>(qT + (c0 + cc) * M + a_row + quarter * 32 +
-                                              (lane & 1) * 16) = val;
+            uint32_t codes[8];
+            sc = mx_block32(tw, codes);
+            if (cvalid) {
+                uint4* gq = reinterpret_cast<uint4*>(qT + (c0 + lane) * M + a_row + quarter * 32);
+                gq[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+                gq[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+            } else {
+                sc = 0;
             }
-            __syncwarp();
-            if (c0 + lane >= H) my_s = 0;
         }
-        const int64_t cH = c0 + lane;  // row of h^T (columns past H: padding 0)
-        sT[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] =
-            (uint8_t)my_s;
+        const int64_t cq = prow0 / 32 + quarter;  // scale column of this 32-token block
+        const int64_t cH = c0 + lane;             // row of h^T (columns past H: padding 0)
+        sT[((cH >> 7) * ct_T + (cq >> 2)) * 512 + (cH & 31) * 16 + ((cH >> 5) & 3) * 4 + (cq & 3)] = (uint8_t)sc;
     }
 }
 
@@ -1092,7 +1128,7 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
             // ------------------------------------------------ SwiGLU epilogue (both CTAs: own 128 rows)
             const int quarter = warp & 3;
             const int jb = (warp - 2) >> 2;  // 32-column block of h of this warp
-            uint8_t* stg = smem + C::kOffStage + (warp - 2) * 1024;
+            uint8_t* stg = smem + C::kOffStage + (warp - 2) * 2048;  // 2 KB a warp (16 warps: 32 KB)
             const int64_t ct_T = ptotal / 128;
             const uint32_t tempty_leader = cluster_addr(tempty, 0);
             uint32_t acc_phase = 0;
