@@ -721,7 +721,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // gate/up (a 128-column tile of h; the even CTA stages gate rows, the odd CTA the same up rows,
 // and each CTA's 16 epilogue warps turn its own 128 token rows into h1, h3 and quantized h).
 // ============================================================================================
-constexpr int kPairStages = 5;
 constexpr int kSortGroups = 128;  // K-grouped schedules rank at most this many groups (O(G^2) per CTA)
 // Epilogue warps of the pair kernel: two per tensor-memory lane quarter, each draining one 128-column
 // half of the accumulator, so the single accumulator is handed back to the MMA warp in half the time
@@ -740,9 +739,13 @@ constexpr int kThreadsPairOf = 96 + 32 * kPairEpiOf<kSwi>;
 // 8 A and 10 B operand slabs instead of 16 and 5 (a long group's slabs do not fit in L2 together).
 constexpr int kBandPairK = 8;
 
+// Operand stages: the plain and two-operand kernels stage their epilogue through 1 KB a warp, which
+// leaves room in shared memory for six; the SwiGLU kernel's 16 epilogue warps stage 2 KB each and it
+// keeps five.
+template <bool kSwi>
 struct CfgPair {
     static constexpr int BN = 256;
-    static constexpr int kStages = kPairStages;
+    static constexpr int kStages = kSwi ? 5 : 6;
     static constexpr int kABytes = BM * BK;          // this CTA's 128 rows of A
     static constexpr int kBBytes = 128 * BK;         // this CTA's 128 rows of B
     static constexpr int kSfaBytes = 512;
@@ -756,11 +759,15 @@ struct CfgPair {
     static constexpr int kOffSfa = kOffB + kStages * kBBytes;
     static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
     static constexpr int kOffStage = kOffSfb + kStages * kSfbBytes;
-    static constexpr int kStageBytes = kPairEpiWarps * 32 * 128;
+    static constexpr int kStageBytes = kSwi ? kPairSwiEpiWarps * 2048 : kPairEpiWarps * 1024;
     static constexpr int kOffBar = kOffStage + kStageBytes;
     static constexpr int kBarBytes = (3 * kStages + 2 + 2) * 8 + 16;
     static constexpr int kSmem = kOffBar + kBarBytes + 1024;
 };
+static_assert(CfgPair<false>::kSmem + 3 * MXFP8_MAX_GROUPS * 4 + kSortGroups * 4 + 16 <= 227 * 1024,
+              "pair kernel shared memory");
+static_assert(CfgPair<true>::kSmem + 3 * MXFP8_MAX_GROUPS * 4 + kSortGroups * 4 + 16 <= 227 * 1024,
+              "pair kernel shared memory");
 
 struct PairTile {
     int g;
@@ -858,13 +865,13 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
                            const __grid_constant__ CUtensorMap tmap_a2, const __grid_constant__ CUtensorMap tmap_b2,
                            const __grid_constant__ CUtensorMap tmap_sfa2, const __grid_constant__ CUtensorMap tmap_sfb2,
                            const GemmParams p) {
-    using C = CfgPair;
+    using C = CfgPair<kSwi>;
     constexpr int BN = 256;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int32_t ends_s[kMaxGroups];
     __shared__ int32_t pstart_s[kMaxGroups];
     __shared__ int32_t tstart_s[kMaxGroups];  // ROWGROUPED: first pair tile (256 rows) of each group
-    __shared__ int32_t gorder_s[kMaxGroups];  // K-grouped, G <= kSortGroups: groups by size, largest first
+    __shared__ int32_t gorder_s[kSortGroups];  // K-grouped, G <= kSortGroups: groups by size, largest first
     __shared__ int32_t ptotal_s;
     __shared__ int32_t bad_s;
     __shared__ uint32_t tmem_base_s;
@@ -1157,7 +1164,7 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
             constexpr int kHalfCols = BN / 2;
             const int quarter = warp & 3;
             const int c_base = ((warp - 2) >> 2) * kHalfCols;
-            uint8_t* stg = smem + C::kOffStage + (warp - 2) * (32 * 128);
+            uint8_t* stg = smem + C::kOffStage + (warp - 2) * 1024;  // 32 rows x 32 bytes
             const uint32_t tempty_leader = cluster_addr(tempty, 0);
             uint32_t acc_phase = 0;
             for (int64_t j = 0; j * ncl < ntiles; ++j) {
@@ -1194,21 +1201,24 @@ __global__ void __launch_bounds__(kThreadsPairOf<kSwi>, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+                // 16 columns a pass: lane = row writes its two 16-byte pieces (the piece order flips every
+                // 4 rows, so each 8-lane phase covers all 32 banks), then two lanes a row store whole
+                // 32-byte sectors of 16 rows per instruction.
 #pragma unroll
-                for (int ch = 0; ch < kHalfCols / 64; ++ch) {
-                    if (ch * 64 >= vcols) break;
+                for (int ch = 0; ch < kHalfCols / 16; ++ch) {
+                    if (ch * 16 >= vcols) break;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) * 16),
-                                     make_uint4(packed[ch * 32 + 4 * j], packed[ch * 32 + 4 * j + 1],
-                                                packed[ch * 32 + 4 * j + 2], packed[ch * 32 + 4 * j + 3]));
+                    for (int j = 0; j < 2; ++j)
+                        st_shared_v4(stg + lane * 32 + ((j ^ ((lane >> 2) & 1)) * 16),
+                                     make_uint4(packed[ch * 8 + 4 * j], packed[ch * 8 + 4 * j + 1],
+                                                packed[ch * 8 + 4 * j + 2], packed[ch * 8 + 4 * j + 3]));
                     __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int rl = (lane >> 3) + 4 * i, piece = lane & 7;
-                        const uint4 val = ld_shared_v4(stg + rl * 128 + ((piece ^ (rl & 7)) * 16));
-                        if (rl < vrows && ch * 64 + piece * 8 < vcols)
-                            *reinterpret_cast<uint4*>(wout + (int64_t)rl * ti.ldo + ch * 64 + piece * 8) = val;
+                    for (int i = 0; i < 2; ++i) {
+                        const int rl = (lane >> 1) + 16 * i, piece = lane & 1;
+                        const uint4 val = ld_shared_v4(stg + rl * 32 + ((piece ^ ((rl >> 2) & 1)) * 16));
+                        if (rl < vrows && ch * 16 + piece * 8 < vcols)
+                            *reinterpret_cast<uint4*>(wout + (int64_t)rl * ti.ldo + ch * 16 + piece * 8) = val;
                     }
                     __syncwarp();
                 }
@@ -1306,7 +1316,7 @@ static mxfp8_status_t launch_pair(const void* a, int64_t a_rows, int64_t a_cols,
                                   int64_t b_cols, int64_t sfa_bytes, int64_t sfb_bytes, GemmParams& p,
                                   int64_t pair_tiles_bound, cudaStream_t st, const void* a2 = nullptr,
                                   const void* b2 = nullptr) {
-    using C = CfgPair;
+    using C = CfgPair<kSwi>;
     CUtensorMap ma, mb, msa, msb, ma2, mb2, msa2, msb2;
     if (!make_map(&ma, a, a_rows, a_cols, BM) || !make_map(&mb, b, b_rows, b_cols, 128) ||
         !make_scale_map(&msa, p.sfa, sfa_bytes) || !make_scale_map(&msb, p.sfb, sfb_bytes))
